@@ -1,0 +1,194 @@
+"""Seeded synthetic inputs for the gpt-oss MoE layer.
+
+This module holds none of the layer's arithmetic: it draws seeded random
+numbers (``synth.c``, splitmix64 in counter mode, Box-Muller normals) and
+rounds them to the storage formats (bf16, MXFP4 codes and E8M0 block scales).
+The CPU oracle and the CUDA library are both fed from the buffers it fills.
+
+Workload recipes (shapes from the xserv page "Phase 19: gpt-oss-20b", §1
+model-architecture table: hidden 2880, 32 experts top-4, expert inter 2880;
+the 120b-shaped layer keeps the same widths with 128 experts):
+
+* expert and router weights ~ N(0, 0.02), biases ~ N(0, 0.01), activations
+  ~ N(0, 1), all rounded to bf16;
+* "hot experts": +2.0 added to the router bias of experts 0-3 (skewed load);
+* outliers: each activation element independently, with probability 0.01,
+  is multiplied by 20 before rounding;
+* MXFP4: e2m1 codes uniform over the 16 nibble values, two per byte, and one
+  E8M0 scale byte per 32 consecutive input elements with exponent uniform in
+  [-8, -4] (bytes 119..123).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libsynth.so")
+_lock = threading.Lock()
+_lib = None
+
+# Stream ids: one independent random stream per tensor.
+S_X, S_WR, S_BR, S_WGU, S_BGU, S_WD, S_BD = 1, 2, 3, 4, 5, 6, 7
+S_GU_CODES, S_GU_SCALES, S_D_CODES, S_D_SCALES = 8, 9, 10, 11
+
+
+def build(force: bool = False) -> str:
+    """Compile ``libsynth.so`` next to this file (gcc, OpenMP)."""
+    src = os.path.join(_HERE, "synth.c")
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared",
+                               "-ffp-contract=off", src, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
+            vp, sz, u64, d, u32 = (ctypes.c_void_p, ctypes.c_size_t,
+                                   ctypes.c_uint64, ctypes.c_double,
+                                   ctypes.c_uint32)
+            L.synth_normal_f32.argtypes = [vp, sz, u64, u64, d, d]
+            L.synth_normal_bf16.argtypes = [vp, sz, u64, u64, d, d, d, d]
+            L.synth_uniform_u8.argtypes = [vp, sz, u64, u64, u32, u32]
+            L.synth_round_bf16.argtypes = [vp, vp, sz]
+            L.synth_f32_to_bf16.argtypes = [ctypes.c_float]
+            L.synth_f32_to_bf16.restype = ctypes.c_uint16
+            _lib = L
+    return _lib
+
+
+def _empty(shape, dtype, pin):
+    return torch.empty(shape, dtype=dtype, pin_memory=pin)
+
+
+def normal_bf16(shape, seed, stream, mean=0.0, std=1.0, p_outlier=0.0,
+                outlier_scale=20.0, pin=False) -> torch.Tensor:
+    t = _empty(shape, torch.bfloat16, pin)
+    lib().synth_normal_bf16(t.data_ptr(), t.numel(), seed, stream, mean, std,
+                            p_outlier, outlier_scale)
+    return t
+
+
+def normal_f32(shape, seed, stream, mean=0.0, std=1.0, pin=False):
+    t = _empty(shape, torch.float32, pin)
+    lib().synth_normal_f32(t.data_ptr(), t.numel(), seed, stream, mean, std)
+    return t
+
+
+def uniform_u8(shape, seed, stream, lo, hi, pin=False) -> torch.Tensor:
+    t = _empty(shape, torch.uint8, pin)
+    lib().synth_uniform_u8(t.data_ptr(), t.numel(), seed, stream, lo, hi)
+    return t
+
+
+def round_bf16(t: torch.Tensor, pin=False) -> torch.Tensor:
+    t = t.contiguous().to(torch.float32)
+    out = _empty(tuple(t.shape), torch.bfloat16, pin)
+    lib().synth_round_bf16(t.data_ptr(), out.data_ptr(), t.numel())
+    return out
+
+
+@dataclass
+class Layer:
+    """Host copies of one MoE layer's inputs (torch CPU tensors).
+
+    bf16 tensors are ``torch.bfloat16``; MXFP4 codes and scales are
+    ``torch.uint8``.  ``w_gu`` rows alternate gate/up features (row 2j is
+    gate_j, row 2j+1 is up_j).
+    """
+    T: int
+    H: int
+    I: int
+    E: int
+    top_k: int
+    wfmt: str                      # "bf16" or "mxfp4"
+    x: torch.Tensor                # [T, H] bf16
+    wr: torch.Tensor               # [E, H] bf16
+    br: torch.Tensor               # [E] bf16
+    w_gu: torch.Tensor             # [E, 2I, H] bf16 | [E, 2I, H/2] u8
+    b_gu: torch.Tensor             # [E, 2I] bf16
+    w_d: torch.Tensor              # [E, H, I] bf16 | [E, H, I/2] u8
+    b_d: torch.Tensor              # [E, H] bf16
+    s_gu: Optional[torch.Tensor] = None   # [E, 2I, H/32] u8 (mxfp4)
+    s_d: Optional[torch.Tensor] = None    # [E, H, I/32] u8 (mxfp4)
+    meta: dict = field(default_factory=dict)
+
+
+def make_x(T, H, seed, p_outlier=0.0, outlier_scale=20.0, pin=False):
+    """Activations: element i of stream S_X, so a smaller T is a prefix."""
+    return normal_bf16((T, H), seed, S_X, 0.0, 1.0, p_outlier, outlier_scale,
+                       pin)
+
+
+def make_layer(E: int, T: int, H: int = 2880, I: int = 2880, top_k: int = 4,
+               seed: int = 0, wfmt: str = "bf16",
+               hot: Sequence[int] = (), hot_bias: float = 0.0,
+               p_outlier: float = 0.0, outlier_scale: float = 20.0,
+               w_std: float = 0.02, b_std: float = 0.01,
+               router_w_std: Optional[float] = None,
+               scale_lo: int = 119, scale_hi: int = 123,
+               pin: bool = False) -> Layer:
+    if wfmt not in ("bf16", "mxfp4"):
+        raise ValueError(f"unknown weight format {wfmt!r}")
+    rws = w_std if router_w_std is None else router_w_std
+    x = make_x(T, H, seed, p_outlier, outlier_scale, pin)
+    wr = normal_bf16((E, H), seed, S_WR, 0.0, rws, pin=pin)
+    br32 = normal_f32((E,), seed, S_BR, 0.0, b_std)
+    for e in hot:
+        br32[e] += hot_bias
+    br = round_bf16(br32, pin)
+    b_gu = normal_bf16((E, 2 * I), seed, S_BGU, 0.0, b_std, pin=pin)
+    b_d = normal_bf16((E, H), seed, S_BD, 0.0, b_std, pin=pin)
+    s_gu = s_d = None
+    if wfmt == "bf16":
+        w_gu = normal_bf16((E, 2 * I, H), seed, S_WGU, 0.0, w_std, pin=pin)
+        w_d = normal_bf16((E, H, I), seed, S_WD, 0.0, w_std, pin=pin)
+    else:
+        if H % 32 or I % 32:
+            raise ValueError("MXFP4 needs H and I multiples of 32")
+        w_gu = uniform_u8((E, 2 * I, H // 2), seed, S_GU_CODES, 0, 255, pin)
+        s_gu = uniform_u8((E, 2 * I, H // 32), seed, S_GU_SCALES, scale_lo,
+                          scale_hi, pin)
+        w_d = uniform_u8((E, H, I // 2), seed, S_D_CODES, 0, 255, pin)
+        s_d = uniform_u8((E, H, I // 32), seed, S_D_SCALES, scale_lo,
+                         scale_hi, pin)
+    return Layer(T=T, H=H, I=I, E=E, top_k=top_k, wfmt=wfmt, x=x, wr=wr,
+                 br=br, w_gu=w_gu, b_gu=b_gu, w_d=w_d, b_d=b_d, s_gu=s_gu,
+                 s_d=s_d,
+                 meta=dict(seed=seed, hot=tuple(hot), hot_bias=hot_bias,
+                           p_outlier=p_outlier, outlier_scale=outlier_scale,
+                           w_std=w_std, b_std=b_std))
+
+
+# The five workload families.  Each is (E, seed, token counts, extra recipe).
+WORKLOADS = {
+    "20b_t8": dict(E=32, seed=0, Ts=(8,), wfmt="bf16"),
+    "20b_decode": dict(E=32, seed=1, Ts=(1, 16, 64), wfmt="bf16"),
+    "20b_prefill_skewed": dict(E=32, seed=2, Ts=(4096,), wfmt="bf16",
+                               hot=(0, 1, 2, 3), hot_bias=2.0,
+                               p_outlier=0.01, outlier_scale=20.0),
+    "120b_shape": dict(E=128, seed=3, Ts=(1, 8, 64, 512, 4096, 8192),
+                       wfmt="bf16"),
+    "20b_mxfp4": dict(E=32, seed=4, Ts=(1, 64, 512), wfmt="mxfp4"),
+}
+
+
+def make_workload(name: str, T: int, pin: bool = False, **over) -> Layer:
+    """Full-size gpt-oss layer for one of the named workloads at T tokens."""
+    w = dict(WORKLOADS[name])
+    w.pop("Ts")
+    w.update(over)
+    return make_layer(T=T, pin=pin, **w)
