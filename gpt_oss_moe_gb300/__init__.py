@@ -1,0 +1,199 @@
+"""Python binding of the gpt-oss MoE layer library (``include/moe.h``).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+of ``libgpt_oss_moe.so``.  PyTorch supplies device memory and streams.  The
+names mirror the C ABI (``moe_route``, ``moe_forward``, ...).  There is no
+fallback: if the library has not been built, importing the binding's calls
+raises.
+
+Build the library with ``python -c "import __graft_entry__ as g; g.build()"``
+or ``python gpt_oss_moe_gb300/_build.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgpt_oss_moe.so")
+
+MOE_W_BF16, MOE_W_MXFP4 = 0, 1
+MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_BAD_TILE = 0x1, 0x2, 0x4
+
+# Every function the C header declares, in order (checked by the tests).
+EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_forward",
+           "moe_get_device_status", "moe_clear_device_status",
+           "moe_set_tuning", "moe_profile_enable", "moe_profile_read",
+           "moe_status_str")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {moe_status_str(code)} (status {code})")
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
+                ("E", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("wfmt", ctypes.c_int)]
+
+
+class moe_weight(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it first "
+                    "(python gpt_oss_moe_gb300/_build.py)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            S = ctypes.POINTER(moe_shape)
+            L.moe_workspace_bytes.argtypes = [S]
+            L.moe_workspace_bytes.restype = sz
+            L.moe_route.argtypes = [S, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.moe_route.restype = i
+            L.moe_forward.argtypes = [S, vp, vp, vp, moe_weight, moe_weight, vp, i,
+                                      vp, vp, vp, sz, vp]
+            L.moe_forward.restype = i
+            L.moe_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+            L.moe_get_device_status.restype = i
+            L.moe_clear_device_status.argtypes = [vp, vp]
+            L.moe_clear_device_status.restype = i
+            L.moe_set_tuning.argtypes = [ctypes.c_char_p, i]
+            L.moe_set_tuning.restype = i
+            L.moe_profile_enable.argtypes = [i]
+            L.moe_profile_enable.restype = i
+            L.moe_profile_read.argtypes = [ctypes.POINTER(ctypes.c_char_p),
+                                           ctypes.POINTER(ctypes.c_float), i,
+                                           ctypes.POINTER(ctypes.c_int)]
+            L.moe_profile_read.restype = i
+            L.moe_status_str.argtypes = [i]
+            L.moe_status_str.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the library must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise MoEError(code, where)
+
+
+def make_shape(T, H, I, E, top_k, wfmt=MOE_W_BF16) -> moe_shape:
+    return moe_shape(int(T), int(H), int(I), int(E), int(top_k), int(wfmt))
+
+
+def moe_status_str(code: int) -> str:
+    return lib().moe_status_str(int(code)).decode()
+
+
+def moe_workspace_bytes(shape: moe_shape) -> int:
+    return lib().moe_workspace_bytes(ctypes.byref(shape))
+
+
+def alloc_workspace(shape: moe_shape, device=None) -> torch.Tensor:
+    """Zeroed device workspace (status word cleared) for ``shape``."""
+    n = moe_workspace_bytes(shape)
+    if n == 0:
+        raise MoEError(-2, "moe_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_route(shape, hidden, router_w, router_b, topk_ids=None, topk_w=None,
+              expert_offsets=None, sorted_assign=None, workspace=None,
+              stream=None):
+    ws = workspace if workspace is not None else alloc_workspace(shape, hidden.device)
+    code = lib().moe_route(ctypes.byref(shape), _p(hidden), _p(router_w),
+                           _p(router_b), _p(topk_ids), _p(topk_w),
+                           _p(expert_offsets), _p(sorted_assign), _p(ws),
+                           ws.numel(), _stream(stream))
+    _check(code, "moe_route")
+    return ws
+
+
+def moe_forward(shape, hidden, router_w, router_b, w_gu, b_gu, w_d, b_d,
+                out, s_gu=None, s_d=None, topk_ids_out=None, topk_w_out=None,
+                workspace=None, stream=None):
+    """Enqueue the layer forward; ``out`` is fp32 or bf16 [T, H]."""
+    ws = workspace if workspace is not None else alloc_workspace(shape, hidden.device)
+    gu = moe_weight(_p(w_gu), _p(s_gu), _p(b_gu))
+    dn = moe_weight(_p(w_d), _p(s_d), _p(b_d))
+    out_f32 = 1 if out.dtype == torch.float32 else 0
+    if not out_f32 and out.dtype != torch.bfloat16:
+        raise ValueError("out must be float32 or bfloat16")
+    code = lib().moe_forward(ctypes.byref(shape), _p(hidden), _p(router_w),
+                             _p(router_b), gu, dn, _p(out), out_f32,
+                             _p(topk_ids_out), _p(topk_w_out), _p(ws),
+                             ws.numel(), _stream(stream))
+    _check(code, "moe_forward")
+    return ws
+
+
+def moe_get_device_status(workspace: torch.Tensor) -> int:
+    """Synchronising read of the device status word (0 = no error)."""
+    v = ctypes.c_int32(0)
+    code = lib().moe_get_device_status(_p(workspace), ctypes.byref(v))
+    if code not in (0, -7):
+        _check(code, "moe_get_device_status")
+    return v.value
+
+
+def moe_clear_device_status(workspace: torch.Tensor, stream=None):
+    _check(lib().moe_clear_device_status(_p(workspace), _stream(stream)),
+           "moe_clear_device_status")
+
+
+def moe_set_tuning(key: str, value: int):
+    _check(lib().moe_set_tuning(key.encode(), int(value)), "moe_set_tuning")
+
+
+def moe_profile_enable(enable: bool):
+    _check(lib().moe_profile_enable(1 if enable else 0), "moe_profile_enable")
+
+
+def moe_profile_read(cap: int = 16):
+    """[(kernel name, milliseconds)] for the most recent call."""
+    names = (ctypes.c_char_p * cap)()
+    ms = (ctypes.c_float * cap)()
+    n = ctypes.c_int(0)
+    _check(lib().moe_profile_read(names, ms, cap, ctypes.byref(n)),
+           "moe_profile_read")
+    return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
+
+
+def layer_shape(layer, T=None) -> moe_shape:
+    """Shape of a synthetic layer object (fields T, H, I, E, top_k, wfmt)."""
+    return make_shape(layer.T if T is None else T, layer.H, layer.I, layer.E,
+                      layer.top_k,
+                      MOE_W_BF16 if layer.wfmt == "bf16" else MOE_W_MXFP4)

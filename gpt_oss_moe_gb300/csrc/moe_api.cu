@@ -1,0 +1,458 @@
+// C ABI of the library (include/moe.h): argument validation on the host,
+// workspace layout, TMA tensor maps and the launch sequence
+//   router+top-k -> permutation -> gate_up GEMM (+GLU) -> down GEMM (+combine)
+//   [-> fp32->bf16 when a bf16 output is asked for]
+// all on the caller's stream, with no host synchronisation (xserv
+// docs/19-gpt-oss-moe.md, "Phase 19: gpt-oss-20b", §2 "MoE 前向").
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "moe_internal.cuh"
+#include "../../include/moe.h"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------ device cache
+
+struct DevInfo {
+    int sms = 0;
+    int max_smem = 0;
+    bool ok = false;
+};
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+moe_status device_info(DevInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.ok) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return MOE_ERR_CUDA;
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10) return MOE_ERR_UNSUPPORTED;   // built for sm_103a only
+        d.ok = true;
+    }
+    *out = d;
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+moe_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::call_once(g_encode_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!g_encode) return MOE_ERR_CUDA;
+    *fn = g_encode;
+    return MOE_OK;
+}
+
+// bf16 tensor, 128-byte swizzle, box inner extent 64 elements (128 B).
+moe_status make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides, const cuuint32_t* box) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    moe_status st = encode_fn(&enc);
+    if (st != MOE_OK) return st;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                     const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ tuning
+
+std::atomic<int> g_token_tile{0};
+std::atomic<int> g_pdl{1};
+
+// ------------------------------------------------------------ profiling
+
+constexpr int kMaxProf = 16;
+struct Prof {
+    bool on = false;
+    bool created = false;
+    cudaEvent_t ev[kMaxProf + 1];
+    const char* names[kMaxProf];
+    int n = 0;
+};
+Prof g_prof;
+std::mutex g_prof_mu;
+
+void prof_reset(cudaStream_t s) {
+    if (!g_prof.on) return;
+    g_prof.n = 0;
+    cudaEventRecord(g_prof.ev[0], s);
+}
+void prof_mark(const char* name, cudaStream_t s) {
+    if (!g_prof.on || g_prof.n >= kMaxProf) return;
+    g_prof.names[g_prof.n] = name;
+    cudaEventRecord(g_prof.ev[g_prof.n + 1], s);
+    ++g_prof.n;
+}
+
+// ------------------------------------------------------------ validation
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_shape(const moe_shape* s) {
+    if (!s) return MOE_ERR_ARG;
+    if (s->wfmt != MOE_W_BF16 && s->wfmt != MOE_W_MXFP4) return MOE_ERR_ARG;
+    if (s->T < 0 || s->T > (1 << 20)) return MOE_ERR_SHAPE;
+    if (s->H <= 0 || s->H % 64 || s->H > 32768) return MOE_ERR_SHAPE;
+    if (s->I <= 0 || s->I % 64 || s->I > 32768) return MOE_ERR_SHAPE;
+    if (s->E < 1 || s->E > kMaxExperts) return MOE_ERR_SHAPE;
+    if (s->top_k < 1 || s->top_k > kMaxTopK || s->top_k > s->E) return MOE_ERR_SHAPE;
+    return MOE_OK;
+}
+
+moe_status check_ptr(const void* p) {
+    if (!p) return MOE_ERR_ARG;
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+#define MOE_TRY(expr)                         \
+    do {                                      \
+        moe_status _st = (expr);              \
+        if (_st != MOE_OK) return _st;        \
+    } while (0)
+
+#define MOE_CUDA(expr)                                \
+    do {                                              \
+        if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)
+
+int auto_token_tile(int T) {
+    const int tuned = g_token_tile.load();
+    if (tuned > 0) return tuned;
+    int t = (T + 15) / 16 * 16;
+    return t < kMaxTokenTile ? t : kMaxTokenTile;
+}
+
+int next_pow2(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+struct Routing {
+    int32_t* ids;
+    float* w;
+    int32_t* offsets;
+    int32_t* sorted_assign;
+};
+
+// K1 + K2.  x_perm null = no gather (routing only).
+moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, const void* hidden,
+                          const void* router_w, const void* router_b, const Routing& r,
+                          float* zero_out, __nv_bfloat16* x_perm, int token_tile,
+                          cudaStream_t stream) {
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    RouterParams rp{};
+    rp.x = static_cast<const __nv_bfloat16*>(hidden);
+    rp.wr = static_cast<const __nv_bfloat16*>(router_w);
+    rp.br = static_cast<const __nv_bfloat16*>(router_b);
+    rp.T = s.T;
+    rp.H = s.H;
+    rp.E = s.E;
+    rp.top_k = s.top_k;
+    rp.topk_ids = r.ids;
+    rp.topk_w = r.w;
+    rp.blk_cnt = reinterpret_cast<int32_t*>(ws + L.blk_cnt);
+    rp.zero_out = zero_out;
+    rp.status = status;
+    MOE_CUDA(launch_router(rp, stream));
+    prof_mark("router_topk", stream);
+
+    PermuteParams pp{};
+    pp.topk_ids = r.ids;
+    pp.blk_cnt = rp.blk_cnt;
+    pp.x = rp.x;
+    pp.T = s.T;
+    pp.H = s.H;
+    pp.E = s.E;
+    pp.top_k = s.top_k;
+    pp.nblocks = (s.T + kRouterTokens - 1) / kRouterTokens;
+    pp.token_tile = token_tile;
+    pp.offsets = r.offsets;
+    pp.sorted_assign = r.sorted_assign;
+    pp.assign_row = reinterpret_cast<int32_t*>(ws + L.assign_row);
+    pp.tiles = reinterpret_cast<int4*>(ws + L.tiles);
+    pp.max_tiles = L.max_tiles;
+    pp.x_perm = x_perm;
+    pp.status = status;
+    MOE_CUDA(launch_permute(pp, stream, g_pdl.load() != 0));
+    prof_mark("permute_gather", stream);
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_shape* shape) {
+    if (check_shape(shape) != MOE_OK) return 0;
+    return ws_layout(shape->T, shape->H, shape->I, shape->E, shape->top_k).total;
+}
+
+moe_status moe_route(const moe_shape* shape, const void* hidden, const void* router_w,
+                     const void* router_b, int32_t* topk_ids, float* topk_w,
+                     int32_t* expert_offsets, int32_t* sorted_assign, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_shape(shape));
+    const moe_shape s = *shape;
+    if (s.T == 0) return MOE_OK;
+    MOE_TRY(check_ptr(hidden));
+    MOE_TRY(check_ptr(router_w));
+    MOE_TRY(check_ptr(router_b));
+    MOE_TRY(check_ptr(workspace));
+    for (const void* p : {static_cast<const void*>(topk_ids), static_cast<const void*>(topk_w),
+                          static_cast<const void*>(expert_offsets),
+                          static_cast<const void*>(sorted_assign)})
+        if (p && !aligned16(p)) return MOE_ERR_ALIGN;
+    const WsLayout L = ws_layout(s.T, s.H, s.I, s.E, s.top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DevInfo dev;
+    MOE_TRY(device_info(&dev));
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    Routing r;
+    r.ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(ws + L.topk_ids);
+    r.w = topk_w ? topk_w : reinterpret_cast<float*>(ws + L.topk_w);
+    r.offsets = expert_offsets ? expert_offsets : reinterpret_cast<int32_t*>(ws + L.offsets);
+    r.sorted_assign =
+        sorted_assign ? sorted_assign : reinterpret_cast<int32_t*>(ws + L.sorted_assign);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    prof_reset(stream);
+    return launch_routing(s, L, ws, hidden, router_w, router_b, r, nullptr, nullptr,
+                          auto_token_tile(s.T), stream);
+}
+
+moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* router_w,
+                       const void* router_b, moe_weight gate_up, moe_weight down, void* out,
+                       int out_is_fp32, int32_t* topk_ids_out, float* topk_w_out,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_shape(shape));
+    const moe_shape s = *shape;
+    if (s.T == 0) return MOE_OK;
+    MOE_TRY(check_ptr(hidden));
+    MOE_TRY(check_ptr(router_w));
+    MOE_TRY(check_ptr(router_b));
+    MOE_TRY(check_ptr(gate_up.w));
+    MOE_TRY(check_ptr(gate_up.bias));
+    MOE_TRY(check_ptr(down.w));
+    MOE_TRY(check_ptr(down.bias));
+    MOE_TRY(check_ptr(out));
+    MOE_TRY(check_ptr(workspace));
+    if (s.wfmt == MOE_W_MXFP4) {
+        MOE_TRY(check_ptr(gate_up.scale));
+        MOE_TRY(check_ptr(down.scale));
+        return MOE_ERR_UNSUPPORTED;
+    }
+    if ((topk_ids_out && !aligned16(topk_ids_out)) || (topk_w_out && !aligned16(topk_w_out)))
+        return MOE_ERR_ALIGN;
+    const WsLayout L = ws_layout(s.T, s.H, s.I, s.E, s.top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DevInfo dev;
+    MOE_TRY(device_info(&dev));
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    const int R = s.T * s.top_k;
+    const int box = auto_token_tile(s.T);
+    const bool pdl = g_pdl.load() != 0;
+
+    // Pipeline depth: as many stages as the shared memory allows (2..12).
+    const size_t stage_bytes = static_cast<size_t>(kWeightTileRows) * kBlockK * 2 +
+                               static_cast<size_t>(box) * kBlockK * 2;
+    const size_t fixed = gemm_smem_bytes(0, box);
+    const size_t budget = static_cast<size_t>(dev.max_smem) - 1024;
+    if (budget < fixed + 2 * stage_bytes) return MOE_ERR_UNSUPPORTED;
+    int stages = static_cast<int>((budget - fixed) / stage_bytes);
+    if (stages > 12) stages = 12;
+    const size_t smem = gemm_smem_bytes(stages, box) + 1024;
+    const int tmem_cols = next_pow2(2 * box < 32 ? 32 : 2 * box);
+
+    __nv_bfloat16* x_perm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm);
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+    float* out32 = out_is_fp32 ? static_cast<float*>(out) : reinterpret_cast<float*>(ws + L.out_acc);
+
+    // Tensor maps (host-side descriptors; cheap to build per call).
+    CUtensorMap tm_wgu, tm_x, tm_wd, tm_h;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(2 * s.I),
+                                    static_cast<cuuint64_t>(s.E)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(s.H) * 2,
+                                   static_cast<cuuint64_t>(2 * s.I) * s.H * 2};
+        const cuuint32_t boxd[3] = {64, 128, 1};
+        MOE_TRY(make_tmap(&tm_wgu, gate_up.w, 3, dims, str, boxd));
+    }
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.I), static_cast<cuuint64_t>(s.H),
+                                    static_cast<cuuint64_t>(s.E)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(s.I) * 2,
+                                   static_cast<cuuint64_t>(s.H) * s.I * 2};
+        const cuuint32_t boxd[3] = {64, 128, 1};
+        MOE_TRY(make_tmap(&tm_wd, down.w, 3, dims, str, boxd));
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(R)};
+        const cuuint64_t str[1] = {static_cast<cuuint64_t>(s.H) * 2};
+        const cuuint32_t boxd[2] = {64, static_cast<cuuint32_t>(box)};
+        MOE_TRY(make_tmap(&tm_x, x_perm, 2, dims, str, boxd));
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.I), static_cast<cuuint64_t>(R)};
+        const cuuint64_t str[1] = {static_cast<cuuint64_t>(s.I) * 2};
+        const cuuint32_t boxd[2] = {64, static_cast<cuuint32_t>(box)};
+        MOE_TRY(make_tmap(&tm_h, h, 2, dims, str, boxd));
+    }
+
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    prof_reset(stream);
+
+    Routing r;
+    r.ids = topk_ids_out ? topk_ids_out : reinterpret_cast<int32_t*>(ws + L.topk_ids);
+    r.w = topk_w_out ? topk_w_out : reinterpret_cast<float*>(ws + L.topk_w);
+    r.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    r.sorted_assign = reinterpret_cast<int32_t*>(ws + L.sorted_assign);
+    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r, out32, x_perm, box, stream));
+
+    GemmParams g{};
+    g.tiles = reinterpret_cast<const int4*>(ws + L.tiles);
+    g.num_tiles = status + kNumTilesWord;
+    g.token_box = box;
+    g.stages = stages;
+    g.tmem_cols = tmem_cols;
+    g.num_experts = s.E;
+    g.rows_total = R;
+    g.status = status;
+
+    // gate_up + bias + GLU -> h
+    g.n_wblocks = 2 * s.I / kWeightTileRows;
+    g.k_blocks = s.H / kBlockK;
+    g.w_rows = 2 * s.I;
+    g.bias = static_cast<const __nv_bfloat16*>(gate_up.bias);
+    g.h = h;
+    int grid = L.max_tiles * g.n_wblocks;
+    if (grid > dev.sms) grid = dev.sms;
+    MOE_CUDA(launch_gemm(kEpiGlu, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
+    prof_mark("gate_up_glu", stream);
+
+    // down + bias + weighted combine -> out (fp32 accumulation)
+    g.n_wblocks = (s.H + kWeightTileRows - 1) / kWeightTileRows;
+    g.k_blocks = s.I / kBlockK;
+    g.w_rows = s.H;
+    g.bias = static_cast<const __nv_bfloat16*>(down.bias);
+    g.h = nullptr;
+    g.out = out32;
+    g.sorted_assign = r.sorted_assign;
+    g.topk_w = r.w;
+    g.top_k = s.top_k;
+    grid = L.max_tiles * g.n_wblocks;
+    if (grid > dev.sms) grid = dev.sms;
+    MOE_CUDA(launch_gemm(kEpiCombine, g, &tm_wd, &tm_h, grid, smem, stream, pdl));
+    prof_mark("down_combine", stream);
+
+    if (!out_is_fp32) {
+        MOE_CUDA(launch_to_bf16(out32, static_cast<__nv_bfloat16*>(out),
+                                static_cast<size_t>(s.T) * s.H, stream, pdl));
+        prof_mark("to_bf16", stream);
+    }
+    return MOE_OK;
+}
+
+moe_status moe_get_device_status(const void* workspace, int32_t* host_status) {
+    if (!workspace || !host_status) return MOE_ERR_ARG;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *host_status = v;
+    return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+moe_status moe_clear_device_status(void* workspace, cudaStream_t stream) {
+    if (!workspace) return MOE_ERR_ARG;
+    return cudaMemsetAsync(workspace, 0, 256, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_set_tuning(const char* key, int value) {
+    if (!key) return MOE_ERR_ARG;
+    if (std::strcmp(key, "token_tile") == 0) {
+        if (value != 0 && (value < 16 || value > kMaxTokenTile || value % 16)) return MOE_ERR_ARG;
+        g_token_tile.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "pdl") == 0) {
+        if (value != 0 && value != 1) return MOE_ERR_ARG;
+        g_pdl.store(value);
+        return MOE_OK;
+    }
+    return MOE_ERR_ARG;
+}
+
+moe_status moe_profile_enable(int enable) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (enable && !g_prof.created) {
+        for (int i = 0; i <= kMaxProf; ++i)
+            if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) return MOE_ERR_CUDA;
+        g_prof.created = true;
+    }
+    g_prof.on = enable != 0;
+    g_prof.n = 0;
+    return MOE_OK;
+}
+
+moe_status moe_profile_read(const char** names, float* ms, int cap, int* count) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (!count) return MOE_ERR_ARG;
+    *count = 0;
+    if (!g_prof.created || g_prof.n == 0) return MOE_OK;
+    if (cudaEventSynchronize(g_prof.ev[g_prof.n]) != cudaSuccess) return MOE_ERR_CUDA;
+    const int n = g_prof.n < cap ? g_prof.n : cap;
+    for (int i = 0; i < n; ++i) {
+        if (names) names[i] = g_prof.names[i];
+        if (ms && cudaEventElapsedTime(&ms[i], g_prof.ev[i], g_prof.ev[i + 1]) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    *count = n;
+    return MOE_OK;
+}
+
+const char* moe_status_str(moe_status st) {
+    switch (st) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_ARG: return "invalid argument (null pointer or bad enum)";
+        case MOE_ERR_SHAPE: return "unsupported shape";
+        case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_UNSUPPORTED: return "unsupported by this build or device";
+        case MOE_ERR_CUDA: return "CUDA runtime/driver call failed";
+        case MOE_ERR_DEVICE: return "device status word reports an error";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

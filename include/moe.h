@@ -1,0 +1,166 @@
+/*
+ * gpt-oss mixture-of-experts layer forward on one GB300 (sm_103a).
+ *
+ * The operation (xserv docs/19-gpt-oss-moe.md, "Phase 19: gpt-oss-20b",
+ * §1 model-architecture table "MoE" and "激活" rows, §2 "MoE 前向"):
+ *
+ *   logits[t,e] = sum_h x[t,h] * Wr[e,h] + br[e]                 (router)
+ *   ids[t,:]    = the top_k experts by logit, descending, ties to the lower
+ *                 expert index; w[t,:] = softmax over those k logits
+ *   gu          = W_gu[e] x[t] + b_gu[e]           (2I features, interleaved)
+ *   gate_j      = min(gu[2j], 7),  up_j = clamp(gu[2j+1], -7, 7)
+ *   h_j         = (up_j + 1) * gate_j * sigmoid(1.702 * gate_j)
+ *   y           = W_d[e] h + b_d[e]
+ *   out[t,:]    = sum_{j<top_k} w[t,j] * y(expert ids[t,j], token t)
+ *
+ * Unselected experts are skipped (never multiplied by zero).  Expert ids stay
+ * on the device: no call below synchronises the host with the GPU, except
+ * moe_get_device_status, which says so.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers, row-major, densely packed,
+ *     16-byte aligned.  The caller owns every buffer; the library allocates
+ *     no device memory and keeps no state beyond a per-device cache of device
+ *     attributes and the optional profiling events below.
+ *   - bf16 is IEEE-754 binary16-brain (uint16 storage).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and returned as a negative moe_status; nothing is launched then.
+ *   - Errors that only the device can see (an expert id out of range, a
+ *     pipeline wait that timed out) set bits in the device status word held
+ *     in the workspace; read it with moe_get_device_status.
+ *   - T == 0 is valid and enqueues nothing.
+ *
+ * Supported shapes: H % 64 == 0, I % 64 == 0, 1 <= E <= 256,
+ * 1 <= top_k <= min(E, 8), 0 <= T <= 1048576.
+ */
+#ifndef GPT_OSS_MOE_H
+#define GPT_OSS_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = -1,          /* null pointer or bad enum value */
+    MOE_ERR_SHAPE = -2,        /* a dimension outside the supported set */
+    MOE_ERR_ALIGN = -3,        /* a pointer not 16-byte aligned */
+    MOE_ERR_WORKSPACE = -4,    /* workspace missing or smaller than needed */
+    MOE_ERR_UNSUPPORTED = -5,  /* valid request this build cannot serve */
+    MOE_ERR_CUDA = -6,         /* a CUDA runtime/driver call failed */
+    MOE_ERR_DEVICE = -7        /* the device status word reported an error */
+} moe_status;
+
+/* Expert weight storage format. */
+typedef enum {
+    MOE_W_BF16 = 0,   /* bf16 values */
+    MOE_W_MXFP4 = 1   /* OCP MX FP4: E2M1 codes, two per byte (element 2i in
+                         the low nibble of byte i), plus one E8M0 scale byte
+                         (value 2^(s-127)) per 32 consecutive input elements
+                         of each output row (§5 "量化") */
+} moe_wfmt;
+
+/* Layer shape.  T tokens, hidden size H, expert intermediate size I,
+ * E experts, top_k experts per token. */
+typedef struct {
+    int T, H, I, E, top_k;
+    int wfmt;                  /* a moe_wfmt */
+} moe_shape;
+
+/* One expert weight bank.
+ *   gate_up: w bf16 [E, 2I, H] (row 2j = gate_j, row 2j+1 = up_j) or MXFP4
+ *            codes u8 [E, 2I, H/2] with scale u8 [E, 2I, H/32];
+ *            bias bf16 [E, 2I].
+ *   down:    w bf16 [E, H, I] or codes u8 [E, H, I/2], scale u8 [E, H, I/32];
+ *            bias bf16 [E, H].
+ * scale is NULL for bf16 weights. */
+typedef struct {
+    const void* w;
+    const void* scale;
+    const void* bias;
+} moe_weight;
+
+/* Device status word bits (moe_get_device_status). */
+#define MOE_DEV_BAD_EXPERT_ID  0x1   /* a routed id fell outside [0, E) */
+#define MOE_DEV_WAIT_TIMEOUT   0x2   /* a pipeline wait gave up (~1 s) */
+#define MOE_DEV_BAD_TILE       0x4   /* a work tile failed its bounds check */
+
+/* Bytes of device workspace moe_route / moe_forward need for this shape
+ * (0 for an invalid shape).  The workspace is scratch owned by the caller;
+ * its contents between calls are unspecified except for the status word,
+ * which only moe_clear_device_status resets. */
+size_t moe_workspace_bytes(const moe_shape* shape);
+
+/* Router + top-k softmax + expert permutation (§2: "router GEMV ->
+ * topk_softmax", ids kept on the GPU).
+ *   hidden   bf16 [T, H];  router_w bf16 [E, H];  router_b bf16 [E]
+ *   topk_ids int32 [T, top_k]   out: expert of slot j of token t
+ *   topk_w   fp32  [T, top_k]   out: its softmax weight
+ *   expert_offsets int32 [E+1]  out: exclusive scan of per-expert counts
+ *   sorted_assign  int32 [T*top_k] out: assignment a = t*top_k + j placed at
+ *                  row r, rows sorted by (expert, a) ascending
+ * Any of the four outputs may be NULL (that result is then kept in the
+ * workspace only).  Returns MOE_OK once the work is enqueued. */
+moe_status moe_route(const moe_shape* shape, const void* hidden,
+                     const void* router_w, const void* router_b,
+                     int32_t* topk_ids, float* topk_w,
+                     int32_t* expert_offsets, int32_t* sorted_assign,
+                     void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/* The whole layer forward (§2 step list, routed form).
+ *   hidden, router_w, router_b as for moe_route;
+ *   gate_up, down: expert weight banks (see moe_weight);
+ *   out: [T, H], fp32 when out_is_fp32 != 0, else bf16 (rounded to nearest
+ *        even from the fp32 sum);
+ *   topk_ids_out int32 [T, top_k], topk_w_out fp32 [T, top_k]: optional
+ *        copies of the routing (NULL to skip).
+ * The fp32 combine adds the top_k expert outputs of a token in an order that
+ * may vary from run to run (last-bit differences only). */
+moe_status moe_forward(const moe_shape* shape, const void* hidden,
+                       const void* router_w, const void* router_b,
+                       moe_weight gate_up, moe_weight down,
+                       void* out, int out_is_fp32,
+                       int32_t* topk_ids_out, float* topk_w_out,
+                       void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Copies the device status word of `workspace` to *host_status.  This call
+ * synchronises the calling thread with the device (cudaMemcpy).  Returns
+ * MOE_ERR_DEVICE when the word is non-zero, MOE_OK otherwise. */
+moe_status moe_get_device_status(const void* workspace, int32_t* host_status);
+
+/* Zeroes the device status word (enqueued on `stream`). */
+moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
+
+/* Process-wide tuning switches for tests and benchmarks:
+ *   "token_tile": rows of tokens per GEMM tile, 0 = automatic, else a
+ *                 multiple of 16 in [16, 256];
+ *   "pdl":        1 = launch dependent kernels with programmatic dependent
+ *                 launch (default), 0 = plain stream order.
+ * Returns MOE_ERR_ARG for an unknown key or value. */
+moe_status moe_set_tuning(const char* key, int value);
+
+/* Optional per-kernel timing.  moe_profile_enable(1) makes later calls record
+ * a CUDA event around every kernel they launch (on the call's stream);
+ * moe_profile_read returns, for the most recent call, up to `cap` kernel
+ * names (static strings) and their durations in milliseconds; it waits for
+ * the last recorded event.  Returns the number of kernels through *count. */
+moe_status moe_profile_enable(int enable);
+moe_status moe_profile_read(const char** names, float* ms, int cap,
+                            int* count);
+
+/* Static description of a status code. */
+const char* moe_status_str(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPT_OSS_MOE_H */

@@ -140,7 +140,7 @@ def make_layer(E: int, T: int, H: int = 2880, I: int = 2880, top_k: int = 4,
                w_std: float = 0.02, b_std: float = 0.01,
                router_w_std: Optional[float] = None,
                scale_lo: int = 119, scale_hi: int = 123,
-               pin: bool = False) -> Layer:
+               pin: bool = False, with_experts: bool = True) -> Layer:
     if wfmt not in ("bf16", "mxfp4"):
         raise ValueError(f"unknown weight format {wfmt!r}")
     rws = w_std if router_w_std is None else router_w_std
@@ -150,10 +150,14 @@ def make_layer(E: int, T: int, H: int = 2880, I: int = 2880, top_k: int = 4,
     for e in hot:
         br32[e] += hot_bias
     br = round_bf16(br32, pin)
-    b_gu = normal_bf16((E, 2 * I), seed, S_BGU, 0.0, b_std, pin=pin)
-    b_d = normal_bf16((E, H), seed, S_BD, 0.0, b_std, pin=pin)
     s_gu = s_d = None
-    if wfmt == "bf16":
+    b_gu = w_gu = b_d = w_d = None       # routing-only inputs keep these empty
+    if with_experts:
+        b_gu = normal_bf16((E, 2 * I), seed, S_BGU, 0.0, b_std, pin=pin)
+        b_d = normal_bf16((E, H), seed, S_BD, 0.0, b_std, pin=pin)
+    if not with_experts:
+        pass
+    elif wfmt == "bf16":
         w_gu = normal_bf16((E, 2 * I, H), seed, S_WGU, 0.0, w_std, pin=pin)
         w_d = normal_bf16((E, H, I), seed, S_WD, 0.0, w_std, pin=pin)
     else:

@@ -1,0 +1,130 @@
+"""The C-ABI library builds, loads and exports every symbol include/moe.h
+declares; host-side argument checks reject bad calls before touching a GPU.
+
+No test here launches work: with no GPU present, only calls that fail
+validation (or never reach CUDA) are made.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from gpt_oss_moe_gb300 import _build
+    _build.build()
+    import gpt_oss_moe_gb300 as m
+    return m
+
+
+def _declared_functions():
+    names = []
+    for hdr in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*"
+                            r"(moe_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_binding_names(moe):
+    declared = _declared_functions()
+    assert sorted(declared) == sorted(moe.EXPORTS)
+    assert "moe_route" in declared and "moe_forward" in declared
+
+
+def test_library_exports_every_declared_symbol(moe):
+    L = ctypes.CDLL(moe.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(moe):
+    for code in range(-7, 1):
+        assert moe.moe_status_str(code) != "unknown status"
+    assert moe.moe_status_str(-99) == "unknown status"
+
+
+def _shape(moe, **kw):
+    d = dict(T=8, H=2880, I=2880, E=32, top_k=4, wfmt=0)
+    d.update(kw)
+    return moe.make_shape(**d)
+
+
+def test_workspace_bytes(moe):
+    small = moe.moe_workspace_bytes(_shape(moe, T=8))
+    big = moe.moe_workspace_bytes(_shape(moe, T=4096))
+    assert 0 < small < big
+    # T * k rows of activations and of h, T rows of fp32 output
+    assert big >= 4096 * 4 * 2880 * 2 * 2 + 4096 * 2880 * 4
+    assert moe.moe_workspace_bytes(_shape(moe, T=0)) > 0
+    for bad in [dict(H=2880 + 32), dict(I=100), dict(E=0), dict(E=257),
+                dict(top_k=0), dict(top_k=9), dict(E=2, top_k=3), dict(T=-1),
+                dict(T=(1 << 20) + 1)]:
+        assert moe.moe_workspace_bytes(_shape(moe, **bad)) == 0, bad
+
+
+def _fwd(moe, shape, ptrs, ws_bytes=1 << 30):
+    L = moe.lib()
+    gu = moe.moe_weight(ptrs.get("wgu", 256), ptrs.get("sgu"), ptrs.get("bgu", 512))
+    dn = moe.moe_weight(ptrs.get("wd", 768), ptrs.get("sd"), ptrs.get("bd", 1024))
+    return L.moe_forward(ctypes.byref(shape), ptrs.get("x", 16), ptrs.get("wr", 32),
+                         ptrs.get("br", 48), gu, dn, ptrs.get("out", 64), 1,
+                         None, None, ptrs.get("ws", 4096), ws_bytes, None)
+
+
+def test_forward_rejects_bad_arguments_on_the_host(moe):
+    s = _shape(moe)
+    assert _fwd(moe, _shape(moe, H=100), {}) == -2          # MOE_ERR_SHAPE
+    assert _fwd(moe, _shape(moe, wfmt=7), {}) == -1         # MOE_ERR_ARG
+    assert _fwd(moe, s, {"x": 0}) == -1                     # null hidden
+    assert _fwd(moe, s, {"out": 0}) == -1                   # null out
+    assert _fwd(moe, s, {"wd": 0}) == -1                    # null down weights
+    assert _fwd(moe, s, {"x": 24}) == -3                    # misaligned
+    assert _fwd(moe, s, {"wgu": 520}) == -3
+    assert _fwd(moe, s, {}, ws_bytes=100) == -4             # workspace too small
+    assert moe.lib().moe_forward(None, 16, 32, 48, moe.moe_weight(), moe.moe_weight(),
+                                 64, 1, None, None, 4096, 1 << 30, None) == -1
+    # T == 0 is valid and enqueues nothing (no device needed)
+    assert _fwd(moe, _shape(moe, T=0), {"x": 0, "out": 0}) == 0
+
+
+def test_route_rejects_bad_arguments_on_the_host(moe):
+    L = moe.lib()
+    s = _shape(moe)
+    assert L.moe_route(ctypes.byref(s), 0, 32, 48, None, None, None, None, 4096,
+                       1 << 30, None) == -1
+    assert L.moe_route(ctypes.byref(s), 16, 32, 48, 8, None, None, None, 4096,
+                       1 << 30, None) == -3
+    assert L.moe_route(ctypes.byref(s), 16, 32, 48, None, None, None, None, 4096,
+                       10, None) == -4
+    s0 = _shape(moe, T=0)
+    assert L.moe_route(ctypes.byref(s0), 0, 0, 0, None, None, None, None, 0, 0,
+                       None) == 0
+
+
+def test_tuning_switches(moe):
+    with pytest.raises(moe.MoEError):
+        moe.moe_set_tuning("token_tile", 24)
+    with pytest.raises(moe.MoEError):
+        moe.moe_set_tuning("token_tile", 512)
+    with pytest.raises(moe.MoEError):
+        moe.moe_set_tuning("no_such_key", 1)
+    moe.moe_set_tuning("token_tile", 64)
+    moe.moe_set_tuning("token_tile", 0)
+    moe.moe_set_tuning("pdl", 0)
+    moe.moe_set_tuning("pdl", 1)
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import gpt_oss_moe_gb300 as m
+    monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(m, "_lib", None)
+    with pytest.raises(ImportError):
+        m.lib()

@@ -1,0 +1,220 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small shapes span several tiles and every ragged tail (token counts, the
+128-row weight blocks, expert counts, forced token-tile sizes); the
+full-size gpt-oss shapes are checked on every token's routing and on every
+output row where the oracle finishes in seconds, else on sampled rows.
+"""
+import dataclasses
+
+import pytest
+import torch
+
+from parity_util import (TOL_BF16, compare_output, compare_routing, gpu_forward,
+                         tie_masks, to_device)
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from gpt_oss_moe_gb300 import _build
+    _build.build()
+    import gpt_oss_moe_gb300 as m
+    m.lib()
+    return m
+
+
+def _prefix(layer, T):
+    return dataclasses.replace(layer, T=T, x=layer.x[:T].contiguous())
+
+
+def _check(moe, oracle_lib, layer, dev=None, T=None, sample=None, tol=TOL_BF16,
+           out_dtype=torch.float32):
+    """GPU forward of the first T tokens vs the oracle (all rows or a sample)."""
+    T = layer.T if T is None else T
+    ids, w, out, ws = gpu_forward(moe, layer, dev=dev, T=T, out_dtype=out_dtype)
+    assert moe.moe_get_device_status(ws) == 0
+    L = _prefix(layer, T) if T != layer.T else layer
+    # routing of every token
+    logits = oracle_lib.router_logits(L)
+    o_ids, o_w = oracle_lib.topk_softmax(logits, L.top_k)
+    rep = compare_routing(ids, w, o_ids, o_w, logits, L.top_k)
+    excluded, _ = tie_masks(logits, L.top_k)
+    # outputs of all tokens, or of a sample
+    tokens = list(range(T)) if sample is None else sorted(set(sample))
+    keep = [t for t in tokens if not excluded[t]]
+    _, _, o_out = oracle_lib.forward(L, tokens=keep)
+    err, ref = compare_output(out.float()[keep], o_out, slice(None), tol)
+    return rep, err, ref, ids
+
+
+SMALL_CASES = [
+    # E, k, H, I, T, w_std, token_tile
+    (8, 2, 128, 128, 1, 0.05, 0),
+    (8, 4, 320, 192, 37, 0.05, 0),      # 320 = 2*128 + 64: weight-row tail
+    (16, 4, 256, 384, 300, 0.05, 0),
+    (4, 2, 192, 64, 700, 0.05, 0),      # several token tiles per expert
+    (8, 4, 256, 256, 200, 0.2, 16),     # clamps active, forced token tiles
+    (8, 4, 256, 256, 200, 0.2, 48),
+    (8, 4, 256, 256, 200, 0.2, 128),
+    (8, 4, 256, 256, 200, 0.2, 256),
+    (8, 1, 128, 128, 64, 0.05, 0),      # top-1
+    (256, 8, 128, 128, 40, 0.05, 0),    # most experts, largest top_k
+    (5, 3, 64, 64, 19, 0.1, 0),         # E not a multiple of 8, 64-wide
+    (32, 4, 2880, 2880, 3, 0.02, 0),    # gpt-oss widths, tiny T
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: "E{}k{}H{}I{}T{}s{}tile{}".format(*c))
+def test_forward_small_shapes(moe, oracle_lib, synth_lib, case):
+    E, k, H, I, T, wstd, tile = case
+    L = synth_lib.make_layer(E=E, T=T, H=H, I=I, top_k=k, seed=100 + T, w_std=wstd,
+                             router_w_std=0.05)
+    moe.moe_set_tuning("token_tile", tile)
+    try:
+        _check(moe, oracle_lib, L)
+    finally:
+        moe.moe_set_tuning("token_tile", 0)
+
+
+def test_clamps_are_exercised(oracle_lib, synth_lib):
+    L = synth_lib.make_layer(E=8, T=200, H=256, I=256, top_k=4, seed=300, w_std=0.2,
+                             router_w_std=0.05)
+    x = L.x[:16].float()
+    gu = torch.einsum("nh,th->tn", L.w_gu[0].float(), x) + L.b_gu[0].float()
+    assert (gu[:, 0::2] > 7).any() and (gu[:, 1::2].abs() > 7).any()
+
+
+def test_bf16_output_is_rounded_fp32_output(moe, synth_lib):
+    L = synth_lib.make_layer(E=8, T=50, H=256, I=256, top_k=4, seed=7, w_std=0.05)
+    dev = to_device(L)
+    _, _, o32, _ = gpu_forward(moe, L, dev=dev)
+    _, _, o16, _ = gpu_forward(moe, L, dev=dev, out_dtype=torch.bfloat16)
+    # the fp32 combine order may differ between the runs in the last bit
+    diff = (o16.float() - o32.to(torch.bfloat16).float()).abs()
+    ulp = o32.abs().clamp_min(1e-30) * 2.0 ** -7
+    assert (diff <= ulp).all()
+
+
+def test_zero_tokens_enqueues_nothing(moe, synth_lib):
+    L = synth_lib.make_layer(E=8, T=4, H=128, I=128, top_k=2, seed=1)
+    dev = to_device(L)
+    shape = moe.layer_shape(L, 0)
+    out = torch.full((1, 128), 3.0, device="cuda")
+    moe.moe_forward(shape, dev["x"], dev["wr"], dev["br"], dev["w_gu"], dev["b_gu"],
+                    dev["w_d"], dev["b_d"], out,
+                    workspace=torch.zeros(1024, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert (out == 3.0).all()
+
+
+def test_outputs_stay_inside_their_buffers(moe, synth_lib):
+    """Canary rows around out/topk buffers must be untouched."""
+    L = synth_lib.make_layer(E=16, T=45, H=320, I=192, top_k=4, seed=5, w_std=0.05)
+    dev = to_device(L)
+    shape = moe.layer_shape(L)
+    pad = 8
+    big = torch.full((L.T + 2 * pad, L.H), float("nan"), device="cuda")
+    ids_big = torch.full((L.T + 2 * pad, 4), -7, dtype=torch.int32, device="cuda")
+    w_big = torch.full((L.T + 2 * pad, 4), -7.0, device="cuda")
+    ws = moe.alloc_workspace(shape)
+    moe.moe_forward(shape, dev["x"], dev["wr"], dev["br"], dev["w_gu"], dev["b_gu"],
+                    dev["w_d"], dev["b_d"], big[pad:pad + L.T], topk_ids_out=ids_big[pad:pad + L.T],
+                    topk_w_out=w_big[pad:pad + L.T], workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.isnan(big[:pad]).all() and torch.isnan(big[pad + L.T:]).all()
+    assert torch.isfinite(big[pad:pad + L.T]).all()
+    assert (ids_big[:pad] == -7).all() and (ids_big[pad + L.T:] == -7).all()
+    assert (w_big[:pad] == -7).all() and (w_big[pad + L.T:] == -7).all()
+
+
+# ---------------------------------------------------------------- routing
+
+
+ROUTE_CASES = [("20b_t8", 8), ("20b_decode", 1), ("20b_decode", 64),
+               ("20b_prefill_skewed", 4096), ("120b_shape", 512), ("120b_shape", 8192)]
+
+
+@pytest.mark.parametrize("name,T", ROUTE_CASES, ids=lambda v: str(v))
+def test_route_full_size(moe, oracle_lib, synth_lib, name, T):
+    L = synth_lib.make_workload(name, T, with_experts=False)
+    k, E = L.top_k, L.E
+    x, wr, br = (t.cuda() for t in (L.x, L.wr, L.br))
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sa = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    shape = moe.make_shape(T, L.H, 2880, E, k)
+    ws = moe.moe_route(shape, x, wr, br, ids, w, off, sa)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    logits = oracle_lib.router_logits(L)
+    o_ids, o_w = oracle_lib.topk_softmax(logits, k)
+    rep = compare_routing(ids, w, o_ids, o_w, logits, k)
+    # the permutation is the oracle's stable sort of the GPU's ids, bit-exact
+    o_off, o_sa, _ = oracle_lib.permute(ids.cpu(), E)
+    assert torch.equal(off.cpu(), o_off) and torch.equal(sa.cpu(), o_sa)
+    assert rep.n_near_tie <= max(2, T // 500)
+    # a second run gives bit-identical routing
+    ids2, w2 = torch.empty_like(ids), torch.empty_like(w)
+    off2, sa2 = torch.empty_like(off), torch.empty_like(sa)
+    moe.moe_route(shape, x, wr, br, ids2, w2, off2, sa2, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids2) and torch.equal(w, w2)
+    assert torch.equal(off, off2) and torch.equal(sa, sa2)
+
+
+def test_hot_experts_take_a_large_share(moe, synth_lib):
+    L = synth_lib.make_workload("20b_prefill_skewed", 4096, with_experts=False)
+    shape = moe.make_shape(4096, L.H, 2880, L.E, 4)
+    off = torch.empty(L.E + 1, dtype=torch.int32, device="cuda")
+    moe.moe_route(shape, L.x.cuda(), L.wr.cuda(), L.br.cuda(), expert_offsets=off)
+    counts = off.diff().cpu()
+    share = counts[:4].sum().item() / counts.sum().item()
+    assert 0.2 < share < 0.7
+
+
+# ---------------------------------------------------------------- full size
+
+
+@pytest.fixture(scope="module")
+def layer_20b_decode(synth_lib):
+    L = synth_lib.make_workload("20b_decode", 64)
+    return L, to_device(L)
+
+
+@pytest.mark.parametrize("T", [1, 16, 64])
+def test_forward_20b_decode(moe, oracle_lib, layer_20b_decode, T):
+    L, dev = layer_20b_decode
+    _check(moe, oracle_lib, L, dev=dev, T=T)
+
+
+def test_forward_20b_t8(moe, oracle_lib, synth_lib):
+    L = synth_lib.make_workload("20b_t8", 8)
+    _check(moe, oracle_lib, L)
+
+
+def test_forward_20b_prefill_skewed_sampled(moe, oracle_lib, synth_lib):
+    L = synth_lib.make_workload("20b_prefill_skewed", 4096)
+    g = torch.Generator().manual_seed(2)
+    sample = list(range(8)) + list(range(4088, 4096)) + \
+        torch.randint(0, 4096, (32,), generator=g).tolist()
+    rep, err, ref, ids = _check(moe, oracle_lib, L, sample=sample)
+
+
+@pytest.fixture(scope="module")
+def layer_120b(synth_lib):
+    L = synth_lib.make_workload("120b_shape", 8192)
+    return L, to_device(L)
+
+
+@pytest.mark.parametrize("T", [1, 8, 64, 512, 4096, 8192])
+def test_forward_120b_shape(moe, oracle_lib, layer_120b, T):
+    L, dev = layer_120b
+    sample = None
+    if T > 64:
+        g = torch.Generator().manual_seed(T)
+        sample = [0, T - 1] + torch.randint(0, T, (30,), generator=g).tolist()
+    _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample)
