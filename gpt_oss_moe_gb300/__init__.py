@@ -178,12 +178,13 @@ def moe_set_tuning(key: str, value: int):
     _check(lib().moe_set_tuning(key.encode(), int(value)), "moe_set_tuning")
 
 
-def moe_profile_enable(enable: bool):
-    _check(lib().moe_profile_enable(1 if enable else 0), "moe_profile_enable")
+def moe_profile_enable(calls: int):
+    """Record per-kernel events for the next ``calls`` calls (0 = off)."""
+    _check(lib().moe_profile_enable(int(calls)), "moe_profile_enable")
 
 
-def moe_profile_read(cap: int = 16):
-    """[(kernel name, milliseconds)] for the most recent call."""
+def moe_profile_read(cap: int = 8):
+    """[(kernel name, mean milliseconds over the recorded calls)]."""
     names = (ctypes.c_char_p * cap)()
     ms = (ctypes.c_float * cap)()
     n = ctypes.c_int(0)

@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -86,28 +87,45 @@ std::atomic<int> g_token_tile{0};
 std::atomic<int> g_pdl{1};
 
 // ------------------------------------------------------------ profiling
+//
+// When enabled for C calls, each of the next C calls records one CUDA event
+// before its first kernel and one after each kernel, on the call's stream.
+// Reading waits for the last event and averages each kernel over the calls.
 
-constexpr int kMaxProf = 16;
+constexpr int kMaxProf = 8;          // kernels per call
+constexpr int kMaxProfCalls = 8192;
 struct Prof {
-    bool on = false;
-    bool created = false;
-    cudaEvent_t ev[kMaxProf + 1];
+    int capacity = 0;                // calls to record (0 = off)
+    int calls = 0;                   // calls recorded so far
+    int created = 0;                 // events created (capacity * (kMaxProf + 1))
+    cudaEvent_t* ev = nullptr;
     const char* names[kMaxProf];
-    int n = 0;
+    int n = 0;                       // kernels in the current call
+    int n_first = 0;                 // kernels per call (from the first call)
 };
 Prof g_prof;
 std::mutex g_prof_mu;
 
+cudaEvent_t* prof_slot() {
+    return g_prof.ev + static_cast<size_t>(g_prof.calls) * (kMaxProf + 1);
+}
 void prof_reset(cudaStream_t s) {
-    if (!g_prof.on) return;
+    g_prof.n = -1;
+    if (g_prof.calls >= g_prof.capacity) return;
     g_prof.n = 0;
-    cudaEventRecord(g_prof.ev[0], s);
+    cudaEventRecord(prof_slot()[0], s);
 }
 void prof_mark(const char* name, cudaStream_t s) {
-    if (!g_prof.on || g_prof.n >= kMaxProf) return;
-    g_prof.names[g_prof.n] = name;
-    cudaEventRecord(g_prof.ev[g_prof.n + 1], s);
+    if (g_prof.n < 0 || g_prof.n >= kMaxProf) return;
+    if (g_prof.calls == 0) g_prof.names[g_prof.n] = name;
+    cudaEventRecord(prof_slot()[g_prof.n + 1], s);
     ++g_prof.n;
+}
+void prof_finish() {
+    if (g_prof.n < 0) return;
+    if (g_prof.calls == 0) g_prof.n_first = g_prof.n;
+    if (g_prof.n == g_prof.n_first) ++g_prof.calls;   // calls of another shape are dropped
+    g_prof.n = -1;
 }
 
 // ------------------------------------------------------------ validation
@@ -246,8 +264,10 @@ moe_status moe_route(const moe_shape* shape, const void* hidden, const void* rou
         sorted_assign ? sorted_assign : reinterpret_cast<int32_t*>(ws + L.sorted_assign);
     std::lock_guard<std::mutex> lock(g_prof_mu);
     prof_reset(stream);
-    return launch_routing(s, L, ws, hidden, router_w, router_b, r, nullptr, nullptr,
-                          auto_token_tile(s.T), stream);
+    const moe_status st = launch_routing(s, L, ws, hidden, router_w, router_b, r, nullptr,
+                                         nullptr, auto_token_tile(s.T), stream);
+    prof_finish();
+    return st;
 }
 
 moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* router_w,
@@ -381,6 +401,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
                                 static_cast<size_t>(s.T) * s.H, stream, pdl));
         prof_mark("to_bf16", stream);
     }
+    prof_finish();
     return MOE_OK;
 }
 
@@ -413,15 +434,28 @@ moe_status moe_set_tuning(const char* key, int value) {
     return MOE_ERR_ARG;
 }
 
-moe_status moe_profile_enable(int enable) {
+moe_status moe_profile_enable(int calls) {
     std::lock_guard<std::mutex> lock(g_prof_mu);
-    if (enable && !g_prof.created) {
-        for (int i = 0; i <= kMaxProf; ++i)
-            if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) return MOE_ERR_CUDA;
-        g_prof.created = true;
+    if (calls < 0 || calls > kMaxProfCalls) return MOE_ERR_ARG;
+    const int need = calls * (kMaxProf + 1);
+    if (need > g_prof.created) {
+        cudaEvent_t* ev = static_cast<cudaEvent_t*>(
+            std::realloc(g_prof.ev, sizeof(cudaEvent_t) * static_cast<size_t>(need)));
+        if (!ev) return MOE_ERR_ARG;
+        g_prof.ev = ev;
+        for (int i = g_prof.created; i < need; ++i) {
+            if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+                g_prof.created = i;
+                g_prof.capacity = 0;
+                return MOE_ERR_CUDA;
+            }
+        }
+        g_prof.created = need;
     }
-    g_prof.on = enable != 0;
-    g_prof.n = 0;
+    g_prof.capacity = calls;
+    g_prof.calls = 0;
+    g_prof.n = -1;
+    g_prof.n_first = 0;
     return MOE_OK;
 }
 
@@ -429,13 +463,21 @@ moe_status moe_profile_read(const char** names, float* ms, int cap, int* count) 
     std::lock_guard<std::mutex> lock(g_prof_mu);
     if (!count) return MOE_ERR_ARG;
     *count = 0;
-    if (!g_prof.created || g_prof.n == 0) return MOE_OK;
-    if (cudaEventSynchronize(g_prof.ev[g_prof.n]) != cudaSuccess) return MOE_ERR_CUDA;
-    const int n = g_prof.n < cap ? g_prof.n : cap;
+    const int calls = g_prof.calls, nk = g_prof.n_first;
+    if (calls == 0 || nk == 0) return MOE_OK;
+    cudaEvent_t* last = g_prof.ev + static_cast<size_t>(calls - 1) * (kMaxProf + 1);
+    if (cudaEventSynchronize(last[nk]) != cudaSuccess) return MOE_ERR_CUDA;
+    const int n = nk < cap ? nk : cap;
     for (int i = 0; i < n; ++i) {
+        double sum = 0.0;
+        for (int c = 0; c < calls; ++c) {
+            cudaEvent_t* e = g_prof.ev + static_cast<size_t>(c) * (kMaxProf + 1);
+            float t = 0.f;
+            if (cudaEventElapsedTime(&t, e[i], e[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+            sum += t;
+        }
         if (names) names[i] = g_prof.names[i];
-        if (ms && cudaEventElapsedTime(&ms[i], g_prof.ev[i], g_prof.ev[i + 1]) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (ms) ms[i] = static_cast<float>(sum / calls);
     }
     *count = n;
     return MOE_OK;

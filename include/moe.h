@@ -147,12 +147,15 @@ moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
  * Returns MOE_ERR_ARG for an unknown key or value. */
 moe_status moe_set_tuning(const char* key, int value);
 
-/* Optional per-kernel timing.  moe_profile_enable(1) makes later calls record
- * a CUDA event around every kernel they launch (on the call's stream);
- * moe_profile_read returns, for the most recent call, up to `cap` kernel
- * names (static strings) and their durations in milliseconds; it waits for
- * the last recorded event.  Returns the number of kernels through *count. */
-moe_status moe_profile_enable(int enable);
+/* Optional per-kernel timing.  moe_profile_enable(n) with n > 0 makes the
+ * next n calls of moe_route / moe_forward record a CUDA event before their
+ * first kernel and after each kernel, on the call's stream (events break the
+ * overlap of dependent launches, a few microseconds per kernel); n == 0
+ * turns recording off.  moe_profile_read waits for the last recorded event
+ * and returns, per kernel of those calls, its name (a static string) and its
+ * mean duration in milliseconds; *count receives the number of kernels.
+ * Not thread-safe against concurrent calls on other threads. */
+moe_status moe_profile_enable(int calls);
 moe_status moe_profile_read(const char** names, float* ms, int cap,
                             int* count);
 
