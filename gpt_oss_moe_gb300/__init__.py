@@ -26,7 +26,8 @@ MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_BAD_TILE = 0x1, 0x2, 0x4
 
 # Every function the C header declares, in order (checked by the tests).
 EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_forward",
-           "moe_get_device_status", "moe_clear_device_status",
+           "moe_forward_noalloc", "moe_get_device_status",
+           "moe_clear_device_status",
            "moe_set_tuning", "moe_profile_enable", "moe_profile_read",
            "moe_status_str")
 
@@ -71,6 +72,9 @@ def lib():
             L.moe_forward.argtypes = [S, vp, vp, vp, moe_weight, moe_weight, vp, i,
                                       vp, vp, vp, sz, vp]
             L.moe_forward.restype = i
+            L.moe_forward_noalloc.argtypes = [S, vp, vp, vp, moe_weight, moe_weight,
+                                              vp, i, vp, vp, vp, vp]
+            L.moe_forward_noalloc.restype = i
             L.moe_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
             L.moe_get_device_status.restype = i
             L.moe_clear_device_status.argtypes = [vp, vp]
@@ -158,6 +162,25 @@ def moe_forward(shape, hidden, router_w, router_b, w_gu, b_gu, w_d, b_d,
                              ws.numel(), _stream(stream))
     _check(code, "moe_forward")
     return ws
+
+
+def moe_forward_noalloc(shape, hidden, router_w, router_b, w_gu, b_gu, w_d, b_d,
+                        out, s_gu=None, s_d=None, topk_ids_out=None,
+                        topk_w_out=None, device_status_out=None, stream=None):
+    """The layer forward without a workspace, for callers that cannot
+    allocate device memory: the scratch is the library's own static device
+    array (shapes up to MOE_NOALLOC_SCRATCH_BYTES of scratch).  Calls share
+    that array, so calls that overlap on the GPU race."""
+    gu = moe_weight(_p(w_gu), _p(s_gu), _p(b_gu))
+    dn = moe_weight(_p(w_d), _p(s_d), _p(b_d))
+    out_f32 = 1 if out.dtype == torch.float32 else 0
+    if not out_f32 and out.dtype != torch.bfloat16:
+        raise ValueError("out must be float32 or bfloat16")
+    code = lib().moe_forward_noalloc(ctypes.byref(shape), _p(hidden), _p(router_w),
+                                     _p(router_b), gu, dn, _p(out), out_f32,
+                                     _p(topk_ids_out), _p(topk_w_out),
+                                     _p(device_status_out), _stream(stream))
+    _check(code, "moe_forward_noalloc")
 
 
 def moe_get_device_status(workspace: torch.Tensor) -> int:

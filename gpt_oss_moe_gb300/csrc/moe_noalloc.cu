@@ -1,0 +1,83 @@
+// moe_forward_noalloc: the layer forward for callers that cannot allocate
+// device memory.
+//
+// Some hosts hand a plugin only its input and output buffers and plan every
+// other byte of device memory themselves (a serving runtime with a fixed
+// memory budget, an embedded engine that forbids cudaMalloc after start-up,
+// or a thread where cudaMalloc's implicit synchronisation would stall other
+// work).  Such a caller cannot provide the workspace moe_forward asks for.
+// This entry point runs the same kernels as moe_forward but keeps their
+// scratch in one fixed-size array that lives in the library's own device
+// memory, so the call allocates nothing.
+//
+// The array is a file-scope `static __device__` object: every GPU that loads
+// the library holds its kNoallocScratchBytes until the process exits.  In
+// host code its name is only a host-side stand-in, never a device address, so
+// the first call on each device looks the real address up with
+// cudaGetSymbolAddress (with that device current) and caches it.
+#include <mutex>
+
+#include "moe_internal.cuh"
+#include "../../include/moe.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kNoallocScratchBytes = static_cast<size_t>(MOE_NOALLOC_SCRATCH_BYTES);
+constexpr int kMaxNoallocDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxNoallocDevices] = {};
+
+// Device address of the scratch array on the current device (set-up on the
+// first call per device).
+moe_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxNoallocDevices)
+        return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+            return MOE_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_forward_noalloc(const moe_shape* shape, const void* hidden,
+                                          const void* router_w, const void* router_b,
+                                          moe_weight gate_up, moe_weight down, void* out,
+                                          int out_is_fp32, int32_t* topk_ids_out,
+                                          float* topk_w_out, int32_t* device_status_out,
+                                          cudaStream_t stream) {
+    if (!shape) return MOE_ERR_ARG;
+    const size_t need = moe_workspace_bytes(shape);
+    if (need == 0) return shape->wfmt == MOE_W_BF16 || shape->wfmt == MOE_W_MXFP4
+                              ? MOE_ERR_SHAPE
+                              : MOE_ERR_ARG;
+    if (shape->T == 0) return MOE_OK;
+    if (need > moe::kNoallocScratchBytes) return MOE_ERR_WORKSPACE;
+    if (device_status_out && (reinterpret_cast<uintptr_t>(device_status_out) & 3u))
+        return MOE_ERR_ALIGN;
+    void* scratch = nullptr;
+    moe_status st = moe::noalloc_scratch(&scratch);
+    if (st != MOE_OK) return st;
+    // The array keeps the previous call's contents; only the status word must
+    // start from zero (every other region is fully rewritten by the kernels).
+    if (cudaMemsetAsync(scratch, 0, 256, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    st = moe_forward(shape, hidden, router_w, router_b, gate_up, down, out, out_is_fp32,
+                     topk_ids_out, topk_w_out, scratch, moe::kNoallocScratchBytes, stream);
+    if (st != MOE_OK) return st;
+    if (device_status_out &&
+        cudaMemcpyAsync(device_status_out, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                        stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}

@@ -131,6 +131,36 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden,
                        void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* Size of the library-owned scratch array used by moe_forward_noalloc
+ * (8 MiB per device that loads the library, held until the process exits). */
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* moe_forward for callers that cannot allocate device memory.  The source
+ * page has no counterpart of this call: it exists for hosts that give a
+ * plugin only its inputs and outputs and plan all other device memory
+ * themselves (or cannot afford cudaMalloc's implicit synchronisation), so
+ * they cannot provide moe_forward's workspace.
+ *   Arguments as for moe_forward, minus the workspace; device_status_out
+ *   (int32 [1], device memory, nullable) receives this call's device status
+ *   word (MOE_DEV_* bits) when the call's work completes.
+ * The scratch lives in one static device array of MOE_NOALLOC_SCRATCH_BYTES
+ * inside the library; the call allocates and frees nothing.  Shapes whose
+ * moe_workspace_bytes exceeds that size are rejected with MOE_ERR_WORKSPACE
+ * (at H = I = 2880 and top_k = 4 this admits up to T = 128 tokens).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and it keeps
+ * the last call's contents (the status word is cleared at the start of each
+ * call): calls whose work overlaps on the GPU -- on different streams, or
+ * from different threads -- race on it and must be serialised by the caller. */
+moe_status moe_forward_noalloc(const moe_shape* shape, const void* hidden,
+                               const void* router_w, const void* router_b,
+                               moe_weight gate_up, moe_weight down,
+                               void* out, int out_is_fp32,
+                               int32_t* topk_ids_out, float* topk_w_out,
+                               int32_t* device_status_out,
+                               cudaStream_t stream);
+
 /* Copies the device status word of `workspace` to *host_status.  This call
  * synchronises the calling thread with the device (cudaMemcpy).  Returns
  * MOE_ERR_DEVICE when the word is non-zero, MOE_OK otherwise. */
