@@ -3,7 +3,7 @@
 // the bias + top-k weighted combine fused into the down epilogue
 // (xserv docs/19-gpt-oss-moe.md, "Phase 19: gpt-oss-20b": §2 "MoE 前向"
 // step list gate_up -> bias -> GLU -> down -> bias -> weighted_sum; §1 table
-// "激活" row for the GLU).
+// "激活" row for the GLU; §5 "量化" for MXFP4 weights).
 //
 // Orientation.  The weight matrix is the MMA's A operand (M = 128 weight
 // rows per tile) and the tokens routed to one expert are the B operand
@@ -16,10 +16,13 @@
 // the units in order; units of one token tile are consecutive, so the
 // token tile stays hot in L2 while its 128-row weight blocks stream past.
 //
-// CTA = 6 warps:
+// CTA roles:
 //   warp 0      TMA producer (one lane): W tile [128 x 64] via a 3-D map
 //               (k, row, expert) and token tile [box x 64] via a 2-D map,
 //               both 128-byte swizzled, into a ring of `stages` slots.
+//               MXFP4: the W tile arrives as packed E2M1 codes [128 x 32 B]
+//               (unswizzled), and once per unit one bulk copy brings the
+//               unit's E8M0 scales [128 x K/32 B] (double-buffered).
 //   warp 1      TMEM owner + MMA issuer (one lane): 4 x (128 x N x 16)
 //               tcgen05.mma per slot into one of two TMEM accumulators.
 //   warps 2..5  epilogue (128 threads): tcgen05.ld of the accumulator, one
@@ -29,6 +32,12 @@
 //                              shfl.xor 1), clamp, GLU, bf16 store of h;
 //                 kEpiCombine: + bias, x routing weight, red.global.add.f32
 //                              into out[token, row].
+//   warps 6..9  (MXFP4 only) converters: thread r expands row r of the code
+//               tile to bf16 (E2M1 via byte-permute lookups -- every E2M1
+//               value is a normal bf16 -- times 2^(s-127), an exact bf16x2
+//               multiply), writes the 128-byte-swizzled A tile, fences the
+//               async proxy and arrives on the slot's "converted" barrier,
+//               which the MMA issuer waits for.
 // The two accumulators let the epilogue of one unit overlap the main loop
 // of the next.  Tails: weight rows past the matrix are zero-filled by TMA
 // and masked at the store; token rows past the tile are computed on
@@ -45,26 +54,36 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr uint32_t kATileBytes = kWeightTileRows * kBlockK * 2;  // 16 KB
+constexpr int kConvThreads = 256;   // two threads per weight row (half a row each)
+constexpr uint32_t kATileBytes = kWeightTileRows * kBlockK * 2;      // 16 KB bf16
+constexpr uint32_t kCodeTileBytes = kWeightTileRows * kBlockK / 2;   // 4 KB E2M1
 constexpr int kMaxStages = 12;
 
+template <int WF>
+constexpr int kThreadsOf = WF == 1 ? 192 + kConvThreads : 192;
+
 struct SmemPlan {
-    uint8_t* a;          // stages x 16 KB
-    uint8_t* b;          // stages x box*128 B
+    uint8_t* a;          // stages x 16 KB bf16 W tiles (1024-aligned)
+    uint8_t* b;          // stages x box*128 B token tiles (1024-aligned)
+    uint8_t* codes;      // stages x 4 KB E2M1 tiles (MXFP4)
+    uint8_t* scales;     // 2 x 128*kscale B (MXFP4)
     int* meta_tok;       // [box] token of each tile row (combine)
     float* meta_w;       // [box] routing weight of each tile row (combine)
-    uint64_t* full;      // [stages]
-    uint64_t* empty;     // [stages]
+    uint64_t* full;      // [stages] TMA landed
+    uint64_t* conv;      // [stages] A tile converted (MXFP4)
+    uint64_t* empty;     // [stages] MMAs done with the slot
     uint64_t* tfull;     // [2]
     uint64_t* tempty;    // [2]
+    uint64_t* sfull;     // [2] scales landed (MXFP4)
+    uint64_t* sempty;    // [2] scales consumed (MXFP4)
     uint64_t* drain;     // [1]
     uint32_t* tmem_base;
     int* flags;          // [0] abort, [1..2] epilogue broadcast (alternating)
 };
 
-__device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int box) {
+__device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int box, int wf,
+                                              int kscale) {
     SmemPlan s;
     const uint32_t base = smem_u32(raw);
     uint8_t* p = raw + ((1024u - (base & 1023u)) & 1023u);
@@ -72,16 +91,26 @@ __device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int box)
     p += static_cast<size_t>(stages) * kATileBytes;
     s.b = p;
     p += static_cast<size_t>(stages) * box * 128;
+    s.codes = p;
+    s.scales = p;
+    if (wf == 1) {
+        p += static_cast<size_t>(stages) * kCodeTileBytes;
+        s.scales = p;
+        p += 2 * ((kWeightTileRows * kscale + 15) / 16 * 16);
+    }
     s.meta_tok = reinterpret_cast<int*>(p);
     p += box * 4;
     s.meta_w = reinterpret_cast<float*>(p);
     p += box * 4;
     uint64_t* bars = reinterpret_cast<uint64_t*>(p);
     s.full = bars;
-    s.empty = bars + stages;
-    s.tfull = bars + 2 * stages;
+    s.conv = bars + stages;
+    s.empty = bars + 2 * stages;
+    s.tfull = bars + 3 * stages;
     s.tempty = s.tfull + 2;
-    s.drain = s.tempty + 2;
+    s.sfull = s.tempty + 2;
+    s.sempty = s.sfull + 2;
+    s.drain = s.sempty + 2;
     s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.flags = reinterpret_cast<int*>(s.tmem_base + 1);
     return s;
@@ -104,26 +133,78 @@ __device__ __forceinline__ float clamped_glu(float gate, float up) {
     return (up + 1.0f) * g;
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+// Eight E2M1 codes (one 32-bit word, element 2i in the low nibble of byte i)
+// to eight bf16 values times 2^(s-127).
+//
+// For the byte b of elements (2i, 2i+1), two integer multiplies place the
+// nibbles at the bf16 bit positions: b * (2^6 + 2^18) puts the magnitude bits
+// (exponent e, mantissa m) of the low nibble at bits 6..8 and of the high
+// nibble at 22..24; b * (2^12 + 2^24) puts their sign bits at 15 and 31.
+// Read as bf16, each half is then exactly e2m1(code) * 2^-126 -- a normal
+// number for e >= 1 and the subnormal 2^-127 for the code 0.5 (e = 0,
+// m = 1) -- so one exact bf16x2 multiply by 2^(s-1) yields
+// e2m1(code) * 2^(s-127).  The multiplies run on the FMA pipe, leaving the
+// integer pipe two masks and one byte extraction per pair.
+__device__ __forceinline__ uint4 e2m1x8_to_bf16(uint32_t w, uint32_t scale2, uint32_t scale2b) {
+    uint4 r;
+    uint32_t* rr = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t b = __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(i));
+        const uint32_t mag = (b * 0x00040040u) & 0x01C001C0u;
+        const uint32_t emb = mag | ((b * 0x01001000u) & 0x80008000u);
+        __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&emb),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&scale2));
+        if (scale2b != 0x3F803F80u)   // only for scales above 2^1 (s > 128)
+            v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&scale2b));
+        rr[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    return r;
+}
+
+// The factor(s) that turn an embedded code into e2m1(code) * 2^(s-127),
+// as bf16x2: 2^(s-1) when s <= 128 (bf16 exponent field s + 126), else
+// 2^127 then 2^(s-128).  Scale bytes 0 and 255 (zero, NaN) are not produced
+// by MX quantisers for weights and are not supported.
+__device__ __forceinline__ void e8m0_factors(uint32_t s, uint32_t& f1, uint32_t& f2) {
+    s &= 0xFFu;
+    if (s <= 128u) {
+        const uint32_t h = (s + 126u) << 7;
+        f1 = h | (h << 16);
+        f2 = 0x3F803F80u;                       // 1.0
+    } else {
+        const uint32_t h1 = 254u << 7;          // 2^127
+        const uint32_t h2 = (s - 1u) << 7;      // 2^(s-128)
+        f1 = h1 | (h1 << 16);
+        f2 = h2 | (h2 << 16);
+    }
+}
+
+template <int EPI, int WF>
+__global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     grouped_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x) {
     extern __shared__ uint8_t smem_raw[];
     const int stages = p.stages, box = p.token_box;
     const uint32_t b_bytes = static_cast<uint32_t>(box) * 128u;
-    SmemPlan sm = plan_smem(smem_raw, stages, box);
+    SmemPlan sm = plan_smem(smem_raw, stages, box, WF, p.kscale);
     volatile int* flags = sm.flags;
+    const uint32_t scale_buf_bytes =
+        static_cast<uint32_t>((kWeightTileRows * p.kscale + 15) / 16 * 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(sm.full + s), 1);
+            mbar_init(smem_u32(sm.conv + s), kConvThreads);
             mbar_init(smem_u32(sm.empty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(sm.tfull + b), 1);
             mbar_init(smem_u32(sm.tempty + b), kEpiThreads);
+            mbar_init(smem_u32(sm.sfull + b), 1);
+            mbar_init(smem_u32(sm.sempty + b), kConvThreads);
         }
         mbar_init(smem_u32(sm.drain), 1);
         flags[0] = 0;
@@ -155,14 +236,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
+            const uint32_t w_bytes = WF == 1 ? kCodeTileBytes : kATileBytes;
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
+            int local = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
                 const int4 t = p.tiles[u / p.n_wblocks];
                 if (!tile_ok(t, p)) continue;
                 const int mb = u % p.n_wblocks;
+                if (WF == 1) {
+                    // this unit's scale rows, one bulk copy, double-buffered
+                    const int sb = local & 1;
+                    const uint32_t sph = static_cast<uint32_t>(local >> 1) & 1u;
+                    if (!mbar_wait(smem_u32(sm.sempty + sb), sph ^ 1u, flags)) {
+                        raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    const int rows = min(kWeightTileRows, p.w_rows - mb * kWeightTileRows);
+                    const uint32_t bytes = static_cast<uint32_t>(rows * p.kscale);
+                    const uint32_t sf = smem_u32(sm.sfull + sb);
+                    mbar_arrive_expect_tx(sf, bytes);
+                    bulk_load(smem_u32(sm.scales + sb * scale_buf_bytes),
+                              p.scales + (static_cast<size_t>(t.x) * p.w_rows +
+                                          static_cast<size_t>(mb) * kWeightTileRows) * p.kscale,
+                              bytes, sf);
+                }
+                ++local;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
                         raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
@@ -170,9 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t fb = smem_u32(sm.full + stage);
-                    mbar_arrive_expect_tx(fb, kATileBytes + b_bytes);
-                    tma_load_3d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes), &tmap_w,
-                                fb, kb * kBlockK, mb * kWeightTileRows, t.x, pol_w);
+                    mbar_arrive_expect_tx(fb, w_bytes + b_bytes);
+                    if (WF == 1)
+                        tma_load_3d(smem_u32(sm.codes + static_cast<size_t>(stage) * kCodeTileBytes),
+                                    &tmap_w, fb, kb * (kBlockK / 2), mb * kWeightTileRows, t.x, pol_w);
+                    else
+                        tma_load_3d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
+                                    &tmap_w, fb, kb * kBlockK, mb * kWeightTileRows, t.x, pol_w);
                     tma_load_2d(smem_u32(sm.b + static_cast<size_t>(stage) * b_bytes), &tmap_x, fb,
                                 kb * kBlockK, t.y, pol_x);
                     ++issued;
@@ -194,6 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ph ^= 1u;
                     }
                     mbar_wait(smem_u32(sm.full + s), ph, nullptr);
+                }
+                if (WF == 1 && local > 0) {
+                    const int sb = (local - 1) & 1;
+                    mbar_wait(smem_u32(sm.sfull + sb), static_cast<uint32_t>((local - 1) >> 1) & 1u,
+                              nullptr);
                 }
             }
         }
@@ -220,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * acc_stride;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(smem_u32(sm.full + stage), phase, flags)) {
+                    const uint32_t ready = smem_u32((WF == 1 ? sm.conv : sm.full) + stage);
+                    if (!mbar_wait(ready, phase, flags)) {
                         raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                         ok = false;
                         break;
@@ -247,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(smem_u32(sm.drain));
             mbar_wait(smem_u32(sm.drain), 0, nullptr);
         }
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------ epilogue
         const int ep = threadIdx.x - 64;          // 0..127
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
@@ -329,6 +441,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(sm.tempty + buf));
         }
+    } else if (WF == 1) {
+        // ------------------------------------------------ MXFP4 converters
+        const int ct = threadIdx.x - 192;         // 0..255
+        const int r = ct & 127;                   // weight row within the tile
+        const int half = ct >> 7;                 // chunks 4*half .. 4*half+3 of the row
+        const uint32_t a_row_off = static_cast<uint32_t>(r) * 128u;
+        const uint32_t swz = static_cast<uint32_t>(r & 7);
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+            const int4 t = p.tiles[u / p.n_wblocks];
+            if (!tile_ok(t, p)) continue;
+            const int sb = local & 1;
+            const uint32_t sph = static_cast<uint32_t>(local >> 1) & 1u;
+            ++local;
+            if (!mbar_wait(smem_u32(sm.sfull + sb), sph, flags)) {
+                raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                break;
+            }
+            const uint8_t* srow = sm.scales + sb * scale_buf_bytes + r * p.kscale;
+            // rows past the matrix: codes are TMA zero-fill and no scale bytes
+            // were copied for them; use scale 1 so they stay exactly zero
+            const bool row_ok = (u % p.n_wblocks) * kWeightTileRows + r < p.w_rows;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait(smem_u32(sm.full + stage), phase, flags)) {
+                    raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                uint32_t f1, f2;
+                e8m0_factors(row_ok ? srow[2 * kb + half] : 127u, f1, f2);
+                const uint4 cw = *reinterpret_cast<const uint4*>(
+                    sm.codes + static_cast<size_t>(stage) * kCodeTileBytes + r * 32 + half * 16);
+                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                uint8_t* arow = sm.a + static_cast<size_t>(stage) * kATileBytes + a_row_off;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t chunk = static_cast<uint32_t>(4 * half + c);
+                    const uint4 v = e2m1x8_to_bf16(words[c], f1, f2);
+                    *reinterpret_cast<uint4*>(arow + ((chunk ^ swz) << 4)) = v;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(sm.conv + stage));
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            mbar_arrive(smem_u32(sm.sempty + sb));
+        }
     }
 
     tc_fence_before();
@@ -339,15 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-}  // namespace
-
-cudaError_t launch_gemm(int epi, const GemmParams& p, const CUtensorMap* tmap_w,
-                        const CUtensorMap* tmap_x, int grid, size_t smem, cudaStream_t s,
-                        bool pdl) {
-    if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
+template <int EPI, int WF>
+cudaError_t launch_gemm_t(const GemmParams& p, const CUtensorMap* tmap_w, const CUtensorMap* tmap_x,
+                          int grid, size_t smem, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreadsOf<WF>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -355,19 +517,24 @@ cudaError_t launch_gemm(int epi, const GemmParams& p, const CUtensorMap* tmap_w,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cudaError_t err;
-    if (epi == kEpiGlu) {
-        err = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiGlu>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(smem));
-        if (err != cudaSuccess) return err;
-        return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kEpiGlu>, p, *tmap_w, *tmap_x);
-    }
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiCombine>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, WF>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kEpiCombine>, p, *tmap_w, *tmap_x);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI, WF>, p, *tmap_w, *tmap_x);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int epi, int wf, const GemmParams& p, const CUtensorMap* tmap_w,
+                        const CUtensorMap* tmap_x, int grid, size_t smem, cudaStream_t s,
+                        bool pdl) {
+    if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
+    if (epi == kEpiGlu)
+        return wf == 1 ? launch_gemm_t<kEpiGlu, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
+                       : launch_gemm_t<kEpiGlu, 0>(p, tmap_w, tmap_x, grid, smem, s, pdl);
+    return wf == 1 ? launch_gemm_t<kEpiCombine, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
+                   : launch_gemm_t<kEpiCombine, 0>(p, tmap_w, tmap_x, grid, smem, s, pdl);
 }
 
 // fp32 -> bf16 (round to nearest even) of the combined output.

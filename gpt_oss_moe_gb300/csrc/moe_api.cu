@@ -67,18 +67,32 @@ moe_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     return MOE_OK;
 }
 
-// bf16 tensor, 128-byte swizzle, box inner extent 64 elements (128 B).
+// bf16 tensors use the 128-byte swizzle (box inner extent 64 elements =
+// 128 B); MXFP4 code tensors are plain bytes without swizzle.
 moe_status make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-                     const cuuint64_t* strides, const cuuint32_t* box) {
+                     const cuuint64_t* strides, const cuuint32_t* box, bool bytes = false) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     moe_status st = encode_fn(&enc);
     if (st != MOE_OK) return st;
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
-                     const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// 3-D map over one expert weight bank [E, rows, K]: bf16 values or MXFP4
+// codes (K/2 bytes per row); box = 64 K elements x 128 rows x 1 expert.
+moe_status weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K, bool mxfp4) {
+    const cuuint64_t row_bytes = mxfp4 ? static_cast<cuuint64_t>(K) / 2
+                                       : static_cast<cuuint64_t>(K) * 2;
+    const cuuint64_t dims[3] = {mxfp4 ? static_cast<cuuint64_t>(K) / 2 : static_cast<cuuint64_t>(K),
+                                static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(E)};
+    const cuuint64_t str[2] = {row_bytes, row_bytes * static_cast<cuuint64_t>(rows)};
+    const cuuint32_t boxd[3] = {mxfp4 ? 32u : 64u, 128u, 1u};
+    return make_tmap(m, w, 3, dims, str, boxd, mxfp4);
 }
 
 // ------------------------------------------------------------ tuning
@@ -184,43 +198,76 @@ struct Routing {
 moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, const void* hidden,
                           const void* router_w, const void* router_b, const Routing& r,
                           float* zero_out, __nv_bfloat16* x_perm, int token_tile,
-                          cudaStream_t stream) {
+                          const DevInfo& dev, cudaStream_t stream) {
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    const int nb = (s.T + kRouterTokens - 1) / kRouterTokens;
+
+    // Router operands through TMA: x [T, H] box 64 x 32, Wr [E, H] box 64 x E_pad.
+    CUtensorMap tm_x, tm_wr;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.T)};
+        const cuuint64_t str[1] = {static_cast<cuuint64_t>(s.H) * 2};
+        const cuuint32_t boxd[2] = {64, static_cast<cuuint32_t>(kRouterTokens)};
+        MOE_TRY(make_tmap(&tm_x, hidden, 2, dims, str, boxd));
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.E)};
+        const cuuint64_t str[1] = {static_cast<cuuint64_t>(s.H) * 2};
+        const cuuint32_t boxd[2] = {64, static_cast<cuuint32_t>(kRouterTokens)};
+        MOE_TRY(make_tmap(&tm_wr, router_w, 2, dims, str, boxd));
+    }
+    const int nchunks = s.H / kBlockK;
+    const size_t fixed = router_smem_bytes(0);
+    int stages = static_cast<int>((static_cast<size_t>(dev.max_smem) - fixed) /
+                                  router_stage_bytes());
+    if (stages > router_max_stages()) stages = router_max_stages();
+    if (stages > nchunks) stages = nchunks;
+    if (stages < 1) return MOE_ERR_UNSUPPORTED;
+
     RouterParams rp{};
-    rp.x = static_cast<const __nv_bfloat16*>(hidden);
-    rp.wr = static_cast<const __nv_bfloat16*>(router_w);
     rp.br = static_cast<const __nv_bfloat16*>(router_b);
     rp.T = s.T;
     rp.H = s.H;
     rp.E = s.E;
     rp.top_k = s.top_k;
+    rp.nblocks = nb;
+    rp.egroups = (s.E + 31) / 32;
+    rp.stages = stages;
+    rp.logits = reinterpret_cast<float*>(ws + L.logits);
+    rp.blk_counter = reinterpret_cast<int32_t*>(ws + L.blk_counter);
     rp.topk_ids = r.ids;
     rp.topk_w = r.w;
     rp.blk_cnt = reinterpret_cast<int32_t*>(ws + L.blk_cnt);
-    rp.zero_out = zero_out;
+    rp.offsets = r.offsets;
+    rp.tiles = reinterpret_cast<int4*>(ws + L.tiles);
+    rp.max_tiles = L.max_tiles;
+    rp.token_tile = token_tile;
     rp.status = status;
-    MOE_CUDA(launch_router(rp, stream));
+    MOE_CUDA(launch_router(rp, &tm_x, &tm_wr, router_smem_bytes(stages), stream));
     prof_mark("router_topk", stream);
 
     PermuteParams pp{};
     pp.topk_ids = r.ids;
-    pp.blk_cnt = rp.blk_cnt;
-    pp.x = rp.x;
+    pp.blk_base = rp.blk_cnt;
+    pp.offsets = r.offsets;
+    pp.x = static_cast<const __nv_bfloat16*>(hidden);
     pp.T = s.T;
     pp.H = s.H;
     pp.E = s.E;
     pp.top_k = s.top_k;
-    pp.nblocks = (s.T + kRouterTokens - 1) / kRouterTokens;
-    pp.token_tile = token_tile;
-    pp.offsets = r.offsets;
+    pp.nblocks = nb;
+    const int rows_per_block = (s.T < kRouterTokens ? s.T : kRouterTokens) * s.top_k;
+    int g = (x_perm || zero_out) ? (2 * dev.sms + nb - 1) / nb : 1;
+    if (g > 32) g = 32;
+    if (g > rows_per_block) g = rows_per_block;
+    pp.gather_split = g < 1 ? 1 : g;
+    pp.zero_out = zero_out;
     pp.sorted_assign = r.sorted_assign;
     pp.assign_row = reinterpret_cast<int32_t*>(ws + L.assign_row);
-    pp.tiles = reinterpret_cast<int4*>(ws + L.tiles);
-    pp.max_tiles = L.max_tiles;
     pp.x_perm = x_perm;
     pp.status = status;
     MOE_CUDA(launch_permute(pp, stream, g_pdl.load() != 0));
-    prof_mark("permute_gather", stream);
+    prof_mark(x_perm ? "permute_gather" : "permute", stream);
     return MOE_OK;
 }
 
@@ -265,7 +312,7 @@ moe_status moe_route(const moe_shape* shape, const void* hidden, const void* rou
     std::lock_guard<std::mutex> lock(g_prof_mu);
     prof_reset(stream);
     const moe_status st = launch_routing(s, L, ws, hidden, router_w, router_b, r, nullptr,
-                                         nullptr, auto_token_tile(s.T), stream);
+                                         nullptr, auto_token_tile(s.T), dev, stream);
     prof_finish();
     return st;
 }
@@ -286,10 +333,10 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     MOE_TRY(check_ptr(down.bias));
     MOE_TRY(check_ptr(out));
     MOE_TRY(check_ptr(workspace));
-    if (s.wfmt == MOE_W_MXFP4) {
+    const bool mxfp4 = s.wfmt == MOE_W_MXFP4;
+    if (mxfp4) {
         MOE_TRY(check_ptr(gate_up.scale));
         MOE_TRY(check_ptr(down.scale));
-        return MOE_ERR_UNSUPPORTED;
     }
     if ((topk_ids_out && !aligned16(topk_ids_out)) || (topk_w_out && !aligned16(topk_w_out)))
         return MOE_ERR_ALIGN;
@@ -305,14 +352,15 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     const bool pdl = g_pdl.load() != 0;
 
     // Pipeline depth: as many stages as the shared memory allows (2..12).
-    const size_t stage_bytes = static_cast<size_t>(kWeightTileRows) * kBlockK * 2 +
-                               static_cast<size_t>(box) * kBlockK * 2;
-    const size_t fixed = gemm_smem_bytes(0, box);
+    const int wf = mxfp4 ? 1 : 0;
+    const int kscale_max = (s.H > s.I ? s.H : s.I) / 32;
+    const size_t stage_bytes = gemm_stage_bytes(box, wf);
+    const size_t fixed = gemm_fixed_bytes(box, wf, kscale_max);
     const size_t budget = static_cast<size_t>(dev.max_smem) - 1024;
     if (budget < fixed + 2 * stage_bytes) return MOE_ERR_UNSUPPORTED;
     int stages = static_cast<int>((budget - fixed) / stage_bytes);
     if (stages > 12) stages = 12;
-    const size_t smem = gemm_smem_bytes(stages, box) + 1024;
+    const size_t smem = fixed + stages * stage_bytes + 1024;
     const int tmem_cols = next_pow2(2 * box < 32 ? 32 : 2 * box);
 
     __nv_bfloat16* x_perm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm);
@@ -321,22 +369,8 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
 
     // Tensor maps (host-side descriptors; cheap to build per call).
     CUtensorMap tm_wgu, tm_x, tm_wd, tm_h;
-    {
-        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(2 * s.I),
-                                    static_cast<cuuint64_t>(s.E)};
-        const cuuint64_t str[2] = {static_cast<cuuint64_t>(s.H) * 2,
-                                   static_cast<cuuint64_t>(2 * s.I) * s.H * 2};
-        const cuuint32_t boxd[3] = {64, 128, 1};
-        MOE_TRY(make_tmap(&tm_wgu, gate_up.w, 3, dims, str, boxd));
-    }
-    {
-        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.I), static_cast<cuuint64_t>(s.H),
-                                    static_cast<cuuint64_t>(s.E)};
-        const cuuint64_t str[2] = {static_cast<cuuint64_t>(s.I) * 2,
-                                   static_cast<cuuint64_t>(s.H) * s.I * 2};
-        const cuuint32_t boxd[3] = {64, 128, 1};
-        MOE_TRY(make_tmap(&tm_wd, down.w, 3, dims, str, boxd));
-    }
+    MOE_TRY(weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H, mxfp4));
+    MOE_TRY(weight_tmap(&tm_wd, down.w, s.E, s.H, s.I, mxfp4));
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(R)};
         const cuuint64_t str[1] = {static_cast<cuuint64_t>(s.H) * 2};
@@ -358,7 +392,8 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     r.w = topk_w_out ? topk_w_out : reinterpret_cast<float*>(ws + L.topk_w);
     r.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
     r.sorted_assign = reinterpret_cast<int32_t*>(ws + L.sorted_assign);
-    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r, out32, x_perm, box, stream));
+    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r, out32, x_perm, box, dev,
+                           stream));
 
     GemmParams g{};
     g.tiles = reinterpret_cast<const int4*>(ws + L.tiles);
@@ -376,9 +411,11 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.w_rows = 2 * s.I;
     g.bias = static_cast<const __nv_bfloat16*>(gate_up.bias);
     g.h = h;
+    g.scales = static_cast<const uint8_t*>(gate_up.scale);
+    g.kscale = s.H / 32;
     int grid = L.max_tiles * g.n_wblocks;
     if (grid > dev.sms) grid = dev.sms;
-    MOE_CUDA(launch_gemm(kEpiGlu, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
+    MOE_CUDA(launch_gemm(kEpiGlu, wf, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
     prof_mark("gate_up_glu", stream);
 
     // down + bias + weighted combine -> out (fp32 accumulation)
@@ -391,9 +428,11 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.sorted_assign = r.sorted_assign;
     g.topk_w = r.w;
     g.top_k = s.top_k;
+    g.scales = static_cast<const uint8_t*>(down.scale);
+    g.kscale = s.I / 32;
     grid = L.max_tiles * g.n_wblocks;
     if (grid > dev.sms) grid = dev.sms;
-    MOE_CUDA(launch_gemm(kEpiCombine, g, &tm_wd, &tm_h, grid, smem, stream, pdl));
+    MOE_CUDA(launch_gemm(kEpiCombine, wf, g, &tm_wd, &tm_h, grid, smem, stream, pdl));
     prof_mark("down_combine", stream);
 
     if (!out_is_fp32) {

@@ -19,13 +19,15 @@ constexpr int kWeightTileRows = 128;   // MMA M: weight rows per tile
 constexpr int kMaxTokenTile = 256;     // MMA N upper bound
 
 // Status region: word 0 is the device status word (MOE_DEV_* bits),
-// word 1 the number of GEMM token tiles written by the permutation kernel.
+// word 1 the number of GEMM token tiles written by the router kernel,
+// word 2 the router's grid-completion counter (zero between calls).
 constexpr int kStatusWord = 0;
 constexpr int kNumTilesWord = 1;
+constexpr int kGridCounterWord = 2;
 
 struct WsLayout {
-    size_t status, topk_ids, topk_w, blk_cnt, offsets, sorted_assign, assign_row;
-    size_t tiles, x_perm, h, out_acc, total;
+    size_t status, topk_ids, topk_w, blk_cnt, logits, blk_counter, offsets;
+    size_t sorted_assign, assign_row, tiles, x_perm, h, out_acc, total;
     int max_tiles;
 };
 
@@ -46,6 +48,8 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
     L.topk_ids = take(R * 4);
     L.topk_w = take(R * 4);
     L.blk_cnt = take(nb * E * 4);
+    L.logits = take(E > 32 ? nb * kRouterTokens * E * 4 : 0);
+    L.blk_counter = take(E > 32 ? nb * 4 : 0);
     L.offsets = take((E + 1) * 4);
     L.sorted_assign = take(R * 4);
     L.assign_row = take(R * 4);
@@ -60,30 +64,36 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
 // ------------------------------------------------------------ router (K1)
 
 struct RouterParams {
-    const __nv_bfloat16* x;      // [T, H]
-    const __nv_bfloat16* wr;     // [E, H]
     const __nv_bfloat16* br;     // [E]
     int T, H, E, top_k;
+    int nblocks;                 // grid = (nblocks token blocks of 32, egroups of 32 experts)
+    int egroups;
+    int stages;                  // TMA ring depth
+    float* logits;               // [nblocks, 32, E] when egroups > 1
+    int32_t* blk_counter;        // [nblocks] when egroups > 1, zero between calls
     int32_t* topk_ids;           // [T, k]
     float* topk_w;               // [T, k]
-    int32_t* blk_cnt;            // [nblocks, E]
-    float* zero_out;             // [T, H] fp32 rows to clear, or null
-    int32_t* status;
+    int32_t* blk_cnt;            // [E, nblocks]: counts, then (after the
+                                 // last block) the exclusive prefix per expert
+    int32_t* offsets;            // [E+1]
+    int4* tiles;                 // GEMM token tiles (expert, first row, rows, 0)
+    int max_tiles;
+    int token_tile;              // rows of tokens per GEMM tile
+    int32_t* status;             // status region (status word, tile count, counter)
 };
 
 // ------------------------------------------------------------ permutation (K2)
 
 struct PermuteParams {
     const int32_t* topk_ids;     // [T, k]
-    const int32_t* blk_cnt;      // [nblocks, E]
+    const int32_t* blk_base;     // [E, nblocks] exclusive prefix per expert
+    const int32_t* offsets;      // [E+1]
     const __nv_bfloat16* x;      // [T, H]
     int T, H, E, top_k, nblocks;
-    int token_tile;              // rows of tokens per GEMM tile
-    int32_t* offsets;            // [E+1]
+    int gather_split;            // CTAs per 32-token block (grid.y)
+    float* zero_out;             // [T, H] fp32 rows to clear, or null
     int32_t* sorted_assign;      // [T*k]
     int32_t* assign_row;         // [T*k]
-    int4* tiles;                 // (expert, first row, rows, 0)
-    int max_tiles;
     __nv_bfloat16* x_perm;       // [T*k, H] or null (no gather)
     int32_t* status;
 };
@@ -103,6 +113,8 @@ struct GemmParams {
     int tmem_cols;               // allocated TMEM columns (2 accumulators)
     int num_experts;             // E (tile bounds check)
     int rows_total;              // T * k (tile bounds check)
+    const uint8_t* scales;       // MXFP4: E8M0 [E, w_rows, kscale]
+    int kscale;                  // MXFP4: scale bytes per weight row (K / 32)
     const __nv_bfloat16* bias;   // [E, w_rows]
     // kEpiGlu: h[row, w_rows/2] bf16
     __nv_bfloat16* h;
@@ -114,19 +126,31 @@ struct GemmParams {
     int32_t* status;
 };
 
-// Shared memory used by one GEMM CTA (bytes, excluding the 1 KB alignment slack).
-inline size_t gemm_smem_bytes(int stages, int token_box) {
+// Shared memory of one GEMM pipeline stage and of the fixed part (bytes,
+// excluding the 1 KB alignment slack).  wf: 0 = bf16, 1 = MXFP4.
+inline size_t gemm_stage_bytes(int token_box, int wf) {
     size_t a = static_cast<size_t>(kWeightTileRows) * kBlockK * 2;
     size_t b = static_cast<size_t>(token_box) * kBlockK * 2;
+    size_t codes = wf == 1 ? static_cast<size_t>(kWeightTileRows) * kBlockK / 2 : 0;
+    return a + b + codes;
+}
+inline size_t gemm_fixed_bytes(int token_box, int wf, int kscale) {
+    size_t scales = wf == 1 ? 2 * align_up(static_cast<size_t>(kWeightTileRows) * kscale, 16) : 0;
     size_t meta = static_cast<size_t>(token_box) * 8;
-    size_t bars = 256;
-    return stages * (a + b) + meta + bars;
+    size_t bars = 512;
+    return scales + meta + bars;
 }
 
 // Kernel launchers (defined next to each kernel).
-cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
+// Router: x [T, H] and Wr [E, H] through 2-D tensor maps (box 64 x 32,
+// 128-byte swizzle); each CTA covers 32 tokens x 32 experts.
+size_t router_stage_bytes();
+size_t router_smem_bytes(int stages);
+int router_max_stages();
+cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tmap_x,
+                          const CUtensorMap* tmap_wr, size_t smem, cudaStream_t s);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s, bool pdl);
-cudaError_t launch_gemm(int epi, const GemmParams& p, const CUtensorMap* tmap_w,
+cudaError_t launch_gemm(int epi, int wf, const GemmParams& p, const CUtensorMap* tmap_w,
                         const CUtensorMap* tmap_x, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, size_t n, cudaStream_t s,

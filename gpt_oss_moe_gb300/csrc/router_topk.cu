@@ -1,22 +1,34 @@
 // Router Linear + bias, top-k selection and softmax over the selected logits,
-// fused in one kernel (xserv docs/19-gpt-oss-moe.md, "Phase 19: gpt-oss-20b":
-// §1 table "MoE" row -- the router is a plain Linear [2880 -> 32] with bias;
-// §2 "MoE 前向" -- router GEMV then topk_softmax on the GPU, ids stay there).
+// the per-expert counts and the expert offsets / GEMM tile list, in one
+// launch (xserv docs/19-gpt-oss-moe.md, "Phase 19: gpt-oss-20b": §1 table
+// "MoE" row -- the router is a plain Linear [2880 -> 32] with bias; §2
+// "MoE 前向" -- router GEMV then topk_softmax on the GPU, ids stay there).
 //
-// One CTA of 128 threads handles 32 tokens against all E experts.  The
-// logits are an fp32-accumulated bf16 contraction on the tensor cores
-// (mma.sync m16n8k16; the router is ~0.1% of the layer's flops, far too
-// small for a TMEM pipeline).  Operands are staged through shared memory in
-// 64-wide K chunks with cp.async double buffering.  Each warp then takes
-// 8 tokens and selects the top k with a warp argmax (higher logit first,
-// equal logits -> lower expert index), computes the softmax over the k
-// selected logits (max-subtracted, expf), and counts the assignments per
-// expert for the permutation kernel.  Optionally clears the fp32 output rows
-// of its tokens, which the down-projection epilogue accumulates into.
+// Grid (token blocks of 32, expert groups of 32).  CTA (b, g) computes the
+// logits of tokens [32b, 32b+32) for experts [32g, 32g+32) as an
+// fp32-accumulated bf16 contraction on the tensor cores (mma.sync m16n8k16;
+// the router is ~0.1% of the layer's flops, far too small for a TMEM
+// pipeline).  A producer warp streams 64-wide K chunks of x and Wr through a
+// TMA ring (128-byte swizzle) as deep as shared memory allows; each of the
+// four compute warps owns every fourth chunk, so four independent MMA chains
+// run at once and no block-wide barrier sits in the loop.  The four partial
+// sums are added in warp order (the same order every run).
+// With more than one expert group, each CTA stores its logit columns and the
+// last group of the token block to finish (an atomic ticket -- no waiting)
+// gathers the full rows.  That CTA then
+//   * selects the top k per token (thread t of warp 0 takes token t) by
+//     insertion: higher logit first, equal logits -> lower expert index;
+//   * computes the softmax over the k selected logits (max-subtracted, expf);
+//   * counts its assignments per expert;
+//   * takes a second ticket; the last token block turns the per-block counts
+//     into per-expert exclusive prefixes, scans the totals into expert
+//     offsets and writes the GEMM token-tile list.
+// Every ticket counter is reset by the CTA that takes the last ticket, so the
+// counters are zero between calls.
 //
-// Tails: rows past T and experts past E are zero-filled by cp.async (source
-// size 0) and masked out of the selection; every thread reaches every
-// barrier (no early exit before a __syncthreads, the failure mode of §4).
+// Tails: rows past T and experts past E are zero-filled by TMA and masked
+// out of the selection; a CTA leaves early only as a whole, right after a
+// barrier (the failure mode of §4).  Every wait is bounded.
 #include <cfloat>
 #include <climits>
 
@@ -27,29 +39,21 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kRowStride = kBlockK + 8;  // padded smem row (bf16): 144 B, conflict-free ldmatrix
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
-                 ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+constexpr int kComputeWarps = 4;
+constexpr int kThreads = (kComputeWarps + 1) * 32;   // + one producer warp
+constexpr int kMaxStages = 24;
+constexpr int kGroup = 32;                            // experts per CTA
+constexpr uint32_t kTileBytes = kRouterTokens * kBlockK * 2;   // 4 KB (x or w tile)
+constexpr uint32_t kStageBytes = 2 * kTileBytes;
+constexpr int kPartStride = kGroup + 1;                // padded row of partial logits
+// logits of the top-k CTA: [32][E + 1] floats, E <= 256
+constexpr uint32_t kLogitsBytes = kRouterTokens * (kMaxExperts + 1) * 4;
+constexpr uint32_t kPartialBytes = kComputeWarps * kRouterTokens * kPartStride * 4;
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                             uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
-                 : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
                                                uint32_t b0, uint32_t b1) {
@@ -60,206 +64,368 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// NTW: n-tiles of 8 experts per warp; the CTA covers E_pad = 32 * NTW experts.
-template <int NTW>
-__global__ void __launch_bounds__(kThreads) router_topk_kernel(const RouterParams p) {
-    constexpr int kEPad = 32 * NTW;
-    extern __shared__ __align__(16) uint8_t smem[];
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);            // [2][32][72]
-    __nv_bfloat16* ws = xs + 2 * kRouterTokens * kRowStride;                // [2][E_pad][72]
-    int* hist = reinterpret_cast<int*>(ws + 2 * kEPad * kRowStride);        // [256]
-    float* logits = reinterpret_cast<float*>(ws);                           // [32][E_pad+1], reuses ws
+// Byte offset of the 16-byte chunk `c` (0..7) of row `r` in a tile written
+// by TMA with the 128-byte swizzle (rows of 128 B, 1024-byte aligned tile).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ int warp_inclusive_scan(int v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+    }
+    return v;
+}
+
+// Exclusive scan of vals[0..n) (n <= 256) by one warp; out[0..n] with
+// out[n] = total.
+__device__ __forceinline__ void warp_exclusive_scan256(const int* vals, int* out, int n) {
+    const int lane = threadIdx.x & 31;
+    int local[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = lane * 8 + i;
+        local[i] = idx < n ? vals[idx] : 0;
+        sum += local[i];
+    }
+    const int incl = warp_inclusive_scan(sum);
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = lane * 8 + i;
+        if (idx < n) out[idx] = run;
+        run += local[i];
+    }
+    const int all = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) out[n] = all;
+}
+
+// Last CTA of the grid: per-expert exclusive prefix over token blocks, expert
+// offsets, GEMM token tiles.
+__device__ void finish_routing(const RouterParams& p, int* total_s, int* offs_s, int* tcnt_s,
+                               int* toff_s) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kWarps = kThreads / 32;
+    const int E = p.E, nb = p.nblocks;
+    // Per warp pass: 4 experts x up to 8 chunks of 32 blocks, all loads in
+    // flight before the scans.
+    constexpr int kQ = 4, kC = 8;
+    for (int e0 = warp * kQ; e0 < E; e0 += kQ * kWarps) {
+        int carry[kQ] = {0, 0, 0, 0};
+        for (int bs = 0; bs < nb; bs += 32 * kC) {
+            const int nchunk = min(kC, (nb - bs + 31) / 32);   // chunks holding real blocks
+            int v[kQ][kC];
+#pragma unroll
+            for (int q = 0; q < kQ; ++q)
+#pragma unroll
+                for (int c = 0; c < kC; ++c) {
+                    const int e = e0 + q, b = bs + c * 32 + lane;
+                    v[q][c] = (e < E && b < nb) ? __ldcg(p.blk_cnt + static_cast<size_t>(e) * nb + b)
+                                                : 0;
+                }
+#pragma unroll
+            for (int q = 0; q < kQ; ++q)
+#pragma unroll
+                for (int c = 0; c < kC; ++c) {
+                    if (c >= nchunk) break;
+                    const int e = e0 + q, b = bs + c * 32 + lane;
+                    const int incl = warp_inclusive_scan(v[q][c]);
+                    if (e < E && b < nb)
+                        p.blk_cnt[static_cast<size_t>(e) * nb + b] = carry[q] + incl - v[q][c];
+                    carry[q] += __shfl_sync(0xffffffffu, incl, 31);
+                }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < kQ; ++q)
+                if (e0 + q < E) total_s[e0 + q] = carry[q];
+        }
+    }
+    __syncthreads();
+    if (warp == 0) warp_exclusive_scan256(total_s, offs_s, E);
+    __syncthreads();
+    for (int e = tid; e <= E; e += kThreads) p.offsets[e] = offs_s[e];
+    for (int e = tid; e < E; e += kThreads)
+        tcnt_s[e] = (total_s[e] + p.token_tile - 1) / p.token_tile;
+    __syncthreads();
+    if (warp == 0) warp_exclusive_scan256(tcnt_s, toff_s, E);
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) {
+        const int m = total_s[e];
+        if (m == 0) continue;
+        const int nt = tcnt_s[e];
+        const int per = ((m + nt - 1) / nt + 15) / 16 * 16;
+        for (int i = 0; i < nt; ++i) {
+            const int slot = toff_s[e] + i;
+            if (slot < p.max_tiles)
+                p.tiles[slot] = make_int4(e, offs_s[e] + i * per, min(per, m - i * per), 0);
+            else
+                atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
+        }
+    }
+    if (tid == 0) {
+        p.status[kNumTilesWord] = min(toff_s[E], p.max_tiles);
+        p.status[kGridCounterWord] = 0;   // ready for the next call
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    router_topk_kernel(const RouterParams p, const __grid_constant__ CUtensorMap tmap_x,
+                       const __grid_constant__ CUtensorMap tmap_wr) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int S = p.stages;
+    const size_t ring_bytes = static_cast<size_t>(S) * kStageBytes;
+    const size_t region = ring_bytes > kLogitsBytes ? ring_bytes : kLogitsBytes;
+    uint8_t* ring = smem;                                                   // [S][x | w]
+    float* logits = reinterpret_cast<float*>(smem);                         // after the loop
+    float* partial = reinterpret_cast<float*>(smem + region);               // [4][32][33]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + region + kPartialBytes);
+    uint64_t* empty = full + kMaxStages;
+    int* hist = reinterpret_cast<int*>(empty + kMaxStages);                 // [256]
+    int* scan_a = hist + kMaxExperts;                                       // [257]
+    int* scan_b = scan_a + kMaxExperts + 1;                                 // [256]
+    int* scan_c = scan_b + kMaxExperts;                                     // [257]
+    volatile int* flag = scan_c + kMaxExperts + 1;                          // [3]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t0 = blockIdx.x * kRouterTokens;
-    const int H = p.H, E = p.E;
-    const int nchunks = H / kBlockK;
+    const int b = blockIdx.x, g = blockIdx.y;
+    const int t0 = b * kRouterTokens;
+    const int E = p.E;
+    const int nchunks = p.H / kBlockK;
 
     for (int e = tid; e < kMaxExperts; e += kThreads) hist[e] = 0;
-
-    auto load_chunk = [&](int c, int buf) {
-        const int k0 = c * kBlockK;
-        // activations: 32 rows x 8 segments of 16 B
-        for (int i = tid; i < kRouterTokens * 8; i += kThreads) {
-            const int r = i >> 3, seg = i & 7;
-            const int t = t0 + r;
-            const bool ok = t < p.T;
-            const __nv_bfloat16* src = p.x + static_cast<size_t>(ok ? t : 0) * H + k0 + seg * 8;
-            cp_async16(smem_u32(xs + (buf * kRouterTokens + r) * kRowStride + seg * 8), src, ok);
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(full + s), 1);
+            mbar_init(smem_u32(empty + s), 1);
         }
-        // router weights: E_pad rows x 8 segments
-        for (int i = tid; i < kEPad * 8; i += kThreads) {
-            const int r = i >> 3, seg = i & 7;
-            const bool ok = r < E;
-            const __nv_bfloat16* src = p.wr + static_cast<size_t>(ok ? r : 0) * H + k0 + seg * 8;
-            cp_async16(smem_u32(ws + (buf * kEPad + r) * kRowStride + seg * 8), src, ok);
-        }
-    };
-
-    float acc[2][NTW][4];
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int j = 0; j < NTW; ++j)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
-
-    load_chunk(0, 0);
-    cp_async_commit();
-    for (int c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks) {
-            load_chunk(c + 1, (c + 1) & 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const int buf = c & 1;
-#pragma unroll
-        for (int ks = 0; ks < kBlockK / 16; ++ks) {
-            uint32_t a[2][4];
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int mi = lane >> 3, r = lane & 7;
-                const int row = m * 16 + (mi & 1) * 8 + r;
-                const int col = ks * 16 + (mi >> 1) * 8;
-                ldmatrix_x4(smem_u32(xs + (buf * kRouterTokens + row) * kRowStride + col),
-                            a[m][0], a[m][1], a[m][2], a[m][3]);
-            }
-#pragma unroll
-            for (int j = 0; j < NTW; ++j) {
-                const int nt = warp + 4 * j;
-                const int l16 = lane & 15;
-                const int row = nt * 8 + (l16 & 7);
-                const int col = ks * 16 + (l16 >> 3) * 8;
-                uint32_t b0, b1;
-                ldmatrix_x2(smem_u32(ws + (buf * kEPad + row) * kRowStride + col), b0, b1);
-#pragma unroll
-                for (int m = 0; m < 2; ++m) mma_bf16_16816(acc[m][j], a[m], b0, b1);
-            }
-        }
-        __syncthreads();
-    }
-
-    // Scatter the fragments to smem (ws is free now): logits[token][expert].
-    {
-        const int g = lane >> 2, cq = lane & 3;
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int j = 0; j < NTW; ++j) {
-                const int col = (warp + 4 * j) * 8 + 2 * cq;
-                const int row = m * 16 + g;
-                logits[row * (kEPad + 1) + col] = acc[m][j][0];
-                logits[row * (kEPad + 1) + col + 1] = acc[m][j][1];
-                logits[(row + 8) * (kEPad + 1) + col] = acc[m][j][2];
-                logits[(row + 8) * (kEPad + 1) + col + 1] = acc[m][j][3];
-            }
+        flag[0] = 0;
+        flag[1] = 0;
+        flag[2] = 0;
+        mbar_fence_init();
     }
     __syncthreads();
 
-    // Top-k + softmax: warp w handles tokens 8w .. 8w+7.
-    const int k = p.top_k;
-    float bias[NTW];
+    float acc[2][4][4];
 #pragma unroll
-    for (int i = 0; i < NTW; ++i) {
-        const int e = lane + 32 * i;
-        bias[i] = e < E ? __bfloat162float(p.br[e]) : 0.f;
-    }
-    for (int r = warp * 8; r < warp * 8 + 8; ++r) {
-        const int t = t0 + r;
-        if (t >= p.T) break;  // warp-uniform; no block barrier follows inside
-        float v[NTW];
-        uint32_t taken = 0;
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int i = 0; i < NTW; ++i) {
-            const int e = lane + 32 * i;
-            float l = logits[r * (kEPad + 1) + e] + bias[i];
-            if (!(l == l)) l = -FLT_MAX;            // NaN never wins
-            v[i] = e < E ? l : -INFINITY;
-            if (e >= E) taken |= 1u << i;
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
+
+    if (warp == kComputeWarps) {
+        // ---------------- producer: one lane issues every chunk's two loads
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_x);
+            tma_prefetch_desc(&tmap_wr);
+            const uint64_t pol_x = policy_evict_first();
+            const uint64_t pol_w = policy_evict_last();
+            int issued = 0;
+            for (; issued < nchunks; ++issued) {
+                const int c = issued, s = c % S;
+                if (c >= S &&
+                    !mbar_wait(smem_u32(empty + s), static_cast<uint32_t>(c / S - 1) & 1u, flag)) {
+                    flag[0] = 1;
+                    break;
+                }
+                const uint32_t bar = smem_u32(full + s);
+                uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
+                mbar_arrive_expect_tx(bar, kStageBytes);
+                tma_load_2d(smem_u32(st), &tmap_x, bar, c * kBlockK, t0, pol_x);
+                tma_load_2d(smem_u32(st + kTileBytes), &tmap_wr, bar, c * kBlockK, g * kGroup,
+                            pol_w);
+            }
+            // Every issued load must land before the CTA may leave (bounded).
+            for (int c = issued - S > 0 ? issued - S : 0; c < issued; ++c)
+                mbar_wait(smem_u32(full + c % S), static_cast<uint32_t>(c / S) & 1u, nullptr);
         }
-        int sel_e[kMaxTopK];
-        float sel_v[kMaxTopK];
-        for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int be = INT_MAX;
+    } else {
+        // ---------------- compute warp w: chunks w, w+4, w+8, ...
+        for (int c = warp; c < nchunks; c += kComputeWarps) {
+            const int s = c % S;
+            if (!mbar_wait(smem_u32(full + s), static_cast<uint32_t>(c / S) & 1u, flag)) {
+                flag[0] = 1;
+                break;
+            }
+            const uint8_t* xs = ring + static_cast<size_t>(s) * kStageBytes;
+            const uint8_t* ws = xs + kTileBytes;
 #pragma unroll
-            for (int i = 0; i < NTW; ++i) {
-                const int e = lane + 32 * i;
-                if (!(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < be))) {
-                    bv = v[i];
-                    be = e;
+            for (int ks = 0; ks < kBlockK / 16; ++ks) {
+                uint32_t a[2][4], bw[4][2];
+                const int mi = lane >> 3, r = lane & 7;
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+                    ldmatrix_x4(smem_u32(xs + swz(m * 16 + (mi & 1) * 8 + r, ks * 2 + (mi >> 1))),
+                                a[m][0], a[m][1], a[m][2], a[m][3]);
+                // B fragments of n-tiles (2q, 2q+1): rows n*8 + (lane & 7)
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    ldmatrix_x4(smem_u32(ws + swz((2 * q + (mi >> 1)) * 8 + r, ks * 2 + (mi & 1))),
+                                bw[2 * q][0], bw[2 * q][1], bw[2 * q + 1][0], bw[2 * q + 1][1]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) mma_bf16_16816(acc[m][j], a[m], bw[j][0], bw[j][1]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        }
+        // Partial logits of this warp -> smem [warp][token][expert].
+        const int gq = lane >> 2, cq = lane & 3;
+        float* pw = partial + warp * kRouterTokens * kPartStride;
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = j * 8 + 2 * cq, row = m * 16 + gq;
+                pw[row * kPartStride + col] = acc[m][j][0];
+                pw[row * kPartStride + col + 1] = acc[m][j][1];
+                pw[(row + 8) * kPartStride + col] = acc[m][j][2];
+                pw[(row + 8) * kPartStride + col + 1] = acc[m][j][3];
+            }
+    }
+    __syncthreads();
+    if (flag[0]) {
+        if (tid == 0) atomicOr(p.status + kStatusWord, MOE_DEV_WAIT_TIMEOUT);
+        return;   // block-uniform: flag read after the barrier
+    }
+
+    // Sum the four partials in warp order; keep this group's 32 columns.
+    const int ls = p.egroups > 1 ? E + 1 : kGroup + 1;       // logits row stride
+    const int g0 = g * kGroup;
+    for (int i = tid; i < kRouterTokens * kGroup; i += kThreads) {
+        const int row = i / kGroup, col = i - row * kGroup;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) v += partial[(w * kRouterTokens + row) * kPartStride + col];
+        if (p.egroups == 1) {
+            logits[row * ls + col] = v;
+        } else if (g0 + col < E) {
+            p.logits[(static_cast<size_t>(b) * kRouterTokens + row) * E + g0 + col] = v;
+        }
+    }
+    if (p.egroups > 1) {
+        // The last expert group of this token block gathers the full rows.
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const int ticket = atomicAdd(p.blk_counter + b, 1);
+            flag[1] = (ticket == p.egroups - 1);
+            if (flag[1]) p.blk_counter[b] = 0;
+        }
+        __syncthreads();
+        if (!flag[1]) return;   // block-uniform
+        __threadfence();
+        for (int i = tid; i < kRouterTokens * E; i += kThreads) {
+            const int row = i / E, col = i - row * E;
+            logits[row * ls + col] =
+                __ldcg(p.logits + (static_cast<size_t>(b) * kRouterTokens + row) * E + col);
+        }
+    }
+    __syncthreads();
+
+    // Top-k + softmax: thread t (warp 0) handles token t0 + t.  It scans the
+    // experts in ascending order and keeps the k best by insertion; a logit
+    // equal to a kept one goes after it, so equal logits keep the lower
+    // expert index first.  NaN logits are treated as the lowest value.
+    if (warp == 0 && t0 + lane < p.T) {
+        const int k = p.top_k;
+        const int t = t0 + lane;
+        float bv[kMaxTopK];
+        int be[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            bv[j] = -INFINITY;
+            be[j] = -1;
+        }
+        for (int e = 0; e < E; ++e) {
+            float cv = logits[lane * ls + e] + __bfloat162float(p.br[e]);
+            if (!(cv == cv)) cv = -FLT_MAX;
+            int ce = e;
+            // Insert the candidate before the first kept entry it beats
+            // (strictly greater logit, or an empty slot); every entry from
+            // there on shifts down one slot -- a displaced entry ranks above
+            // the next one even when their logits are equal.
+            bool shifting = false;
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                if (j < k && (shifting || be[j] < 0 || cv > bv[j])) {
+                    shifting = true;
+                    const float tv = bv[j];
+                    const int te = be[j];
+                    bv[j] = cv;
+                    be[j] = ce;
+                    cv = tv;
+                    ce = te;
                 }
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            sel_e[j] = be;
-            sel_v[j] = bv;
         }
         float ex[kMaxTopK];
         float denom = 0.f;
-        for (int j = 0; j < k; ++j) {
-            ex[j] = expf(sel_v[j] - sel_v[0]);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            ex[j] = j < k ? expf(bv[j] - bv[0]) : 0.f;
             denom += ex[j];
         }
-        for (int j = 0; j < k; ++j) {
-            if (lane == j) {
-                p.topk_ids[static_cast<size_t>(t) * k + j] = sel_e[j];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k) {
+                p.topk_ids[static_cast<size_t>(t) * k + j] = be[j];
                 p.topk_w[static_cast<size_t>(t) * k + j] = ex[j] / denom;
-                atomicAdd(&hist[sel_e[j]], 1);
+                atomicAdd(&hist[be[j]], 1);
             }
         }
     }
     __syncthreads();
     for (int e = tid; e < E; e += kThreads)
-        p.blk_cnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+        p.blk_cnt[static_cast<size_t>(e) * p.nblocks + b] = hist[e];
 
-    if (p.zero_out) {
-        const int rows = min(kRouterTokens, p.T - t0);
-        float4* dst = reinterpret_cast<float4*>(p.zero_out + static_cast<size_t>(t0) * H);
-        const int n4 = rows * H / 4;
-        for (int i = tid; i < n4; i += kThreads) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.nblocks > 1) {
+        // The last token block finishes the routing tables.
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const int ticket = atomicAdd(p.status + kGridCounterWord, 1);
+            flag[2] = (ticket == p.nblocks - 1);
+        }
+        __syncthreads();
+        if (!flag[2]) return;   // block-uniform
+        __threadfence();
+    } else {
+        __syncthreads();        // this block's counts are visible to itself
     }
-}
-
-template <int NTW>
-cudaError_t launch_router_t(const RouterParams& p, cudaStream_t s) {
-    constexpr int kEPad = 32 * NTW;
-    const size_t smem = (2 * kRouterTokens * kRowStride + 2 * kEPad * kRowStride) * 2 +
-                        kMaxExperts * 4;
-    auto kern = router_topk_kernel<NTW>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    const int grid = (p.T + kRouterTokens - 1) / kRouterTokens;
-    kern<<<grid, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    finish_routing(p, hist, scan_a, scan_b, scan_c);
 }
 
 }  // namespace
 
-cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
-    switch ((p.E + 31) / 32) {
-        case 1: return launch_router_t<1>(p, s);
-        case 2: return launch_router_t<2>(p, s);
-        case 3: return launch_router_t<3>(p, s);
-        case 4: return launch_router_t<4>(p, s);
-        case 5: return launch_router_t<5>(p, s);
-        case 6: return launch_router_t<6>(p, s);
-        case 7: return launch_router_t<7>(p, s);
-        case 8: return launch_router_t<8>(p, s);
-        default: return cudaErrorInvalidValue;
-    }
+size_t router_stage_bytes() { return kStageBytes; }
+
+// Shared memory for `stages` ring slots (at least the top-k logits), the
+// warp partials, barriers and scan buffers, plus 1 KB alignment slack.
+size_t router_smem_bytes(int stages) {
+    const size_t ring = static_cast<size_t>(stages) * kStageBytes;
+    return 1024 + (ring > kLogitsBytes ? ring : kLogitsBytes) + kPartialBytes +
+           2 * kMaxStages * 8 + (4 * kMaxExperts + 4) * 4;
+}
+
+int router_max_stages() { return kMaxStages; }
+
+cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tx, const CUtensorMap* tw,
+                          size_t smem, cudaStream_t s) {
+    if (p.stages < 1 || p.stages > kMaxStages) return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(router_topk_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    router_topk_kernel<<<dim3(p.nblocks, p.egroups), kThreads, smem, s>>>(p, *tx, *tw);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -92,9 +92,12 @@ typedef struct {
 #define MOE_DEV_BAD_TILE       0x4   /* a work tile failed its bounds check */
 
 /* Bytes of device workspace moe_route / moe_forward need for this shape
- * (0 for an invalid shape).  The workspace is scratch owned by the caller;
- * its contents between calls are unspecified except for the status word,
- * which only moe_clear_device_status resets. */
+ * (0 for an invalid shape).  The workspace is scratch owned by the caller.
+ * A new workspace must be zero-filled once before its first use (e.g.
+ * cudaMemsetAsync(ws, 0, bytes)): it holds completion counters that every
+ * call leaves at zero again.  Apart from those and the status word (which
+ * only moe_clear_device_status resets), its contents between calls are
+ * unspecified.  Calls that share a workspace must not overlap on the GPU. */
 size_t moe_workspace_bytes(const moe_shape* shape);
 
 /* Router + top-k softmax + expert permutation (§2: "router GEMV ->

@@ -166,6 +166,24 @@ def test_route_full_size(moe, oracle_lib, synth_lib, name, T):
     assert torch.equal(off, off2) and torch.equal(sa, sa2)
 
 
+@pytest.mark.parametrize("E,k", [(8, 4), (32, 4), (128, 4), (40, 8), (6, 3)])
+def test_route_exact_ties_go_to_the_lower_index(moe, oracle_lib, synth_lib, E, k):
+    """Router weights zero: every logit equals its bias exactly, and the
+    biases repeat, so the selection is decided by the tie rule alone."""
+    T = 40
+    L = synth_lib.make_layer(E=E, T=T, H=128, I=128, top_k=k, seed=3, with_experts=False)
+    L.wr.zero_()
+    L.br.copy_(torch.tensor([float((e * 7) % 3) * 0.5 for e in range(E)]).to(torch.bfloat16))
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    shape = moe.make_shape(T, 128, 128, E, k)
+    moe.moe_route(shape, L.x.cuda(), L.wr.cuda(), L.br.cuda(), ids, w)
+    torch.cuda.synchronize()
+    o_ids, o_w = oracle_lib.topk_softmax(oracle_lib.router_logits(L), k)
+    assert torch.equal(ids.cpu(), o_ids)
+    assert (w.cpu() - o_w).abs().max() <= 1e-6
+
+
 def test_hot_experts_take_a_large_share(moe, synth_lib):
     L = synth_lib.make_workload("20b_prefill_skewed", 4096, with_experts=False)
     shape = moe.make_shape(4096, L.H, 2880, L.E, 4)
@@ -218,3 +236,63 @@ def test_forward_120b_shape(moe, oracle_lib, layer_120b, T):
         g = torch.Generator().manual_seed(T)
         sample = [0, T - 1] + torch.randint(0, T, (30,), generator=g).tolist()
     _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample)
+
+
+# ---------------------------------------------------------------- MXFP4
+
+MXFP4_CASES = [
+    # E, k, H, I, T, token_tile
+    (8, 2, 128, 128, 1, 0),
+    (8, 4, 320, 192, 37, 0),        # weight-row tail in the down projection
+    (4, 2, 192, 128, 700, 0),       # several token tiles per expert
+    (8, 4, 256, 256, 200, 48),
+    (32, 4, 2880, 2880, 5, 0),
+]
+
+
+@pytest.mark.parametrize("case", MXFP4_CASES, ids=lambda c: "E{}k{}H{}I{}T{}tile{}".format(*c))
+def test_forward_mxfp4_small_shapes(moe, oracle_lib, synth_lib, case):
+    from parity_util import TOL_MXFP4
+    E, k, H, I, T, tile = case
+    L = synth_lib.make_layer(E=E, T=T, H=H, I=I, top_k=k, seed=400 + T, wfmt="mxfp4",
+                             router_w_std=0.05)
+    moe.moe_set_tuning("token_tile", tile)
+    try:
+        _check(moe, oracle_lib, L, tol=TOL_MXFP4)
+    finally:
+        moe.moe_set_tuning("token_tile", 0)
+
+
+@pytest.mark.parametrize("T", [3, 300])
+def test_mxfp4_dequant_is_exact(moe, oracle_lib, synth_lib, T):
+    """In-kernel dequantisation is exact: with top-1 routing each output
+    element is a single combine term (weight 1), so the MXFP4 path must equal
+    bit for bit the bf16 path run on the oracle's dequantised weights."""
+    Lq = synth_lib.make_layer(E=4, T=T, H=320, I=192, top_k=1, seed=9, wfmt="mxfp4",
+                              scale_lo=116, scale_hi=126)
+    Lb = dataclasses.replace(
+        Lq, wfmt="bf16", s_gu=None, s_d=None,
+        w_gu=oracle_lib.dequant_mxfp4(Lq.w_gu, Lq.s_gu).to(torch.bfloat16).contiguous(),
+        w_d=oracle_lib.dequant_mxfp4(Lq.w_d, Lq.s_d).to(torch.bfloat16).contiguous())
+    iq, wq, oq, wsq = gpu_forward(moe, Lq)
+    ib, wb, ob, wsb = gpu_forward(moe, Lb)
+    assert moe.moe_get_device_status(wsq) == 0
+    assert torch.equal(iq, ib) and torch.equal(wq, wb)
+    assert torch.equal(oq, ob)
+
+
+@pytest.fixture(scope="module")
+def layer_20b_mxfp4(synth_lib):
+    L = synth_lib.make_workload("20b_mxfp4", 512)
+    return L, to_device(L)
+
+
+@pytest.mark.parametrize("T", [1, 64, 512])
+def test_forward_20b_mxfp4(moe, oracle_lib, layer_20b_mxfp4, T):
+    from parity_util import TOL_MXFP4
+    L, dev = layer_20b_mxfp4
+    sample = None
+    if T > 64:
+        g = torch.Generator().manual_seed(T)
+        sample = [0, T - 1] + torch.randint(0, T, (30,), generator=g).tolist()
+    _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample, tol=TOL_MXFP4)
