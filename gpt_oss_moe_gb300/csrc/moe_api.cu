@@ -221,7 +221,13 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     int stages = static_cast<int>((static_cast<size_t>(dev.max_smem) - fixed) /
                                   router_stage_bytes());
     if (stages > router_max_stages()) stages = router_max_stages();
-    if (stages > nchunks) stages = nchunks;
+    const int per_slice = (nchunks + router_ksplit(nb * ((s.E + 31) / 32), nchunks) - 1) /
+                          router_ksplit(nb * ((s.E + 31) / 32), nchunks);
+    if (stages >= per_slice) {
+        stages = per_slice;                        // the ring never wraps
+    } else {
+        stages -= stages % router_stage_multiple();   // one consumer warp per slot
+    }
     if (stages < 1) return MOE_ERR_UNSUPPORTED;
 
     RouterParams rp{};
@@ -232,9 +238,11 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     rp.top_k = s.top_k;
     rp.nblocks = nb;
     rp.egroups = (s.E + 31) / 32;
+    rp.ksplit = router_ksplit(nb * rp.egroups, nchunks);
     rp.stages = stages;
     rp.logits = reinterpret_cast<float*>(ws + L.logits);
-    rp.blk_counter = reinterpret_cast<int32_t*>(ws + L.blk_counter);
+    rp.partials = reinterpret_cast<float*>(ws + L.partials);
+    rp.counters = reinterpret_cast<int32_t*>(ws + L.counters);
     rp.topk_ids = r.ids;
     rp.topk_w = r.w;
     rp.blk_cnt = reinterpret_cast<int32_t*>(ws + L.blk_cnt);
@@ -455,7 +463,9 @@ moe_status moe_get_device_status(const void* workspace, int32_t* host_status) {
 
 moe_status moe_clear_device_status(void* workspace, cudaStream_t stream) {
     if (!workspace) return MOE_ERR_ARG;
-    return cudaMemsetAsync(workspace, 0, 256, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    // the status word and the router's ticket counters (fixed offsets)
+    return cudaMemsetAsync(workspace, 0, 256 + kCounterBytes, stream) == cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_set_tuning(const char* key, int value) {

@@ -25,8 +25,31 @@ constexpr int kStatusWord = 0;
 constexpr int kNumTilesWord = 1;
 constexpr int kGridCounterWord = 2;
 
+// Router ticket counters live at a fixed offset, right after the status
+// region, with one slot for every (token block, expert group) pair that can
+// use a K split (fewer than 304 pairs) and one per token block (T <= 2^20):
+// the same slots for every shape, so a workspace reused for another shape
+// still finds them at zero (every call leaves them at zero).
+constexpr int kPairSlots = 304;
+constexpr int kMaxTokenBlocks = (1 << 20) / 32;
+constexpr size_t kCounterBytes = static_cast<size_t>(kPairSlots + kMaxTokenBlocks) * 4;
+
+// K slices of the router: the hidden dimension is cut into `ksplit` slices
+// handled by separate CTAs when there are few (token block, expert group)
+// pairs, so that a small batch still spreads its loads over ~2 CTAs per SM
+// (sized for GB300's 152 SMs; each slice keeps at least 4 chunks of 64).
+inline int router_ksplit(int pairs, int nchunks) {
+    if (pairs < 1 || nchunks < 1) return 1;
+    int ks = (304 + pairs - 1) / pairs;
+    const int cap = nchunks / 4 > 1 ? nchunks / 4 : 1;
+    if (ks > cap) ks = cap;
+    if (ks < 1) ks = 1;
+    const int per = (nchunks + ks - 1) / ks;       // chunks per slice
+    return (nchunks + per - 1) / per;              // no empty slice
+}
+
 struct WsLayout {
-    size_t status, topk_ids, topk_w, blk_cnt, logits, blk_counter, offsets;
+    size_t status, topk_ids, topk_w, blk_cnt, logits, partials, counters, offsets;
     size_t sorted_assign, assign_row, tiles, x_perm, h, out_acc, total;
     int max_tiles;
 };
@@ -45,11 +68,14 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
         return at;
     };
     L.status = take(256);
+    L.counters = take(kCounterBytes);
     L.topk_ids = take(R * 4);
     L.topk_w = take(R * 4);
     L.blk_cnt = take(nb * E * 4);
-    L.logits = take(E > 32 ? nb * kRouterTokens * E * 4 : 0);
-    L.blk_counter = take(E > 32 ? nb * 4 : 0);
+    const size_t eg = (static_cast<size_t>(E) + 31) / 32;
+    const int ks = router_ksplit(static_cast<int>(nb * eg), H / kBlockK);
+    L.logits = take(eg > 1 ? nb * kRouterTokens * E * 4 : 0);
+    L.partials = take(ks > 1 ? nb * eg * ks * kRouterTokens * 32 * 4 : 0);
     L.offsets = take((E + 1) * 4);
     L.sorted_assign = take(R * 4);
     L.assign_row = take(R * 4);
@@ -66,11 +92,13 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
 struct RouterParams {
     const __nv_bfloat16* br;     // [E]
     int T, H, E, top_k;
-    int nblocks;                 // grid = (nblocks token blocks of 32, egroups of 32 experts)
-    int egroups;
+    int nblocks;                 // grid = (token blocks of 32, expert groups of 32,
+    int egroups;                 //         K slices)
+    int ksplit;
     int stages;                  // TMA ring depth
     float* logits;               // [nblocks, 32, E] when egroups > 1
-    int32_t* blk_counter;        // [nblocks] when egroups > 1, zero between calls
+    float* partials;             // [nblocks, egroups, ksplit, 32, 32] when ksplit > 1
+    int32_t* counters;           // [kPairSlots] + [kMaxTokenBlocks], zero between calls
     int32_t* topk_ids;           // [T, k]
     float* topk_w;               // [T, k]
     int32_t* blk_cnt;            // [E, nblocks]: counts, then (after the
@@ -147,6 +175,7 @@ inline size_t gemm_fixed_bytes(int token_box, int wf, int kscale) {
 size_t router_stage_bytes();
 size_t router_smem_bytes(int stages);
 int router_max_stages();
+int router_stage_multiple();
 cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tmap_x,
                           const CUtensorMap* tmap_wr, size_t smem, cudaStream_t s);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s, bool pdl);

@@ -4,25 +4,29 @@
 // "MoE" row -- the router is a plain Linear [2880 -> 32] with bias; §2
 // "MoE 前向" -- router GEMV then topk_softmax on the GPU, ids stay there).
 //
-// Grid (token blocks of 32, expert groups of 32).  CTA (b, g) computes the
-// logits of tokens [32b, 32b+32) for experts [32g, 32g+32) as an
-// fp32-accumulated bf16 contraction on the tensor cores (mma.sync m16n8k16;
-// the router is ~0.1% of the layer's flops, far too small for a TMEM
-// pipeline).  A producer warp streams 64-wide K chunks of x and Wr through a
-// TMA ring (128-byte swizzle) as deep as shared memory allows; each of the
-// four compute warps owns every fourth chunk, so four independent MMA chains
-// run at once and no block-wide barrier sits in the loop.  The four partial
-// sums are added in warp order (the same order every run).
-// With more than one expert group, each CTA stores its logit columns and the
-// last group of the token block to finish (an atomic ticket -- no waiting)
-// gathers the full rows.  That CTA then
-//   * selects the top k per token (thread t of warp 0 takes token t) by
-//     insertion: higher logit first, equal logits -> lower expert index;
-//   * computes the softmax over the k selected logits (max-subtracted, expf);
-//   * counts its assignments per expert;
-//   * takes a second ticket; the last token block turns the per-block counts
-//     into per-expert exclusive prefixes, scans the totals into expert
-//     offsets and writes the GEMM token-tile list.
+// Grid (token blocks of 32, expert groups of 32, K slices).  CTA (b, g, q)
+// computes the logits of tokens [32b, 32b+32) for experts [32g, 32g+32) over
+// the q-th slice of the hidden dimension, as an fp32-accumulated bf16
+// contraction on the tensor cores (mma.sync m16n8k16; the router is ~0.1% of
+// the layer's flops, far too small for a TMEM pipeline).  A producer warp
+// streams 64-wide K chunks of x and Wr through a TMA ring (128-byte
+// swizzle); each of the four compute warps owns every fourth chunk, so four
+// independent MMA chains run at once, and their partial sums are added in
+// warp order.  Slicing K spreads a small batch's loads over many SMs (one
+// CTA streams only ~40 GB/s).
+// Results are merged by atomic tickets -- no CTA ever waits for another:
+//   * the last K slice of (b, g) to finish adds the slices' partials in
+//     slice order (the same order every run);
+//   * with more than one expert group, the last group of block b gathers the
+//     block's full logit rows;
+//   * that CTA selects the top k per token -- one warp per token, lanes over
+//     experts, redux.sync for the maximum and then for the lowest expert
+//     index holding it (equal logits -> lower index) -- computes the softmax
+//     over the k selected logits (max-subtracted, expf) and counts the
+//     assignments per expert;
+//   * the last token block turns the per-block counts into per-expert
+//     exclusive prefixes, scans the totals into expert offsets and writes the
+//     GEMM token-tile list.
 // Every ticket counter is reset by the CTA that takes the last ticket, so the
 // counters are zero between calls.
 //
@@ -41,7 +45,12 @@ namespace {
 
 constexpr int kComputeWarps = 4;
 constexpr int kThreads = (kComputeWarps + 1) * 32;   // + one producer warp
-constexpr int kMaxStages = 24;
+// Ring depth: a multiple of kComputeWarps, so chunk c and chunk c + S (same
+// slot) always belong to the same compute warp.  Each slot then has a single
+// consumer that takes its phases in order, and a parity wait can never be
+// satisfied by a phase two behind.  One CTA streams ~40 GB/s, so 8 x 8 KB in
+// flight covers the latency.
+constexpr int kMaxStages = 8;
 constexpr int kGroup = 32;                            // experts per CTA
 constexpr uint32_t kTileBytes = kRouterTokens * kBlockK * 2;   // 4 KB (x or w tile)
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
@@ -62,6 +71,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Order-preserving unsigned key of a float (-0 is folded into +0 first, so
+// equal values get equal keys).
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+    return __reduce_max_sync(0xffffffffu, v);
+}
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
+    return __reduce_min_sync(0xffffffffu, v);
 }
 
 // Byte offset of the 16-byte chunk `c` (0..7) of row `r` in a tile written
@@ -106,15 +131,20 @@ __device__ __forceinline__ void warp_exclusive_scan256(const int* vals, int* out
 
 // Last CTA of the grid: per-expert exclusive prefix over token blocks, expert
 // offsets, GEMM token tiles.
+// With a single token block the prefixes are all zero and the totals are the
+// block's own counts (already in total_s).
 __device__ void finish_routing(const RouterParams& p, int* total_s, int* offs_s, int* tcnt_s,
                                int* toff_s) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int kWarps = kThreads / 32;
     const int E = p.E, nb = p.nblocks;
+    if (nb == 1) {
+        for (int e = tid; e < E; e += kThreads) p.blk_cnt[e] = 0;
+    }
     // Per warp pass: 4 experts x up to 8 chunks of 32 blocks, all loads in
     // flight before the scans.
-    constexpr int kQ = 4, kC = 8;
-    for (int e0 = warp * kQ; e0 < E; e0 += kQ * kWarps) {
+    for (int e0 = warp * 4; nb > 1 && e0 < E; e0 += 4 * kWarps) {
+        constexpr int kQ = 4, kC = 8;
         int carry[kQ] = {0, 0, 0, 0};
         for (int bs = 0; bs < nb; bs += 32 * kC) {
             const int nchunk = min(kC, (nb - bs + 31) / 32);   // chunks holding real blocks
@@ -190,15 +220,28 @@ __global__ void __launch_bounds__(kThreads)
     int* scan_a = hist + kMaxExperts;                                       // [257]
     int* scan_b = scan_a + kMaxExperts + 1;                                 // [256]
     int* scan_c = scan_b + kMaxExperts;                                     // [257]
-    volatile int* flag = scan_c + kMaxExperts + 1;                          // [3]
+    volatile int* flag = scan_c + kMaxExperts + 1;                          // [4]
+    float* bias_s = reinterpret_cast<float*>(scan_c + kMaxExperts + 5);      // [256]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x, g = blockIdx.y;
+    const int b = blockIdx.x, g = blockIdx.y, q = blockIdx.z;
     const int t0 = b * kRouterTokens;
     const int E = p.E;
     const int nchunks = p.H / kBlockK;
+    const int per = (nchunks + p.ksplit - 1) / p.ksplit;
+    const int c_begin = q * per;
+    const int nc = min(nchunks, c_begin + per) - c_begin;   // chunks of this slice
 
-    for (int e = tid; e < kMaxExperts; e += kThreads) hist[e] = 0;
+    if (nc > S && S % kComputeWarps != 0) {
+        // a slot would be shared by two consumer warps: refuse (the host
+        // never asks for this)
+        if (tid == 0) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
+        return;
+    }
+    for (int e = tid; e < kMaxExperts; e += kThreads) {
+        hist[e] = 0;
+        bias_s[e] = e < E ? __bfloat162float(p.br[e]) : 0.f;
+    }
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(full + s), 1);
@@ -207,6 +250,7 @@ __global__ void __launch_bounds__(kThreads)
         flag[0] = 0;
         flag[1] = 0;
         flag[2] = 0;
+        flag[3] = 0;
         mbar_fence_init();
     }
     __syncthreads();
@@ -217,7 +261,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
+            for (int r = 0; r < 4; ++r) acc[m][j][r] = 0.f;
 
     if (warp == kComputeWarps) {
         // ---------------- producer: one lane issues every chunk's two loads
@@ -227,7 +271,7 @@ __global__ void __launch_bounds__(kThreads)
             const uint64_t pol_x = policy_evict_first();
             const uint64_t pol_w = policy_evict_last();
             int issued = 0;
-            for (; issued < nchunks; ++issued) {
+            for (; issued < nc; ++issued) {
                 const int c = issued, s = c % S;
                 if (c >= S &&
                     !mbar_wait(smem_u32(empty + s), static_cast<uint32_t>(c / S - 1) & 1u, flag)) {
@@ -236,18 +280,18 @@ __global__ void __launch_bounds__(kThreads)
                 }
                 const uint32_t bar = smem_u32(full + s);
                 uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
+                const int k0 = (c_begin + c) * kBlockK;
                 mbar_arrive_expect_tx(bar, kStageBytes);
-                tma_load_2d(smem_u32(st), &tmap_x, bar, c * kBlockK, t0, pol_x);
-                tma_load_2d(smem_u32(st + kTileBytes), &tmap_wr, bar, c * kBlockK, g * kGroup,
-                            pol_w);
+                tma_load_2d(smem_u32(st), &tmap_x, bar, k0, t0, pol_x);
+                tma_load_2d(smem_u32(st + kTileBytes), &tmap_wr, bar, k0, g * kGroup, pol_w);
             }
             // Every issued load must land before the CTA may leave (bounded).
             for (int c = issued - S > 0 ? issued - S : 0; c < issued; ++c)
                 mbar_wait(smem_u32(full + c % S), static_cast<uint32_t>(c / S) & 1u, nullptr);
         }
     } else {
-        // ---------------- compute warp w: chunks w, w+4, w+8, ...
-        for (int c = warp; c < nchunks; c += kComputeWarps) {
+        // ---------------- compute warp w: chunks w, w+4, w+8, ... of the slice
+        for (int c = warp; c < nc; c += kComputeWarps) {
             const int s = c % S;
             if (!mbar_wait(smem_u32(full + s), static_cast<uint32_t>(c / S) & 1u, flag)) {
                 flag[0] = 1;
@@ -263,11 +307,11 @@ __global__ void __launch_bounds__(kThreads)
                 for (int m = 0; m < 2; ++m)
                     ldmatrix_x4(smem_u32(xs + swz(m * 16 + (mi & 1) * 8 + r, ks * 2 + (mi >> 1))),
                                 a[m][0], a[m][1], a[m][2], a[m][3]);
-                // B fragments of n-tiles (2q, 2q+1): rows n*8 + (lane & 7)
+                // B fragments of n-tiles (2h, 2h+1): rows n*8 + (lane & 7)
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    ldmatrix_x4(smem_u32(ws + swz((2 * q + (mi >> 1)) * 8 + r, ks * 2 + (mi & 1))),
-                                bw[2 * q][0], bw[2 * q][1], bw[2 * q + 1][0], bw[2 * q + 1][1]);
+                for (int h = 0; h < 2; ++h)
+                    ldmatrix_x4(smem_u32(ws + swz((2 * h + (mi >> 1)) * 8 + r, ks * 2 + (mi & 1))),
+                                bw[2 * h][0], bw[2 * h][1], bw[2 * h + 1][0], bw[2 * h + 1][1]);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -296,89 +340,172 @@ __global__ void __launch_bounds__(kThreads)
         return;   // block-uniform: flag read after the barrier
     }
 
-    // Sum the four partials in warp order; keep this group's 32 columns.
-    const int ls = p.egroups > 1 ? E + 1 : kGroup + 1;       // logits row stride
-    const int g0 = g * kGroup;
+    // This slice's 32 x 32 block: the warp partials added in warp order.
+    // `blk` lives in the partial buffer's warp-0 slot.
+    float* blk = partial;
     for (int i = tid; i < kRouterTokens * kGroup; i += kThreads) {
         const int row = i / kGroup, col = i - row * kGroup;
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kComputeWarps; ++w) v += partial[(w * kRouterTokens + row) * kPartStride + col];
-        if (p.egroups == 1) {
-            logits[row * ls + col] = v;
-        } else if (g0 + col < E) {
-            p.logits[(static_cast<size_t>(b) * kRouterTokens + row) * E + g0 + col] = v;
-        }
+        for (int w = 0; w < kComputeWarps; ++w)
+            v += partial[(w * kRouterTokens + row) * kPartStride + col];
+        blk[row * kPartStride + col] = v;   // only this thread reads this slot
     }
-    if (p.egroups > 1) {
-        // The last expert group of this token block gathers the full rows.
+    __syncthreads();
+
+    const int pair = b * p.egroups + g;
+    if (p.ksplit > 1) {
+        // The last K slice of (b, g) adds all slices' blocks in slice order.
+        float* mine = p.partials + (static_cast<size_t>(pair) * p.ksplit + q) * kRouterTokens * kGroup;
+        for (int i = tid; i < kRouterTokens * kGroup; i += kThreads)
+            mine[i] = blk[(i / kGroup) * kPartStride + (i % kGroup)];
         __threadfence();
         __syncthreads();
         if (tid == 0) {
-            const int ticket = atomicAdd(p.blk_counter + b, 1);
-            flag[1] = (ticket == p.egroups - 1);
-            if (flag[1]) p.blk_counter[b] = 0;
+            const int ticket = atomicAdd(p.counters + pair, 1);
+            flag[1] = (ticket == p.ksplit - 1);
+            if (flag[1]) p.counters[pair] = 0;
         }
         __syncthreads();
         if (!flag[1]) return;   // block-uniform
         __threadfence();
+        const float* all = p.partials + static_cast<size_t>(pair) * p.ksplit * kRouterTokens * kGroup;
+        constexpr int kPerThread = (kRouterTokens * kGroup + kThreads - 1) / kThreads;   // 7
+        float sum[kPerThread];
+#pragma unroll
+        for (int r = 0; r < kPerThread; ++r) sum[r] = 0.f;
+        for (int s0 = 0; s0 < p.ksplit; s0 += 4) {
+            float v[4][kPerThread];
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+                for (int r = 0; r < kPerThread; ++r) {
+                    const int i = tid + r * kThreads;
+                    v[s][r] = (s0 + s < p.ksplit && i < kRouterTokens * kGroup)
+                                  ? __ldcg(all + static_cast<size_t>(s0 + s) * kRouterTokens * kGroup + i)
+                                  : 0.f;
+                }
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+                for (int r = 0; r < kPerThread; ++r)
+                    if (s0 + s < p.ksplit) sum[r] += v[s][r];
+        }
+#pragma unroll
+        for (int r = 0; r < kPerThread; ++r) {
+            const int i = tid + r * kThreads;
+            if (i < kRouterTokens * kGroup) blk[(i / kGroup) * kPartStride + (i % kGroup)] = sum[r];
+        }
+        __syncthreads();
+    }
+
+    // Full logit rows of the token block in smem: logits[token][expert].
+    const int ls = E + 1;
+    if (p.egroups == 1) {
         for (int i = tid; i < kRouterTokens * E; i += kThreads) {
             const int row = i / E, col = i - row * E;
-            logits[row * ls + col] =
-                __ldcg(p.logits + (static_cast<size_t>(b) * kRouterTokens + row) * E + col);
+            logits[row * ls + col] = blk[row * kPartStride + col];
+        }
+    } else {
+        // The last expert group of block b gathers the block's rows.
+        const int g0 = g * kGroup;
+        for (int i = tid; i < kRouterTokens * kGroup; i += kThreads) {
+            const int row = i / kGroup, col = i - row * kGroup;
+            if (g0 + col < E)
+                p.logits[(static_cast<size_t>(b) * kRouterTokens + row) * E + g0 + col] =
+                    blk[row * kPartStride + col];
+        }
+        __threadfence();
+        __syncthreads();
+        int* gcount = p.counters + kPairSlots + b;
+        if (tid == 0) {
+            const int ticket = atomicAdd(gcount, 1);
+            flag[2] = (ticket == p.egroups - 1);
+            if (flag[2]) *gcount = 0;
+        }
+        __syncthreads();
+        if (!flag[2]) return;   // block-uniform
+        __threadfence();
+        const float* rows = p.logits + static_cast<size_t>(b) * kRouterTokens * E;
+        for (int i0 = 0; i0 < kRouterTokens * E; i0 += 8 * kThreads) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kThreads + tid;
+                v[u] = i < kRouterTokens * E ? __ldcg(rows + i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kThreads + tid;
+                if (i < kRouterTokens * E) logits[(i / E) * ls + (i % E)] = v[u];
+            }
         }
     }
     __syncthreads();
 
-    // Top-k + softmax: thread t (warp 0) handles token t0 + t.  It scans the
-    // experts in ascending order and keeps the k best by insertion; a logit
-    // equal to a kept one goes after it, so equal logits keep the lower
-    // expert index first.  NaN logits are treated as the lowest value.
-    if (warp == 0 && t0 + lane < p.T) {
-        const int k = p.top_k;
-        const int t = t0 + lane;
-        float bv[kMaxTopK];
-        int be[kMaxTopK];
+    // Top-k + softmax, one warp per token: lane l holds experts l, l+32, ...
+    // A selection round takes the largest order key (redux.sync max) and,
+    // among the experts holding it, the lowest index (redux.sync min), so
+    // equal logits go to the lower expert index.  NaN is the lowest value.
+    const int k = p.top_k;
+    const int nkeys = (E + 31) / 32;
+    for (int r = warp; r < kRouterTokens; r += kThreads / 32) {
+        const int t = t0 + r;
+        if (t >= p.T) break;   // warp-uniform; no block barrier inside
+        uint32_t key[kMaxExperts / 32];
+        uint32_t taken = 0;
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            bv[j] = -INFINITY;
-            be[j] = -1;
-        }
-        for (int e = 0; e < E; ++e) {
-            float cv = logits[lane * ls + e] + __bfloat162float(p.br[e]);
-            if (!(cv == cv)) cv = -FLT_MAX;
-            int ce = e;
-            // Insert the candidate before the first kept entry it beats
-            // (strictly greater logit, or an empty slot); every entry from
-            // there on shifts down one slot -- a displaced entry ranks above
-            // the next one even when their logits are equal.
-            bool shifting = false;
-#pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j) {
-                if (j < k && (shifting || be[j] < 0 || cv > bv[j])) {
-                    shifting = true;
-                    const float tv = bv[j];
-                    const int te = be[j];
-                    bv[j] = cv;
-                    be[j] = ce;
-                    cv = tv;
-                    ce = te;
-                }
+        for (int i = 0; i < kMaxExperts / 32; ++i) {
+            const int e = lane + 32 * i;
+            key[i] = 0u;   // below every real logit
+            if (i < nkeys && e < E) {
+                float v = logits[r * ls + e] + bias_s[e];
+                if (!(v == v)) v = -FLT_MAX;
+                key[i] = order_key(v);
+            } else {
+                taken |= 1u << i;
             }
         }
-        float ex[kMaxTopK];
-        float denom = 0.f;
+        int sel_e[kMaxTopK];
+        float sel_v[kMaxTopK];
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j) {
-            ex[j] = j < k ? expf(bv[j] - bv[0]) : 0.f;
-            denom += ex[j];
+            sel_e[j] = 0;
+            sel_v[j] = 0.f;
+            if (j < k) {
+                uint32_t best = 0u;
+                int best_e = 0x7fffffff;
+#pragma unroll
+                for (int i = 0; i < kMaxExperts / 32; ++i)
+                    if (!(taken & (1u << i)) && (key[i] > best || best_e == 0x7fffffff)) {
+                        best = key[i];
+                        best_e = lane + 32 * i;
+                    }
+                const uint32_t m = warp_max_u32(best_e == 0x7fffffff ? 0u : best);
+                const uint32_t cand =
+                    (best_e != 0x7fffffff && best == m) ? static_cast<uint32_t>(best_e) : 0xffffffffu;
+                const int e_sel = static_cast<int>(warp_min_u32(cand));
+                if ((e_sel & 31) == lane) taken |= 1u << (e_sel >> 5);
+                sel_e[j] = e_sel;
+                sel_v[j] = key_value(m);   // the selected logit itself
+            }
         }
+        // softmax over the k selected logits, summed in slot order
+        float denom = 0.f, mine = 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j) {
             if (j < k) {
-                p.topk_ids[static_cast<size_t>(t) * k + j] = be[j];
-                p.topk_w[static_cast<size_t>(t) * k + j] = ex[j] / denom;
-                atomicAdd(&hist[be[j]], 1);
+                const float ex = expf(sel_v[j] - sel_v[0]);
+                denom += ex;
+                if (lane == j) mine = ex;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k && lane == j) {
+                p.topk_ids[static_cast<size_t>(t) * k + j] = sel_e[j];
+                p.topk_w[static_cast<size_t>(t) * k + j] = mine / denom;
+                atomicAdd(&hist[sel_e[j]], 1);
             }
         }
     }
@@ -392,13 +519,13 @@ __global__ void __launch_bounds__(kThreads)
         __syncthreads();
         if (tid == 0) {
             const int ticket = atomicAdd(p.status + kGridCounterWord, 1);
-            flag[2] = (ticket == p.nblocks - 1);
+            flag[3] = (ticket == p.nblocks - 1);
         }
         __syncthreads();
-        if (!flag[2]) return;   // block-uniform
+        if (!flag[3]) return;   // block-uniform
         __threadfence();
     } else {
-        __syncthreads();        // this block's counts are visible to itself
+        __syncthreads();
     }
     finish_routing(p, hist, scan_a, scan_b, scan_c);
 }
@@ -412,10 +539,11 @@ size_t router_stage_bytes() { return kStageBytes; }
 size_t router_smem_bytes(int stages) {
     const size_t ring = static_cast<size_t>(stages) * kStageBytes;
     return 1024 + (ring > kLogitsBytes ? ring : kLogitsBytes) + kPartialBytes +
-           2 * kMaxStages * 8 + (4 * kMaxExperts + 4) * 4;
+           2 * kMaxStages * 8 + (5 * kMaxExperts + 8) * 4;
 }
 
 int router_max_stages() { return kMaxStages; }
+int router_stage_multiple() { return kComputeWarps; }
 
 cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tx, const CUtensorMap* tw,
                           size_t smem, cudaStream_t s) {
@@ -424,7 +552,7 @@ cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tx, const CU
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    router_topk_kernel<<<dim3(p.nblocks, p.egroups), kThreads, smem, s>>>(p, *tx, *tw);
+    router_topk_kernel<<<dim3(p.nblocks, p.egroups, p.ksplit), kThreads, smem, s>>>(p, *tx, *tw);
     return cudaGetLastError();
 }
 

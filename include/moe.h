@@ -94,10 +94,12 @@ typedef struct {
 /* Bytes of device workspace moe_route / moe_forward need for this shape
  * (0 for an invalid shape).  The workspace is scratch owned by the caller.
  * A new workspace must be zero-filled once before its first use (e.g.
- * cudaMemsetAsync(ws, 0, bytes)): it holds completion counters that every
- * call leaves at zero again.  Apart from those and the status word (which
- * only moe_clear_device_status resets), its contents between calls are
- * unspecified.  Calls that share a workspace must not overlap on the GPU. */
+ * cudaMemsetAsync(ws, 0, bytes), or moe_clear_device_status): it starts
+ * with the status word and a fixed block of completion counters that every
+ * call leaves at zero again, so one workspace (large enough) may serve any
+ * shape.  After a device error is reported, clear it again.  Apart from
+ * those, its contents between calls are unspecified.  Calls that share a
+ * workspace must not overlap on the GPU. */
 size_t moe_workspace_bytes(const moe_shape* shape);
 
 /* Router + top-k softmax + expert permutation (§2: "router GEMV ->
@@ -169,7 +171,8 @@ moe_status moe_forward_noalloc(const moe_shape* shape, const void* hidden,
  * MOE_ERR_DEVICE when the word is non-zero, MOE_OK otherwise. */
 moe_status moe_get_device_status(const void* workspace, int32_t* host_status);
 
-/* Zeroes the device status word (enqueued on `stream`). */
+/* Zeroes the device status word and the workspace's completion counters
+ * (enqueued on `stream`). */
 moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
 
 /* Process-wide tuning switches for tests and benchmarks:

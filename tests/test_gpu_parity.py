@@ -296,3 +296,19 @@ def test_forward_20b_mxfp4(moe, oracle_lib, layer_20b_mxfp4, T):
         g = torch.Generator().manual_seed(T)
         sample = [0, T - 1] + torch.randint(0, T, (30,), generator=g).tolist()
     _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample, tol=TOL_MXFP4)
+
+
+def test_one_workspace_serves_successive_shapes(moe, synth_lib):
+    """A workspace sized for the largest call is reused for smaller ones
+    (other token counts shift every region but the status word and the
+    completion counters); each call must match a call on a fresh workspace."""
+    L = synth_lib.make_layer(E=64, T=300, H=256, I=256, top_k=4, seed=77, w_std=0.05,
+                             router_w_std=0.05)
+    dev = to_device(L)
+    big = moe.alloc_workspace(moe.layer_shape(L, 300))
+    for T in (300, 33, 1, 300, 64):
+        ids_a, w_a, out_a, _ = gpu_forward(moe, L, dev=dev, T=T, workspace=big)
+        ids_b, w_b, out_b, _ = gpu_forward(moe, L, dev=dev, T=T)
+        assert moe.moe_get_device_status(big) == 0
+        assert torch.equal(ids_a, ids_b) and torch.equal(w_a, w_b)
+        assert (out_a - out_b).abs().max().item() <= 1e-5 * out_b.abs().max().item()
