@@ -32,12 +32,18 @@
 //                              shfl.xor 1), clamp, GLU, bf16 store of h;
 //                 kEpiCombine: + bias, x routing weight, red.global.add.f32
 //                              into out[token, row].
-//   warps 6..9  (MXFP4 only) converters: thread r expands row r of the code
-//               tile to bf16 (E2M1 via byte-permute lookups -- every E2M1
-//               value is a normal bf16 -- times 2^(s-127), an exact bf16x2
-//               multiply), writes the 128-byte-swizzled A tile, fences the
-//               async proxy and arrives on the slot's "converted" barrier,
-//               which the MMA issuer waits for.
+//   warps 6..21 (MXFP4 only) converters, two teams of 8 warps taking
+//               alternate k-blocks: two threads per weight row, each
+//               expanding half a row of the code tile to bf16 (E2M1 by
+//               integer multiplies into bf16 bit positions, times
+//               2^(s-127) by an exact bf16x2 multiply) and storing it to
+//               TMEM (tcgen05.st: the row's lane, 32 columns per A tile);
+//               one lane per warp then arrives on the A slot's "converted"
+//               barrier, which the MMA issuer waits for.  The MMAs read A
+//               from TMEM and the token tile from shared memory, so the
+//               converted tile costs no shared-memory bandwidth.  MXFP4 uses
+//               two rings: `stages` slots of code + token tiles (deep, to
+//               keep HBM busy) and `astages` A tiles in TMEM.
 // The two accumulators let the epilogue of one unit overlap the main loop
 // of the next.  Tails: weight rows past the matrix are zero-filled by TMA
 // and masked at the store; token rows past the tile are computed on
@@ -55,24 +61,33 @@ namespace moe {
 namespace {
 
 constexpr int kEpiThreads = 128;
-constexpr int kConvThreads = 256;   // two threads per weight row (half a row each)
+constexpr int kConvThreads = 256;   // per team: two threads per weight row (half a row each)
+constexpr int kConvTeams = 2;
 constexpr uint32_t kATileBytes = kWeightTileRows * kBlockK * 2;      // 16 KB bf16
-constexpr uint32_t kCodeTileBytes = kWeightTileRows * kBlockK / 2;   // 4 KB E2M1
-constexpr int kMaxStages = 12;
+// k-blocks (of 64) per ring slot: MXFP4 slots carry 4, so that each slot is
+// two TMA operations of 16 KB codes + 4 token chunks (an SM keeps only about
+// ten TMA operations in flight, so bytes per operation set the bandwidth).
+template <int WF>
+constexpr int kKbPerStage = WF == 1 ? kMxfp4KbPerStage : 1;
+constexpr uint32_t kCodeStageBytes = kWeightTileRows * kMxfp4KbPerStage * kBlockK / 2;  // 16 KB
+constexpr uint32_t kASlotCols = 32u * kMxfp4KbPerStage;    // TMEM columns of one MXFP4 A slot
+constexpr int kMaxStages = 24;
+constexpr int kBarBytes = 768;
 
 template <int WF>
-constexpr int kThreadsOf = WF == 1 ? 192 + kConvThreads : 192;
+constexpr int kThreadsOf = WF == 1 ? 192 + kConvTeams * kConvThreads : 192;
 
 struct SmemPlan {
     uint8_t* a;          // stages x 16 KB bf16 W tiles (1024-aligned)
-    uint8_t* b;          // stages x box*128 B token tiles (1024-aligned)
-    uint8_t* codes;      // stages x 4 KB E2M1 tiles (MXFP4)
+    uint8_t* b;          // stages x kb_per_stage x box*128 B token tiles (1024-aligned)
+    uint8_t* codes;      // stages x 16 KB E2M1 tiles [128 rows x 128 B], 128-byte swizzled (MXFP4)
     uint8_t* scales;     // 2 x 128*kscale B (MXFP4)
     int* meta_tok;       // [box] token of each tile row (combine)
     float* meta_w;       // [box] routing weight of each tile row (combine)
     uint64_t* full;      // [stages] TMA landed
-    uint64_t* conv;      // [stages] A tile converted (MXFP4)
     uint64_t* empty;     // [stages] MMAs done with the slot
+    uint64_t* afull;     // [astages] A tile converted (MXFP4)
+    uint64_t* aempty;    // [astages] MMAs done with the A tile (MXFP4)
     uint64_t* tfull;     // [2]
     uint64_t* tempty;    // [2]
     uint64_t* sfull;     // [2] scales landed (MXFP4)
@@ -82,19 +97,22 @@ struct SmemPlan {
     int* flags;          // [0] abort, [1..2] epilogue broadcast (alternating)
 };
 
-__device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int box, int wf,
-                                              int kscale) {
+// bf16: one ring of `stages` slots, each a W tile + a token tile.
+// MXFP4: one ring of `stages` slots, each a code tile + a token tile; the
+// converted bf16 W tiles live in TMEM, not here.
+__device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int astages, int box,
+                                              int wf, int kscale) {
     SmemPlan s;
     const uint32_t base = smem_u32(raw);
     uint8_t* p = raw + ((1024u - (base & 1023u)) & 1023u);
     s.a = p;
-    p += static_cast<size_t>(stages) * kATileBytes;
+    p += static_cast<size_t>(wf == 1 ? 0 : stages) * kATileBytes;
     s.b = p;
-    p += static_cast<size_t>(stages) * box * 128;
+    p += static_cast<size_t>(stages) * (wf == 1 ? kMxfp4KbPerStage : 1) * box * 128;
     s.codes = p;
     s.scales = p;
     if (wf == 1) {
-        p += static_cast<size_t>(stages) * kCodeTileBytes;
+        p += static_cast<size_t>(stages) * kCodeStageBytes;
         s.scales = p;
         p += 2 * ((kWeightTileRows * kscale + 15) / 16 * 16);
     }
@@ -104,9 +122,10 @@ __device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int box,
     p += box * 4;
     uint64_t* bars = reinterpret_cast<uint64_t*>(p);
     s.full = bars;
-    s.conv = bars + stages;
-    s.empty = bars + 2 * stages;
-    s.tfull = bars + 3 * stages;
+    s.empty = bars + stages;
+    s.afull = bars + 2 * stages;
+    s.aempty = s.afull + astages;
+    s.tfull = s.aempty + astages;
     s.tempty = s.tfull + 2;
     s.sfull = s.tempty + 2;
     s.sempty = s.sfull + 2;
@@ -133,33 +152,45 @@ __device__ __forceinline__ float clamped_glu(float gate, float up) {
     return (up + 1.0f) * g;
 }
 
-// Eight E2M1 codes (one 32-bit word, element 2i in the low nibble of byte i)
-// to eight bf16 values times 2^(s-127).
+// Eight E2M1 codes (one 32-bit word, code q in nibble q) to eight bf16
+// values times 2^(s-127), as four bf16x2 words holding the codes in the
+// order (0,4), (1,5), (2,6), (3,7).  The tile's K positions are permuted the
+// same way within every group of 8, and so are the token operand's (the
+// gather and the GLU epilogue store them in that order), so the products
+// and their sum over K are unchanged.
 //
-// For the byte b of elements (2i, 2i+1), two integer multiplies place the
-// nibbles at the bf16 bit positions: b * (2^6 + 2^18) puts the magnitude bits
-// (exponent e, mantissa m) of the low nibble at bits 6..8 and of the high
-// nibble at 22..24; b * (2^12 + 2^24) puts their sign bits at 15 and 31.
-// Read as bf16, each half is then exactly e2m1(code) * 2^-126 -- a normal
-// number for e >= 1 and the subnormal 2^-127 for the code 0.5 (e = 0,
-// m = 1) -- so one exact bf16x2 multiply by 2^(s-1) yields
-// e2m1(code) * 2^(s-127).  The multiplies run on the FMA pipe, leaving the
-// integer pipe two masks and one byte extraction per pair.
+// Codes q and q+4 sit 16 bits apart, one per bf16 half.  Masking the pair
+// and multiplying by 2^a + 2^(a+6) leaves two non-overlapping copies of each
+// nibble (no carries): the first puts the magnitude bits (exponent e,
+// mantissa m) at bits 6..8 of its half, the second the sign at bit 15.  Read
+// as bf16, each half is then exactly e2m1(code) * 2^-126 -- a normal number
+// for e >= 1 and the subnormal 2^-127 for the code 0.5 (e = 0, m = 1) -- so
+// one exact bf16x2 multiply by 2^(s-1) yields e2m1(code) * 2^(s-127).  Per
+// pair of values: AND, IMAD, AND on the integer pipes, one multiply on the
+// FMA pipe.
+template <bool kTwoFactors>
 __device__ __forceinline__ uint4 e2m1x8_to_bf16(uint32_t w, uint32_t scale2, uint32_t scale2b) {
+    const uint32_t w2 = w >> 8;
+    const uint32_t emb[4] = {((w & 0x000F000Fu) * 0x1040u) & 0x81C081C0u,
+                             ((w & 0x00F000F0u) * 0x0104u) & 0x81C081C0u,
+                             ((w2 & 0x000F000Fu) * 0x1040u) & 0x81C081C0u,
+                             ((w2 & 0x00F000F0u) * 0x0104u) & 0x81C081C0u};
     uint4 r;
     uint32_t* rr = reinterpret_cast<uint32_t*>(&r);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t b = __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(i));
-        const uint32_t mag = (b * 0x00040040u) & 0x01C001C0u;
-        const uint32_t emb = mag | ((b * 0x01001000u) & 0x80008000u);
-        __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&emb),
+        __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&emb[i]),
                                    *reinterpret_cast<const __nv_bfloat162*>(&scale2));
-        if (scale2b != 0x3F803F80u)   // only for scales above 2^1 (s > 128)
+        if (kTwoFactors)   // only for scales above 2^1 (s > 128)
             v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&scale2b));
         rr[i] = *reinterpret_cast<uint32_t*>(&v);
     }
     return r;
+}
+
+// Column c of a row stored in the order above: position of natural column c.
+__device__ __forceinline__ int kperm8_pos(int c) {
+    return (c & ~7) | ((c & 3) << 1) | ((c >> 2) & 1);
 }
 
 // The factor(s) that turn an embedded code into e2m1(code) * 2^(s-127),
@@ -185,9 +216,27 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     grouped_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x) {
     extern __shared__ uint8_t smem_raw[];
-    const int stages = p.stages, box = p.token_box;
-    const uint32_t b_bytes = static_cast<uint32_t>(box) * 128u;
-    SmemPlan sm = plan_smem(smem_raw, stages, box, WF, p.kscale);
+    constexpr int KPS = kKbPerStage<WF>;
+    const int stages = p.stages, astages = p.astages, box = p.token_box;
+    // TMEM columns: two accumulators of acc_stride columns, then (MXFP4)
+    // astages A slots of 128 columns, each the converted weights of one ring
+    // slot (4 k-blocks x 32 columns: 128 rows x 64 bf16 per k-block)
+    const uint32_t acc_stride = WF == 1 ? static_cast<uint32_t>((box + 31) & ~31)
+                                        : static_cast<uint32_t>(p.tmem_cols) / 2u;
+    const uint32_t a_col0 = 2u * acc_stride;
+    // ring sizes the converter teams rely on and the TMEM plan (uniform
+    // exit, nothing started)
+    if (stages < 2 || stages > kMaxStages ||
+        (WF == 1 && (astages < 2 || astages > kMxfp4AStages || 2 * stages < astages + 2 ||
+                     a_col0 + kASlotCols * static_cast<uint32_t>(astages) >
+                         static_cast<uint32_t>(p.tmem_cols)))) {
+        if (threadIdx.x == 0) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
+        return;
+    }
+    const uint32_t b_bytes = static_cast<uint32_t>(box) * 128u;       // one 64-wide K chunk
+    const uint32_t b_stage_bytes = b_bytes * KPS;
+    const int n_st = (p.k_blocks + KPS - 1) / KPS;                     // ring slots per unit
+    SmemPlan sm = plan_smem(smem_raw, stages, astages, box, WF, p.kscale);
     volatile int* flags = sm.flags;
     const uint32_t scale_buf_bytes =
         static_cast<uint32_t>((kWeightTileRows * p.kscale + 15) / 16 * 16);
@@ -197,14 +246,17 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(sm.full + s), 1);
-            mbar_init(smem_u32(sm.conv + s), kConvThreads);
             mbar_init(smem_u32(sm.empty + s), 1);
+        }
+        for (int s = 0; s < astages; ++s) {
+            mbar_init(smem_u32(sm.afull + s), kConvThreads / 32);
+            mbar_init(smem_u32(sm.aempty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(sm.tfull + b), 1);
             mbar_init(smem_u32(sm.tempty + b), kEpiThreads);
             mbar_init(smem_u32(sm.sfull + b), 1);
-            mbar_init(smem_u32(sm.sempty + b), kConvThreads);
+            mbar_init(smem_u32(sm.sempty + b), kConvTeams * kConvThreads);
         }
         mbar_init(smem_u32(sm.drain), 1);
         flags[0] = 0;
@@ -224,7 +276,6 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_base;
-    const uint32_t acc_stride = static_cast<uint32_t>(p.tmem_cols) / 2u;
 
     pdl_wait();                 // tiles, activations and outputs of earlier kernels
     pdl_launch_dependents();
@@ -236,7 +287,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            const uint32_t w_bytes = WF == 1 ? kCodeTileBytes : kATileBytes;
+            const uint32_t w_bytes = WF == 1 ? kCodeStageBytes : kATileBytes;
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -265,22 +316,28 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                               bytes, sf);
                 }
                 ++local;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int st = 0; st < n_st; ++st) {
                     if (!mbar_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
                         raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_u32(sm.full + stage);
-                    mbar_arrive_expect_tx(fb, w_bytes + b_bytes);
-                    if (WF == 1)
-                        tma_load_3d(smem_u32(sm.codes + static_cast<size_t>(stage) * kCodeTileBytes),
-                                    &tmap_w, fb, kb * (kBlockK / 2), mb * kWeightTileRows, t.x, pol_w);
-                    else
+                    // full boxes are counted, zero-filled past K included
+                    mbar_arrive_expect_tx(fb, w_bytes + b_stage_bytes);
+                    const uint32_t b_dst = smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
+                    if (WF == 1) {
+                        // codes of k-blocks 4st..4st+3 (128 B per row), and the
+                        // token rows' K chunks 4st..4st+3 (chunk-major operand)
+                        tma_load_3d(smem_u32(sm.codes + static_cast<size_t>(stage) * kCodeStageBytes),
+                                    &tmap_w, fb, st * KPS * (kBlockK / 2), mb * kWeightTileRows, t.x,
+                                    pol_w);
+                        tma_load_3d(b_dst, &tmap_x, fb, 0, t.y, st * KPS, pol_x);
+                    } else {
                         tma_load_3d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
-                                    &tmap_w, fb, kb * kBlockK, mb * kWeightTileRows, t.x, pol_w);
-                    tma_load_2d(smem_u32(sm.b + static_cast<size_t>(stage) * b_bytes), &tmap_x, fb,
-                                kb * kBlockK, t.y, pol_x);
+                                    &tmap_w, fb, st * kBlockK, mb * kWeightTileRows, t.x, pol_w);
+                        tma_load_2d(b_dst, &tmap_x, fb, st * kBlockK, t.y, pol_x);
+                    }
                     ++issued;
                     if (++stage == stages) {
                         stage = 0;
@@ -313,6 +370,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            int astage = 0;
+            uint32_t aphase = 0;
             int local = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
@@ -330,21 +389,50 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * acc_stride;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    const uint32_t ready = smem_u32((WF == 1 ? sm.conv : sm.full) + stage);
-                    if (!mbar_wait(ready, phase, flags)) {
+                for (int st = 0; st < n_st && ok; ++st) {
+                    const int nk = min(KPS, p.k_blocks - st * KPS);
+                    // bf16: the slot's tiles have landed.  MXFP4: its A slot
+                    // is converted (which implies the codes and token chunks
+                    // landed).  One wait per slot: a wait issued behind
+                    // in-flight MMAs costs about as much as four N = 16 MMAs.
+                    const uint32_t ready =
+                        WF == 1 ? smem_u32(sm.afull + astage) : smem_u32(sm.full + stage);
+                    if (!mbar_wait(ready, WF == 1 ? aphase : phase, flags)) {
                         raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes);
-                    const uint32_t b_addr = smem_u32(sm.b + static_cast<size_t>(stage) * b_bytes);
+                    const uint32_t b_stage =
+                        smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
+                    const uint32_t a_tm = tmem_base + a_col0 + kASlotCols * static_cast<uint32_t>(astage);
+                    for (int jj = 0; jj < nk; ++jj) {
+                        const int kb = st * KPS + jj;
+                        const uint32_t b_addr = b_stage + static_cast<uint32_t>(jj) * b_bytes;
+                        if (WF == 1) {
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                        tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
-                                    smem_desc_sw128(b_addr + kk * 32), idesc,
-                                    (kb | kk) != 0 ? 1u : 0u);
+                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                                tc_mma_bf16_ts(d_tmem, a_tm + 32u * jj + 8u * kk,
+                                               smem_desc_sw128(b_addr + kk * 32), idesc,
+                                               (kb | kk) != 0 ? 1u : 0u);
+                            }
+                        } else {
+                            const uint32_t a_addr =
+                                smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes);
+#pragma unroll
+                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                                tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
+                                            smem_desc_sw128(b_addr + kk * 32), idesc,
+                                            (kb | kk) != 0 ? 1u : 0u);
+                            }
+                        }
+                    }
+                    if (WF == 1) {
+                        tc_commit(smem_u32(sm.aempty + astage));
+                        if (++astage == astages) {
+                            astage = 0;
+                            aphase ^= 1u;
+                        }
                     }
                     tc_commit(smem_u32(sm.empty + stage));
                     if (++stage == stages) {
@@ -412,8 +500,15 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     // even lane: gate row 2j, odd lane: up row 2j+1 (same j)
                     const bool odd = lane & 1;
                     const int hcols = p.w_rows >> 1;
+                    // MXFP4: h is the down projection's token operand in its
+                    // layout -- chunk-major [I/64][T*k][64], each group of 8
+                    // columns in the order 0,4,1,5,2,6,3,7
+                    const int hcol = WF == 1 ? kperm8_pos(wrow >> 1) : (wrow >> 1);
                     __nv_bfloat16* hrow0 =
-                        p.h + static_cast<size_t>(t.y) * hcols + (wrow >> 1);
+                        WF == 1 ? p.h + (static_cast<size_t>(hcol >> 6) * p.rows_total + t.y) * 64 +
+                                      (hcol & 63)
+                                : p.h + static_cast<size_t>(t.y) * hcols + hcol;
+                    const size_t hstride = WF == 1 ? 64 : static_cast<size_t>(hcols);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float send = odd ? v[i] : v[8 + i];
@@ -422,7 +517,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                         const float up = odd ? v[8 + i] : recv;
                         const int c = c0 + i + (odd ? 8 : 0);
                         if (c < t.z)
-                            hrow0[static_cast<size_t>(c) * hcols] =
+                            hrow0[static_cast<size_t>(c) * hstride] =
                                 __float2bfloat16_rn(clamped_glu(gate, up));
                     }
                 } else {
@@ -443,13 +538,28 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         }
     } else if (WF == 1) {
         // ------------------------------------------------ MXFP4 converters
-        const int ct = threadIdx.x - 192;         // 0..255
-        const int r = ct & 127;                   // weight row within the tile
-        const int half = ct >> 7;                 // chunks 4*half .. 4*half+3 of the row
-        const uint32_t a_row_off = static_cast<uint32_t>(r) * 128u;
+        // Two teams of 8 warps take alternate ring slots (team = parity of
+        // the slot use g): a team converts the slot's (up to) 4 k-blocks into
+        // A slot g % astages in TMEM, then each warp arrives once on its
+        // barrier.  Barrier waits cost tens of nanoseconds even when ready,
+        // so they are taken once per slot, not per k-block.  A wait never
+        // passes two phases early: a team at use g has finished g-2, which
+        // needed the MMAs of use g-2-astages, so (MMAs completing in order)
+        // every use up to g-2-astages is complete -- the use before the
+        // previous one of g's A slot (astages >= 2) and of g's code slot
+        // (2 x stages >= astages + 2).  Arrivals for use g come only after
+        // the MMAs of use g-astages, i.e. after that phase was consumed.
+        // A warp may touch only its own TMEM lane quadrant (warp % 4), so
+        // the warp's rows are that quadrant's 32 rows.
+        const int cw_idx = warp - 6;              // 0..15
+        const int team = cw_idx >> 3;
+        const int half = (cw_idx >> 2) & 1;       // K 32*half .. 32*half+31 of each k-block
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;           // weight row within the tile
+        const uint32_t a_tm_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + a_col0 +
+                                  16u * static_cast<uint32_t>(half);
         const uint32_t swz = static_cast<uint32_t>(r & 7);
-        int stage = 0;
-        uint32_t phase = 0;
+        int sbase = 0;                            // ring use of the unit's first slot
         int local = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
@@ -458,7 +568,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             const int sb = local & 1;
             const uint32_t sph = static_cast<uint32_t>(local >> 1) & 1u;
             ++local;
-            if (!mbar_wait(smem_u32(sm.sfull + sb), sph, flags)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(sm.sfull + sb), sph, flags))) {
                 raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                 break;
             }
@@ -466,32 +576,57 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             // rows past the matrix: codes are TMA zero-fill and no scale bytes
             // were copied for them; use scale 1 so they stay exactly zero
             const bool row_ok = (u % p.n_wblocks) * kWeightTileRows + r < p.w_rows;
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
-                if (!mbar_wait(smem_u32(sm.full + stage), phase, flags)) {
+            for (int st = (team ^ sbase) & 1; st < n_st; st += 2) {
+                const int use = sbase + st;
+                const int stage = use % stages;
+                const uint32_t phase = static_cast<uint32_t>(use / stages) & 1u;
+                const int aslot = use % astages;
+                const uint32_t aphase = static_cast<uint32_t>(use / astages) & 1u;
+                // the outcome is made warp-uniform: the lanes must not split
+                // before the warp's single arrival below
+                const bool got = mbar_wait(smem_u32(sm.full + stage), phase, flags) &&
+                                 mbar_wait(smem_u32(sm.aempty + aslot), aphase ^ 1u, flags);
+                if (!__all_sync(0xffffffffu, got)) {
                     raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                     ok = false;
                     break;
                 }
-                uint32_t f1, f2;
-                e8m0_factors(row_ok ? srow[2 * kb + half] : 127u, f1, f2);
-                const uint4 cw = *reinterpret_cast<const uint4*>(
-                    sm.codes + static_cast<size_t>(stage) * kCodeTileBytes + r * 32 + half * 16);
-                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-                uint8_t* arow = sm.a + static_cast<size_t>(stage) * kATileBytes + a_row_off;
+                const int nk = min(KPS, p.k_blocks - st * KPS);
+                const uint8_t* crow = sm.codes + static_cast<size_t>(stage) * kCodeStageBytes + r * 128;
+                const uint32_t a_tm = a_tm_row + kASlotCols * static_cast<uint32_t>(aslot);
+                for (int jj = 0; jj < nk; ++jj) {
+                    const int kb = st * KPS + jj;
+                    uint32_t f1, f2;
+                    e8m0_factors(row_ok ? srow[2 * kb + half] : 127u, f1, f2);
+                    // 16-byte unit jj * 2 + half of the row, 128-byte swizzled
+                    const uint32_t unit = static_cast<uint32_t>(jj * 2 + half);
+                    const uint4 cw = *reinterpret_cast<const uint4*>(crow + ((unit ^ swz) << 4));
+                    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                    uint32_t v[16];
+                    if (f2 == 0x3F803F80u) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t chunk = static_cast<uint32_t>(4 * half + c);
-                    const uint4 v = e2m1x8_to_bf16(words[c], f1, f2);
-                    *reinterpret_cast<uint4*>(arow + ((chunk ^ swz) << 4)) = v;
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 q = e2m1x8_to_bf16<false>(words[c], f1, f2);
+                            v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 q = e2m1x8_to_bf16<true>(words[c], f1, f2);
+                            v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
+                        }
+                    }
+                    // row r, columns 32*jj + 16*half .. +15 of the A slot (word c
+                    // of the thread's 16 B of codes = K 8c..8c+7 = columns 4c..4c+3)
+                    tmem_st16(a_tm + 32u * static_cast<uint32_t>(jj), v);
                 }
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(sm.conv + stage));
-                if (++stage == stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(sm.afull + aslot));
             }
             if (!ok) break;
+            sbase += n_st;
             mbar_arrive(smem_u32(sm.sempty + sb));
         }
     }

@@ -67,8 +67,8 @@ moe_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     return MOE_OK;
 }
 
-// bf16 tensors use the 128-byte swizzle (box inner extent 64 elements =
-// 128 B); MXFP4 code tensors are plain bytes without swizzle.
+// Every map uses the 128-byte swizzle: box inner extent 128 B (64 bf16
+// elements, or 128 MXFP4 code bytes = 4 k-blocks of one row).
 moe_status make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
                      const cuuint64_t* strides, const cuuint32_t* box, bool bytes = false) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
@@ -78,20 +78,21 @@ moe_status make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_
     CUresult r = enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                      static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box,
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// 3-D map over one expert weight bank [E, rows, K]: bf16 values or MXFP4
-// codes (K/2 bytes per row); box = 64 K elements x 128 rows x 1 expert.
+// 3-D map over one expert weight bank [E, rows, K]: bf16 values (box 64 K
+// elements x 128 rows x 1 expert) or MXFP4 codes (K/2 bytes per row; box
+// 128 bytes = kMxfp4KbPerStage k-blocks x 128 rows x 1 expert).
 moe_status weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K, bool mxfp4) {
     const cuuint64_t row_bytes = mxfp4 ? static_cast<cuuint64_t>(K) / 2
                                        : static_cast<cuuint64_t>(K) * 2;
     const cuuint64_t dims[3] = {mxfp4 ? static_cast<cuuint64_t>(K) / 2 : static_cast<cuuint64_t>(K),
                                 static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(E)};
     const cuuint64_t str[2] = {row_bytes, row_bytes * static_cast<cuuint64_t>(rows)};
-    const cuuint32_t boxd[3] = {mxfp4 ? 32u : 64u, 128u, 1u};
+    const cuuint32_t boxd[3] = {mxfp4 ? kMxfp4KbPerStage * 32u : 64u, 128u, 1u};
     return make_tmap(m, w, 3, dims, str, boxd, mxfp4);
 }
 
@@ -174,11 +175,20 @@ moe_status check_ptr(const void* p) {
         if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
     } while (0)
 
-int auto_token_tile(int T) {
+// Rows of tokens per GEMM tile: round_up(T, 16), in [16, 256] -- a box
+// that fits every expert's rows when T is small (one tile per touched
+// expert), the widest MMA N otherwise.  Measured at T = 64 (k = 4, E = 32),
+// boxes of 16 or 32 rows (about the mean rows per expert) are 4-6 % slower
+// than 64: more tiles re-stream the same weight blocks.
+// MXFP4 tiles (tuned or not) are capped at kMxfp4MaxTokenTile rows, the
+// most TMEM holds next to the converted weight tiles.
+int auto_token_tile(const moe_shape& s) {
     const int tuned = g_token_tile.load();
-    if (tuned > 0) return tuned;
-    int t = (T + 15) / 16 * 16;
-    return t < kMaxTokenTile ? t : kMaxTokenTile;
+    long long t = tuned > 0 ? tuned : (static_cast<long long>(s.T) + 15) / 16 * 16;
+    if (t < 16) t = 16;
+    if (t > kMaxTokenTile) t = kMaxTokenTile;
+    if (s.wfmt == MOE_W_MXFP4 && t > kMxfp4MaxTokenTile) t = kMxfp4MaxTokenTile;
+    return static_cast<int>(t);
 }
 
 int next_pow2(int v) {
@@ -273,6 +283,7 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     pp.sorted_assign = r.sorted_assign;
     pp.assign_row = reinterpret_cast<int32_t*>(ws + L.assign_row);
     pp.x_perm = x_perm;
+    pp.mx_layout = s.wfmt == MOE_W_MXFP4 ? 1 : 0;
     pp.status = status;
     MOE_CUDA(launch_permute(pp, stream, g_pdl.load() != 0));
     prof_mark(x_perm ? "permute_gather" : "permute", stream);
@@ -320,7 +331,7 @@ moe_status moe_route(const moe_shape* shape, const void* hidden, const void* rou
     std::lock_guard<std::mutex> lock(g_prof_mu);
     prof_reset(stream);
     const moe_status st = launch_routing(s, L, ws, hidden, router_w, router_b, r, nullptr,
-                                         nullptr, auto_token_tile(s.T), dev, stream);
+                                         nullptr, auto_token_tile(s), dev, stream);
     prof_finish();
     return st;
 }
@@ -356,20 +367,33 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     const int R = s.T * s.top_k;
-    const int box = auto_token_tile(s.T);
+    const int box = auto_token_tile(s);
     const bool pdl = g_pdl.load() != 0;
 
     // Pipeline depth: as many stages as the shared memory allows (2..12).
     const int wf = mxfp4 ? 1 : 0;
     const int kscale_max = (s.H > s.I ? s.H : s.I) / 32;
     const size_t stage_bytes = gemm_stage_bytes(box, wf);
-    const size_t fixed = gemm_fixed_bytes(box, wf, kscale_max);
     const size_t budget = static_cast<size_t>(dev.max_smem) - 1024;
-    if (budget < fixed + 2 * stage_bytes) return MOE_ERR_UNSUPPORTED;
-    int stages = static_cast<int>((budget - fixed) / stage_bytes);
-    if (stages > 12) stages = 12;
+    // MXFP4: A slots of 128 TMEM columns after two accumulators of
+    // round_up(box, 32) columns, all in 512
+    int astages = 0;
+    if (mxfp4) {
+        astages = (512 - 2 * ((box + 31) & ~31)) / 128;
+        if (astages > kMxfp4AStages) astages = kMxfp4AStages;
+        if (astages < 2) return MOE_ERR_UNSUPPORTED;
+    }
+    const size_t fixed = gemm_fixed_bytes(box, wf, kscale_max);
+    int stages = budget < fixed ? 0 : static_cast<int>((budget - fixed) / stage_bytes);
+    // MXFP4 converter teams need 2 x stages >= astages + 2
+    if (stages < 2 || (mxfp4 && 2 * stages < astages + 2)) return MOE_ERR_UNSUPPORTED;
+    const int max_stages = mxfp4 ? 24 : 12;   // MXFP4 slots carry 4 KB of HBM bytes
+    if (stages > max_stages) stages = max_stages;
     const size_t smem = fixed + stages * stage_bytes + 1024;
-    const int tmem_cols = next_pow2(2 * box < 32 ? 32 : 2 * box);
+    // two accumulators (+ MXFP4: A tiles of 32 columns after them)
+    const int tmem_cols =
+        mxfp4 ? 512 : next_pow2(2 * box < 32 ? 32 : 2 * box);
+    if (tmem_cols > 512) return MOE_ERR_UNSUPPORTED;
 
     __nv_bfloat16* x_perm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm);
     __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
@@ -379,18 +403,24 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     CUtensorMap tm_wgu, tm_x, tm_wd, tm_h;
     MOE_TRY(weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H, mxfp4));
     MOE_TRY(weight_tmap(&tm_wd, down.w, s.E, s.H, s.I, mxfp4));
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(R)};
-        const cuuint64_t str[1] = {static_cast<cuuint64_t>(s.H) * 2};
+    // Token operands: bf16 layers read [R, K] row-major, one 64-wide K chunk
+    // per box; MXFP4 layers read the chunk-major [K/64, R, 64] layout the
+    // gather and the GLU epilogue write, kMxfp4KbPerStage chunks per box.
+    const auto token_tmap = [&](CUtensorMap* m, const void* base, int K) {
+        if (mxfp4) {
+            const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(R),
+                                        static_cast<cuuint64_t>(K) / 64};
+            const cuuint64_t str[2] = {128, static_cast<cuuint64_t>(R) * 128};
+            const cuuint32_t boxd[3] = {64, static_cast<cuuint32_t>(box), kMxfp4KbPerStage};
+            return make_tmap(m, base, 3, dims, str, boxd);
+        }
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(R)};
+        const cuuint64_t str[1] = {static_cast<cuuint64_t>(K) * 2};
         const cuuint32_t boxd[2] = {64, static_cast<cuuint32_t>(box)};
-        MOE_TRY(make_tmap(&tm_x, x_perm, 2, dims, str, boxd));
-    }
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.I), static_cast<cuuint64_t>(R)};
-        const cuuint64_t str[1] = {static_cast<cuuint64_t>(s.I) * 2};
-        const cuuint32_t boxd[2] = {64, static_cast<cuuint32_t>(box)};
-        MOE_TRY(make_tmap(&tm_h, h, 2, dims, str, boxd));
-    }
+        return make_tmap(m, base, 2, dims, str, boxd);
+    };
+    MOE_TRY(token_tmap(&tm_x, x_perm, s.H));
+    MOE_TRY(token_tmap(&tm_h, h, s.I));
 
     std::lock_guard<std::mutex> lock(g_prof_mu);
     prof_reset(stream);
@@ -408,6 +438,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.num_tiles = status + kNumTilesWord;
     g.token_box = box;
     g.stages = stages;
+    g.astages = astages;
     g.tmem_cols = tmem_cols;
     g.num_experts = s.E;
     g.rows_total = R;

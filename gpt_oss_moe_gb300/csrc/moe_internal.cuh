@@ -123,6 +123,9 @@ struct PermuteParams {
     int32_t* sorted_assign;      // [T*k]
     int32_t* assign_row;         // [T*k]
     __nv_bfloat16* x_perm;       // [T*k, H] or null (no gather)
+    int mx_layout;               // MXFP4 operand layout: chunk-major
+                                 // [H/64][T*k][64], each group of 8 columns
+                                 // in the order 0,4,1,5,2,6,3,7
     int32_t* status;
 };
 
@@ -137,7 +140,8 @@ struct GemmParams {
     int k_blocks;                // K / 64
     int w_rows;                  // weight rows per expert (2I or H)
     int token_box;               // token rows per TMA box (= MMA N bound)
-    int stages;
+    int stages;                  // ring of W (bf16) or code (MXFP4) + token tiles
+    int astages;                 // MXFP4: ring of converted bf16 W tiles
     int tmem_cols;               // allocated TMEM columns (2 accumulators)
     int num_experts;             // E (tile bounds check)
     int rows_total;              // T * k (tile bounds check)
@@ -155,17 +159,25 @@ struct GemmParams {
 };
 
 // Shared memory of one GEMM pipeline stage and of the fixed part (bytes,
-// excluding the 1 KB alignment slack).  wf: 0 = bf16, 1 = MXFP4.
+// excluding the 1 KB alignment slack).  wf: 0 = bf16, 1 = MXFP4.  An MXFP4
+// stage holds kMxfp4KbPerStage k-blocks (codes [128 x 128 B] + that many
+// 64-wide token chunks); its converted weights take an A slot of 128 TMEM
+// columns after the two accumulators -- up to kMxfp4AStages slots, as many
+// as fit in 512 columns (3 for token tiles up to 64 rows, 2 for 128) --
+// and token tiles are at most kMxfp4MaxTokenTile rows.
+constexpr int kMxfp4AStages = 3;
+constexpr int kMxfp4MaxTokenTile = 128;
+constexpr int kMxfp4KbPerStage = 4;     // k-blocks of 64 per MXFP4 ring slot
 inline size_t gemm_stage_bytes(int token_box, int wf) {
     size_t a = static_cast<size_t>(kWeightTileRows) * kBlockK * 2;
     size_t b = static_cast<size_t>(token_box) * kBlockK * 2;
-    size_t codes = wf == 1 ? static_cast<size_t>(kWeightTileRows) * kBlockK / 2 : 0;
-    return a + b + codes;
+    size_t codes = static_cast<size_t>(kWeightTileRows) * kBlockK / 2;
+    return wf == 1 ? kMxfp4KbPerStage * (codes + b) : a + b;
 }
 inline size_t gemm_fixed_bytes(int token_box, int wf, int kscale) {
     size_t scales = wf == 1 ? 2 * align_up(static_cast<size_t>(kWeightTileRows) * kscale, 16) : 0;
     size_t meta = static_cast<size_t>(token_box) * 8;
-    size_t bars = 512;
+    size_t bars = 768;
     return scales + meta + bars;
 }
 

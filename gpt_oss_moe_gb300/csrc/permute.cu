@@ -12,6 +12,10 @@
 //   2. copies its share (1/gather_split) of those assignments' activation
 //      rows into x_perm[row] -- the contiguous per-expert operand of the
 //      gate_up GEMM -- one warp per row, 16-byte loads kept in flight.
+//      With MXFP4 weights x_perm takes the layout that GEMM reads: chunk-
+//      major [H/64][T*k][64] (one TMA box then spans several 64-wide K
+//      chunks), each group of 8 columns in the order 0,4,1,5,2,6,3,7 (the
+//      order in which the GEMM expands E2M1 codes).
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "../../include/moe.h"
@@ -21,6 +25,16 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kRowVecUnroll = 12;   // 16-byte vectors per lane in flight (H <= 6144)
+
+// Eight bf16 (k = 0..7) to the order 0,4,1,5,2,6,3,7.
+__device__ __forceinline__ uint4 kperm8(const uint4 v) {
+    uint4 r;
+    r.x = __byte_perm(v.x, v.z, 0x5410);
+    r.y = __byte_perm(v.x, v.z, 0x7632);
+    r.z = __byte_perm(v.y, v.w, 0x5410);
+    r.w = __byte_perm(v.y, v.w, 0x7632);
+    return r;
+}
 
 __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p) {
     __shared__ int base[kMaxExperts];
@@ -94,6 +108,9 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
             if (row < 0) continue;
             const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>((a0 + la) / k) * p.H);
             uint4* dst = reinterpret_cast<uint4*>(p.x_perm + static_cast<size_t>(row) * p.H);
+            // chunk-major: vector v (8 columns) of the row goes to chunk v/8
+            uint4* dst_mx = reinterpret_cast<uint4*>(p.x_perm) + static_cast<size_t>(row) * 8;
+            const size_t chunk_vecs = static_cast<size_t>(p.T) * p.top_k * 8;
             for (int v0 = 0; v0 < vec_per_row; v0 += 32 * kRowVecUnroll) {
                 uint4 buf[kRowVecUnroll];
 #pragma unroll
@@ -104,7 +121,12 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
 #pragma unroll
                 for (int u = 0; u < kRowVecUnroll; ++u) {
                     const int v = v0 + u * 32 + lane;
-                    if (v < vec_per_row) dst[v] = buf[u];
+                    if (v < vec_per_row) {
+                        if (p.mx_layout)
+                            dst_mx[static_cast<size_t>(v >> 3) * chunk_vecs + (v & 7)] = kperm8(buf[u]);
+                        else
+                            dst[v] = buf[u];
+                    }
                 }
             }
         }

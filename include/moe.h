@@ -177,7 +177,8 @@ moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
 
 /* Process-wide tuning switches for tests and benchmarks:
  *   "token_tile": rows of tokens per GEMM tile, 0 = automatic, else a
- *                 multiple of 16 in [16, 256];
+ *                 multiple of 16 in [16, 256] (MXFP4 layers use at most
+ *                 128);
  *   "pdl":        1 = launch dependent kernels with programmatic dependent
  *                 launch (default), 0 = plain stream order.
  * Returns MOE_ERR_ARG for an unknown key or value. */
