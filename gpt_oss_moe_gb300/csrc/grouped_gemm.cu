@@ -75,7 +75,8 @@ constexpr int kMaxStages = 24;
 constexpr int kBarBytes = 768;
 
 template <int WF>
-constexpr int kThreadsOf = WF == 1 ? 192 + kConvTeams * kConvThreads : 192;
+constexpr int kThreadsOf = WF == 1 ? 192 + kConvTeams * kConvThreads + 32 : 192;
+constexpr int kSecondIssuerWarp = 6 + kConvTeams * kConvThreads / 32;    // MXFP4: warp 22
 
 struct SmemPlan {
     uint8_t* a;          // stages x 16 KB bf16 W tiles (1024-aligned)
@@ -92,7 +93,7 @@ struct SmemPlan {
     uint64_t* tempty;    // [2]
     uint64_t* sfull;     // [2] scales landed (MXFP4)
     uint64_t* sempty;    // [2] scales consumed (MXFP4)
-    uint64_t* drain;     // [1]
+    uint64_t* drain;     // [2] one per MMA issuer
     uint32_t* tmem_base;
     int* flags;          // [0] abort, [1..2] epilogue broadcast (alternating)
 };
@@ -130,7 +131,7 @@ __device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int asta
     s.sfull = s.tempty + 2;
     s.sempty = s.sfull + 2;
     s.drain = s.sempty + 2;
-    s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 2);
     s.flags = reinterpret_cast<int*>(s.tmem_base + 1);
     return s;
 }
@@ -218,15 +219,20 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     extern __shared__ uint8_t smem_raw[];
     constexpr int KPS = kKbPerStage<WF>;
     const int stages = p.stages, astages = p.astages, box = p.token_box;
-    // TMEM columns: two accumulators of acc_stride columns, then (MXFP4)
-    // astages A slots of 128 columns, each the converted weights of one ring
-    // slot (4 k-blocks x 32 columns: 128 rows x 64 bf16 per k-block)
+    // TMEM columns: per MMA issuer two accumulators of acc_stride columns
+    // (issuer i, buffer b at (2i + b) * acc_stride), then (MXFP4) astages A
+    // slots of 128 columns, each the converted weights of one ring slot
+    // (4 k-blocks x 32 columns: 128 rows x 64 bf16 per k-block).  MXFP4 runs
+    // n_iss = 2 issuers on alternate ring slots of a unit, each into its own
+    // accumulators (a thread issues an N <= 64 MMA only every ~23 ns, the
+    // tensor core takes them faster); the epilogue adds the two.
+    const int n_iss = p.n_iss;
     const uint32_t acc_stride = WF == 1 ? static_cast<uint32_t>((box + 31) & ~31)
                                         : static_cast<uint32_t>(p.tmem_cols) / 2u;
-    const uint32_t a_col0 = 2u * acc_stride;
+    const uint32_t a_col0 = 2u * static_cast<uint32_t>(n_iss) * acc_stride;
     // ring sizes the converter teams rely on and the TMEM plan (uniform
     // exit, nothing started)
-    if (stages < 2 || stages > kMaxStages ||
+    if (stages < 2 || stages > kMaxStages || n_iss < 1 || n_iss > (WF == 1 ? 2 : 1) ||
         (WF == 1 && (astages < 2 || astages > kMxfp4AStages || 2 * stages < astages + 2 ||
                      a_col0 + kASlotCols * static_cast<uint32_t>(astages) >
                          static_cast<uint32_t>(p.tmem_cols)))) {
@@ -253,12 +259,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             mbar_init(smem_u32(sm.aempty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(sm.tfull + b), 1);
+            mbar_init(smem_u32(sm.tfull + b), static_cast<uint32_t>(n_iss));
             mbar_init(smem_u32(sm.tempty + b), kEpiThreads);
             mbar_init(smem_u32(sm.sfull + b), 1);
             mbar_init(smem_u32(sm.sempty + b), kConvTeams * kConvThreads);
         }
         mbar_init(smem_u32(sm.drain), 1);
+        mbar_init(smem_u32(sm.drain + 1), 1);
         flags[0] = 0;
         flags[1] = 0;
         flags[2] = 0;
@@ -365,8 +372,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (WF == 0 && warp == 1) {
+        // ------------------------------------------------ MMA issuer (bf16)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -447,6 +454,93 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             tc_commit(smem_u32(sm.drain));
             mbar_wait(smem_u32(sm.drain), 0, nullptr);
         }
+    } else if (WF == 1 && (warp == 1 || warp == kSecondIssuerWarp)) {
+        // ------------------------------------------------ MMA issuers (MXFP4)
+        // Issuer `is` takes ring slots st = is, is + n_iss, ... of each unit.
+        const int is = warp == 1 ? 0 : 1;
+        if (lane == 0 && is < n_iss) {
+            int local = 0;
+            int sbase = 0;                        // ring use of the unit's first slot
+            // ring positions of use `cur`, advanced (not divided) to each use
+            int cur = 0, stage = 0, astage = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+                const int4 t = p.tiles[u / p.n_wblocks];
+                if (!tile_ok(t, p)) continue;
+                const uint32_t n_mma = static_cast<uint32_t>((t.z + 15) & ~15);
+                const uint32_t idesc = idesc_bf16_f32(kWeightTileRows, n_mma);
+                const int buf = local & 1;
+                const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
+                ++local;
+                if (!mbar_wait(smem_u32(sm.tempty + buf), tph ^ 1u, flags)) {
+                    raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem =
+                    tmem_base + static_cast<uint32_t>(2 * is + buf) * acc_stride;
+                for (int st = is; st < n_st && ok; st += n_iss) {
+                    for (const int use = sbase + st; cur < use; ++cur) {
+                        if (++stage == stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        if (WF == 1 && ++astage == astages) {
+                            astage = 0;
+                            aphase ^= 1u;
+                        }
+                    }
+                    const int nk = min(KPS, p.k_blocks - st * KPS);
+                    // bf16: the slot's tiles have landed.  MXFP4: its A slot
+                    // is converted (which implies the codes and token chunks
+                    // landed).  One wait per slot: a wait issued behind
+                    // in-flight MMAs costs about as much as four N = 16 MMAs.
+                    const uint32_t ready =
+                        WF == 1 ? smem_u32(sm.afull + astage) : smem_u32(sm.full + stage);
+                    if (!mbar_wait(ready, WF == 1 ? aphase : phase, flags)) {
+                        raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t b_stage =
+                        smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
+                    const uint32_t a_tm = tmem_base + a_col0 + kASlotCols * static_cast<uint32_t>(astage);
+                    for (int jj = 0; jj < nk; ++jj) {
+                        // the issuer's first MMA of the unit starts its sum
+                        const bool first = st == is && jj == 0;
+                        const uint32_t b_addr = b_stage + static_cast<uint32_t>(jj) * b_bytes;
+                        if (WF == 1) {
+#pragma unroll
+                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                                tc_mma_bf16_ts(d_tmem, a_tm + 32u * jj + 8u * kk,
+                                               smem_desc_sw128(b_addr + kk * 32), idesc,
+                                               (first && kk == 0) ? 0u : 1u);
+                            }
+                        } else {
+                            const uint32_t a_addr =
+                                smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes);
+#pragma unroll
+                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                                tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
+                                            smem_desc_sw128(b_addr + kk * 32), idesc,
+                                            (first && kk == 0) ? 0u : 1u);
+                            }
+                        }
+                    }
+                    if (WF == 1) tc_commit(smem_u32(sm.aempty + astage));
+                    tc_commit(smem_u32(sm.empty + stage));
+                }
+                if (!ok) break;
+                sbase += n_st;
+                tc_commit(smem_u32(sm.tfull + buf));
+            }
+            // Every MMA this issuer issued has finished once this arrives.
+            tc_commit(smem_u32(sm.drain + is));
+            mbar_wait(smem_u32(sm.drain + is), 0, nullptr);
+        }
     } else if (warp < 6) {
         // ------------------------------------------------ epilogue
         const int ep = threadIdx.x - 64;          // 0..127
@@ -491,9 +585,16 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                    static_cast<uint32_t>(buf) * acc_stride;
             const int n_mma = (t.z + 15) & ~15;
+            const int n_acc = min(n_iss, n_st);   // issuers that had ring slots
             for (int c0 = 0; c0 < n_mma; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+                if (n_acc > 1) {
+                    float v2[16];
+                    tmem_ld16(taddr + 2u * acc_stride + static_cast<uint32_t>(c0), v2);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += v2[i];
+                }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] += bias;
                 if (EPI == kEpiGlu) {

@@ -175,16 +175,26 @@ moe_status check_ptr(const void* p) {
         if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
     } while (0)
 
-// Rows of tokens per GEMM tile: round_up(T, 16), in [16, 256] -- a box
-// that fits every expert's rows when T is small (one tile per touched
-// expert), the widest MMA N otherwise.  Measured at T = 64 (k = 4, E = 32),
-// boxes of 16 or 32 rows (about the mean rows per expert) are 4-6 % slower
-// than 64: more tiles re-stream the same weight blocks.
-// MXFP4 tiles (tuned or not) are capped at kMxfp4MaxTokenTile rows, the
-// most TMEM holds next to the converted weight tiles.
+// Rows of tokens per GEMM tile.  bf16: round_up(T, 16), in [16, 256] -- a
+// box that fits every expert's rows when T is small (one tile per touched
+// expert), the widest MMA N otherwise; measured at T = 64 (k = 4, E = 32),
+// boxes of 16 or 32 rows are 4-6 % slower than 64 (hot experts then take
+// several tiles, re-streaming their weights).  MXFP4: about twice the mean
+// rows per expert, round_up(2 * ceil(T * k / E), 16) in [16, 128] -- its
+// ring slots carry 4 token chunks, so a smaller box buys a deeper ring (at
+// T = 64: 113 us for gate_up with 16 rows against 133 us with 64), and its
+// converted weights need TMEM beside the accumulators (at most 128 rows).
 int auto_token_tile(const moe_shape& s) {
     const int tuned = g_token_tile.load();
-    long long t = tuned > 0 ? tuned : (static_cast<long long>(s.T) + 15) / 16 * 16;
+    long long t;
+    if (tuned > 0) {
+        t = tuned;
+    } else if (s.wfmt == MOE_W_MXFP4) {
+        const long long mean = (static_cast<long long>(s.T) * s.top_k + s.E - 1) / s.E;
+        t = (2 * mean + 15) / 16 * 16;
+    } else {
+        t = (static_cast<long long>(s.T) + 15) / 16 * 16;
+    }
     if (t < 16) t = 16;
     if (t > kMaxTokenTile) t = kMaxTokenTile;
     if (s.wfmt == MOE_W_MXFP4 && t > kMxfp4MaxTokenTile) t = kMxfp4MaxTokenTile;
@@ -375,11 +385,15 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     const int kscale_max = (s.H > s.I ? s.H : s.I) / 32;
     const size_t stage_bytes = gemm_stage_bytes(box, wf);
     const size_t budget = static_cast<size_t>(dev.max_smem) - 1024;
-    // MXFP4: A slots of 128 TMEM columns after two accumulators of
-    // round_up(box, 32) columns, all in 512
-    int astages = 0;
+    // MXFP4: per MMA issuer two accumulators of round_up(box, 32) TMEM
+    // columns, then A slots of 128 columns, all in 512.  Two issuers (one N
+    // <= 64 MMA per ~23 ns each) while their accumulators leave room for two
+    // A slots, else one.
+    int astages = 0, n_iss = 1;
     if (mxfp4) {
-        astages = (512 - 2 * ((box + 31) & ~31)) / 128;
+        const int acc = (box + 31) & ~31;
+        n_iss = 2 * 2 * acc + 2 * 128 <= 512 ? 2 : 1;
+        astages = (512 - 2 * n_iss * acc) / 128;
         if (astages > kMxfp4AStages) astages = kMxfp4AStages;
         if (astages < 2) return MOE_ERR_UNSUPPORTED;
     }
@@ -439,6 +453,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.token_box = box;
     g.stages = stages;
     g.astages = astages;
+    g.n_iss = n_iss;
     g.tmem_cols = tmem_cols;
     g.num_experts = s.E;
     g.rows_total = R;

@@ -142,6 +142,7 @@ struct GemmParams {
     int token_box;               // token rows per TMA box (= MMA N bound)
     int stages;                  // ring of W (bf16) or code (MXFP4) + token tiles
     int astages;                 // MXFP4: ring of converted bf16 W tiles
+    int n_iss;                   // MMA issuers (1; MXFP4 tiles up to 64 rows: 2)
     int tmem_cols;               // allocated TMEM columns (2 accumulators)
     int num_experts;             // E (tile bounds check)
     int rows_total;              // T * k (tile bounds check)
