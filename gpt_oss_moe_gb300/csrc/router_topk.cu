@@ -19,11 +19,12 @@
 //     slice order (the same order every run);
 //   * with more than one expert group, the last group of block b gathers the
 //     block's full logit rows;
-//   * that CTA selects the top k per token -- one warp per token, lanes over
-//     experts, redux.sync for the maximum and then for the lowest expert
-//     index holding it (equal logits -> lower index) -- computes the softmax
-//     over the k selected logits (max-subtracted, expf) and counts the
-//     assignments per expert;
+//   * that CTA selects the top k per token -- one lane per token: each
+//     compute warp scans a quarter of the experts into per-lane sorted
+//     lists (strict > so equal logits keep the lower expert index), warp 0
+//     merges the four lists in expert order -- computes the softmax over the
+//     k selected logits (max-subtracted, expf) and counts the assignments
+//     per expert;
 //   * the last token block turns the per-block counts into per-expert
 //     exclusive prefixes, scans the totals into expert offsets and writes the
 //     GEMM token-tile list.
@@ -73,22 +74,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Order-preserving unsigned key of a float (-0 is folded into +0 first, so
-// equal values get equal keys).
-__device__ __forceinline__ uint32_t order_key(float f) {
-    const uint32_t u = __float_as_uint(f + 0.0f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
-    return __reduce_max_sync(0xffffffffu, v);
-}
-__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
-    return __reduce_min_sync(0xffffffffu, v);
-}
-
 // Byte offset of the 16-byte chunk `c` (0..7) of row `r` in a tile written
 // by TMA with the 128-byte swizzle (rows of 128 B, 1024-byte aligned tile).
 __device__ __forceinline__ uint32_t swz(int r, int c) {
@@ -127,6 +112,95 @@ __device__ __forceinline__ void warp_exclusive_scan256(const int* vals, int* out
     }
     const int all = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) out[n] = all;
+}
+
+// Inserts (v, e) into a top-K list sorted by value, descending.  Candidates
+// arrive in increasing expert order, and an equal value never displaces an
+// entry (strict >), so equal logits keep the lower expert index first.
+template <int K>
+__device__ __forceinline__ void topk_insert(float (&bv)[K], int (&be)[K], float v, int e) {
+#pragma unroll
+    for (int s = K - 1; s > 0; --s) {
+        if (v > bv[s - 1]) {
+            bv[s] = bv[s - 1];
+            be[s] = be[s - 1];
+        } else if (v > bv[s]) {
+            bv[s] = v;
+            be[s] = e;
+        }
+    }
+    if (v > bv[0]) {
+        bv[0] = v;
+        be[0] = e;
+    }
+}
+
+// Top-K selection and softmax for the token block, one lane per token.
+// Compute warp w scans experts [wE/4, (w+1)E/4) of all 32 tokens (logit +
+// bias; NaN counts as the lowest value) into a per-lane list; warp 0 then
+// merges the four lists in warp order -- lower expert ranges first, each list
+// in rank order -- so ties still resolve to the lower expert index.  The
+// softmax runs over the K selected logits, max-subtracted, summed in rank
+// order.  cand: [kComputeWarps][32][K] values then indices (scratch smem).
+template <int K>
+__device__ void topk_block(const RouterParams& p, const float* logits, int ls, const float* bias_s,
+                           float* cand, int t0, int* hist) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+    float* cv = cand;
+    int* ce = reinterpret_cast<int*>(cand + kComputeWarps * kRouterTokens * K);
+    if (warp < kComputeWarps) {
+        float bv[K];
+        int be[K];
+#pragma unroll
+        for (int s = 0; s < K; ++s) {
+            bv[s] = -INFINITY;
+            be[s] = INT_MAX;
+        }
+        const int e_lo = E * warp / kComputeWarps, e_hi = E * (warp + 1) / kComputeWarps;
+        const float* row = logits + lane * ls;
+        for (int e = e_lo; e < e_hi; ++e) {
+            float v = row[e] + bias_s[e];
+            if (!(v == v)) v = -FLT_MAX;
+            topk_insert<K>(bv, be, v, e);
+        }
+#pragma unroll
+        for (int s = 0; s < K; ++s) {
+            cv[(warp * kRouterTokens + lane) * K + s] = bv[s];
+            ce[(warp * kRouterTokens + lane) * K + s] = be[s];
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float bv[K];
+    int be[K];
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+        bv[s] = -INFINITY;
+        be[s] = INT_MAX;
+    }
+    for (int w = 0; w < kComputeWarps; ++w) {
+#pragma unroll
+        for (int s = 0; s < K; ++s) {
+            const int e = ce[(w * kRouterTokens + lane) * K + s];
+            if (e != INT_MAX) topk_insert<K>(bv, be, cv[(w * kRouterTokens + lane) * K + s], e);
+        }
+    }
+    const int t = t0 + lane;
+    if (t >= p.T) return;
+    float ex[K];
+    float denom = 0.f;
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+        ex[s] = expf(bv[s] - bv[0]);
+        denom += ex[s];
+    }
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+        p.topk_ids[static_cast<size_t>(t) * K + s] = be[s];
+        p.topk_w[static_cast<size_t>(t) * K + s] = ex[s] / denom;
+        atomicAdd(&hist[be[s]], 1);
+    }
 }
 
 // Last CTA of the grid: per-expert exclusive prefix over token blocks, expert
@@ -443,71 +517,16 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
 
-    // Top-k + softmax, one warp per token: lane l holds experts l, l+32, ...
-    // A selection round takes the largest order key (redux.sync max) and,
-    // among the experts holding it, the lowest index (redux.sync min), so
-    // equal logits go to the lower expert index.  NaN is the lowest value.
-    const int k = p.top_k;
-    const int nkeys = (E + 31) / 32;
-    for (int r = warp; r < kRouterTokens; r += kThreads / 32) {
-        const int t = t0 + r;
-        if (t >= p.T) break;   // warp-uniform; no block barrier inside
-        uint32_t key[kMaxExperts / 32];
-        uint32_t taken = 0;
-#pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
-            const int e = lane + 32 * i;
-            key[i] = 0u;   // below every real logit
-            if (i < nkeys && e < E) {
-                float v = logits[r * ls + e] + bias_s[e];
-                if (!(v == v)) v = -FLT_MAX;
-                key[i] = order_key(v);
-            } else {
-                taken |= 1u << i;
-            }
-        }
-        int sel_e[kMaxTopK];
-        float sel_v[kMaxTopK];
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            sel_e[j] = 0;
-            sel_v[j] = 0.f;
-            if (j < k) {
-                uint32_t best = 0u;
-                int best_e = 0x7fffffff;
-#pragma unroll
-                for (int i = 0; i < kMaxExperts / 32; ++i)
-                    if (!(taken & (1u << i)) && (key[i] > best || best_e == 0x7fffffff)) {
-                        best = key[i];
-                        best_e = lane + 32 * i;
-                    }
-                const uint32_t m = warp_max_u32(best_e == 0x7fffffff ? 0u : best);
-                const uint32_t cand =
-                    (best_e != 0x7fffffff && best == m) ? static_cast<uint32_t>(best_e) : 0xffffffffu;
-                const int e_sel = static_cast<int>(warp_min_u32(cand));
-                if ((e_sel & 31) == lane) taken |= 1u << (e_sel >> 5);
-                sel_e[j] = e_sel;
-                sel_v[j] = key_value(m);   // the selected logit itself
-            }
-        }
-        // softmax over the k selected logits, summed in slot order
-        float denom = 0.f, mine = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            if (j < k) {
-                const float ex = expf(sel_v[j] - sel_v[0]);
-                denom += ex;
-                if (lane == j) mine = ex;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            if (j < k && lane == j) {
-                p.topk_ids[static_cast<size_t>(t) * k + j] = sel_e[j];
-                p.topk_w[static_cast<size_t>(t) * k + j] = mine / denom;
-                atomicAdd(&hist[sel_e[j]], 1);
-            }
-        }
+    // Top-k + softmax, one lane per token (the partial buffer is free now).
+    switch (p.top_k) {
+        case 1: topk_block<1>(p, logits, ls, bias_s, partial, t0, hist); break;
+        case 2: topk_block<2>(p, logits, ls, bias_s, partial, t0, hist); break;
+        case 3: topk_block<3>(p, logits, ls, bias_s, partial, t0, hist); break;
+        case 4: topk_block<4>(p, logits, ls, bias_s, partial, t0, hist); break;
+        case 5: topk_block<5>(p, logits, ls, bias_s, partial, t0, hist); break;
+        case 6: topk_block<6>(p, logits, ls, bias_s, partial, t0, hist); break;
+        case 7: topk_block<7>(p, logits, ls, bias_s, partial, t0, hist); break;
+        default: topk_block<8>(p, logits, ls, bias_s, partial, t0, hist); break;
     }
     __syncthreads();
     for (int e = tid; e < E; e += kThreads)
