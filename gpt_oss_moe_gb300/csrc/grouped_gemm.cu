@@ -95,7 +95,8 @@ struct SmemPlan {
     uint64_t* sempty;    // [2] scales consumed (MXFP4)
     uint64_t* drain;     // [2] one per MMA issuer
     uint32_t* tmem_base;
-    int* flags;          // [0] abort, [1..2] epilogue broadcast (alternating)
+    int* flags;          // [0] abort, [1..2] epilogue broadcast (alternating),
+                         // [3] K-split: this epilogue holds the last part
 };
 
 // bf16: one ring of `stages` slots, each a W tile + a token tile.
@@ -144,6 +145,24 @@ __device__ __forceinline__ void raise_abort(volatile int* flags, int32_t* status
 __device__ __forceinline__ bool tile_ok(const int4& t, const GemmParams& p) {
     return t.x >= 0 && t.x < p.num_experts && t.z >= 1 && t.z <= p.token_box && t.y >= 0 &&
            t.y + t.z <= p.rows_total;
+}
+
+// Work unit u of a call: K-split part `split` of (token tile, 128-row weight
+// block) pair `pair` = tile * n_wblocks + mb; it covers ring slots
+// [st_lo, st_hi) of the n_st slots of the weights' K range.
+struct Unit {
+    int pair, tile, mb, split, st_lo, st_hi;
+};
+__device__ __forceinline__ Unit unit_of(int u, const GemmParams& p, int n_st) {
+    Unit x;
+    x.split = u % p.ksplit;
+    x.pair = u / p.ksplit;
+    x.tile = x.pair / p.n_wblocks;
+    x.mb = x.pair % p.n_wblocks;
+    const int per = (n_st + p.ksplit - 1) / p.ksplit;
+    x.st_lo = x.split * per;
+    x.st_hi = min(n_st, x.st_lo + per);
+    return x;
 }
 
 __device__ __forceinline__ float clamped_glu(float gate, float up) {
@@ -233,6 +252,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     // ring sizes the converter teams rely on and the TMEM plan (uniform
     // exit, nothing started)
     if (stages < 2 || stages > kMaxStages || n_iss < 1 || n_iss > (WF == 1 ? 2 : 1) ||
+        p.ksplit < 1 || p.ksplit > kMaxKSplit ||
+        (EPI == kEpiGlu && p.ksplit > 1 && (p.partial == nullptr || p.tickets == nullptr)) ||
         (WF == 1 && (astages < 2 || astages > kMxfp4AStages || 2 * stages < astages + 2 ||
                      a_col0 + kASlotCols * static_cast<uint32_t>(astages) >
                          static_cast<uint32_t>(p.tmem_cols)))) {
@@ -269,6 +290,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         flags[0] = 0;
         flags[1] = 0;
         flags[2] = 0;
+        flags[3] = 0;
         mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
@@ -287,7 +309,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     pdl_wait();                 // tiles, activations and outputs of earlier kernels
     pdl_launch_dependents();
 
-    const int num_units = p.num_tiles[0] * p.n_wblocks;
+    const int num_units = p.num_tiles[0] * p.n_wblocks * p.ksplit;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -301,9 +323,10 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             int local = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-                const int4 t = p.tiles[u / p.n_wblocks];
+                const Unit un = unit_of(u, p, n_st);
+                const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
-                const int mb = u % p.n_wblocks;
+                const int mb = un.mb;
                 if (WF == 1) {
                     // this unit's scale rows, one bulk copy, double-buffered
                     const int sb = local & 1;
@@ -323,7 +346,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                               bytes, sf);
                 }
                 ++local;
-                for (int st = 0; st < n_st; ++st) {
+                for (int st = un.st_lo; st < un.st_hi; ++st) {
                     if (!mbar_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
                         raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                         ok = false;
@@ -382,7 +405,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             int local = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-                const int4 t = p.tiles[u / p.n_wblocks];
+                const Unit un = unit_of(u, p, n_st);
+                const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
                 const uint32_t n_mma = static_cast<uint32_t>((t.z + 15) & ~15);
                 const uint32_t idesc = idesc_bf16_f32(kWeightTileRows, n_mma);
@@ -396,7 +420,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * acc_stride;
-                for (int st = 0; st < n_st && ok; ++st) {
+                for (int st = un.st_lo; st < un.st_hi && ok; ++st) {
                     const int nk = min(KPS, p.k_blocks - st * KPS);
                     // bf16: the slot's tiles have landed.  MXFP4: its A slot
                     // is converted (which implies the codes and token chunks
@@ -414,7 +438,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                         smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
                     const uint32_t a_tm = tmem_base + a_col0 + kASlotCols * static_cast<uint32_t>(astage);
                     for (int jj = 0; jj < nk; ++jj) {
-                        const int kb = st * KPS + jj;
+                        const int kb = (st - un.st_lo) * KPS + jj;   // from the part's start
                         const uint32_t b_addr = b_stage + static_cast<uint32_t>(jj) * b_bytes;
                         if (WF == 1) {
 #pragma unroll
@@ -466,7 +490,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-                const int4 t = p.tiles[u / p.n_wblocks];
+                const Unit un = unit_of(u, p, n_st);
+                const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
                 const uint32_t n_mma = static_cast<uint32_t>((t.z + 15) & ~15);
                 const uint32_t idesc = idesc_bf16_f32(kWeightTileRows, n_mma);
@@ -481,8 +506,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 tc_fence_after();
                 const uint32_t d_tmem =
                     tmem_base + static_cast<uint32_t>(2 * is + buf) * acc_stride;
-                for (int st = is; st < n_st && ok; st += n_iss) {
-                    for (const int use = sbase + st; cur < use; ++cur) {
+                for (int st = un.st_lo + is; st < un.st_hi && ok; st += n_iss) {
+                    for (const int use = sbase + (st - un.st_lo); cur < use; ++cur) {
                         if (++stage == stages) {
                             stage = 0;
                             phase ^= 1u;
@@ -510,7 +535,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     const uint32_t a_tm = tmem_base + a_col0 + kASlotCols * static_cast<uint32_t>(astage);
                     for (int jj = 0; jj < nk; ++jj) {
                         // the issuer's first MMA of the unit starts its sum
-                        const bool first = st == is && jj == 0;
+                        const bool first = st == un.st_lo + is && jj == 0;
                         const uint32_t b_addr = b_stage + static_cast<uint32_t>(jj) * b_bytes;
                         if (WF == 1) {
 #pragma unroll
@@ -534,7 +559,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     tc_commit(smem_u32(sm.empty + stage));
                 }
                 if (!ok) break;
-                sbase += n_st;
+                sbase += un.st_hi - un.st_lo;
                 tc_commit(smem_u32(sm.tfull + buf));
             }
             // Every MMA this issuer issued has finished once this arrives.
@@ -548,12 +573,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         const int row_in_tile = quad * 32 + lane;
         int local = 0;
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-            const int4 t = p.tiles[u / p.n_wblocks];
+            const Unit un = unit_of(u, p, n_st);
+            const int4 t = p.tiles[un.tile];
             if (!tile_ok(t, p)) {
                 if (ep == 0) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
                 continue;
             }
-            const int mb = u % p.n_wblocks;
+            const int mb = un.mb;
             const int buf = local & 1;
             const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
             ++local;
@@ -580,14 +606,17 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
 
             const int wrow = mb * kWeightTileRows + row_in_tile;
             const bool row_ok = wrow < p.w_rows;
+            // the bias enters once: down adds it with part 0, gate_up after the sum
             const float bias =
-                row_ok ? __bfloat162float(p.bias[static_cast<size_t>(t.x) * p.w_rows + wrow]) : 0.f;
+                row_ok && (EPI == kEpiGlu || un.split == 0)
+                    ? __bfloat162float(p.bias[static_cast<size_t>(t.x) * p.w_rows + wrow])
+                    : 0.f;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                    static_cast<uint32_t>(buf) * acc_stride;
             const int n_mma = (t.z + 15) & ~15;
-            const int n_acc = min(n_iss, n_st);   // issuers that had ring slots
-            for (int c0 = 0; c0 < n_mma; c0 += 16) {
-                float v[16];
+            const int n_acc = min(n_iss, un.st_hi - un.st_lo);   // issuers that had ring slots
+            // This part's accumulator, 16 token columns from c0 (both issuers added).
+            auto load_acc = [&](int c0, float (&v)[16]) {
                 tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
                 if (n_acc > 1) {
                     float v2[16];
@@ -595,33 +624,91 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] += v2[i];
                 }
+            };
+            // bias + clamped GLU of 16 token columns, bf16 store of h
+            auto glu_store = [&](int c0, float (&v)[16]) {
+                // even lane: gate row 2j, odd lane: up row 2j+1 (same j)
+                const bool odd = lane & 1;
+                const int hcols = p.w_rows >> 1;
+                // MXFP4: h is the down projection's token operand in its
+                // layout -- chunk-major [I/64][T*k][64], each group of 8
+                // columns in the order 0,4,1,5,2,6,3,7
+                const int hcol = WF == 1 ? kperm8_pos(wrow >> 1) : (wrow >> 1);
+                __nv_bfloat16* hrow0 =
+                    WF == 1 ? p.h + (static_cast<size_t>(hcol >> 6) * p.rows_total + t.y) * 64 +
+                                  (hcol & 63)
+                            : p.h + static_cast<size_t>(t.y) * hcols + hcol;
+                const size_t hstride = WF == 1 ? 64 : static_cast<size_t>(hcols);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] += bias;
-                if (EPI == kEpiGlu) {
-                    // even lane: gate row 2j, odd lane: up row 2j+1 (same j)
-                    const bool odd = lane & 1;
-                    const int hcols = p.w_rows >> 1;
-                    // MXFP4: h is the down projection's token operand in its
-                    // layout -- chunk-major [I/64][T*k][64], each group of 8
-                    // columns in the order 0,4,1,5,2,6,3,7
-                    const int hcol = WF == 1 ? kperm8_pos(wrow >> 1) : (wrow >> 1);
-                    __nv_bfloat16* hrow0 =
-                        WF == 1 ? p.h + (static_cast<size_t>(hcol >> 6) * p.rows_total + t.y) * 64 +
-                                      (hcol & 63)
-                                : p.h + static_cast<size_t>(t.y) * hcols + hcol;
-                    const size_t hstride = WF == 1 ? 64 : static_cast<size_t>(hcols);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float send = odd ? v[i] : v[8 + i];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                        const float gate = odd ? recv : v[i];
-                        const float up = odd ? v[8 + i] : recv;
-                        const int c = c0 + i + (odd ? 8 : 0);
-                        if (c < t.z)
-                            hrow0[static_cast<size_t>(c) * hstride] =
-                                __float2bfloat16_rn(clamped_glu(gate, up));
+                for (int i = 0; i < 8; ++i) {
+                    const float send = odd ? v[i] : v[8 + i];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                    const float gate = odd ? recv : v[i];
+                    const float up = odd ? v[8 + i] : recv;
+                    const int c = c0 + i + (odd ? 8 : 0);
+                    if (c < t.z)
+                        hrow0[static_cast<size_t>(c) * hstride] =
+                            __float2bfloat16_rn(clamped_glu(gate, up));
+                }
+            };
+
+            if (EPI == kEpiGlu && p.ksplit > 1) {
+                // K split: store this part's fp32 tile [col][row], release the
+                // accumulator, take a ticket; the last part adds all parts in
+                // part order (the same sum whichever part arrives last).
+                // part q of this unit: rows t.y.. of block mb in part q's plane
+                const size_t part_floats =
+                    static_cast<size_t>(p.n_wblocks) * p.rows_total * kWeightTileRows;
+                const size_t unit_off =
+                    (static_cast<size_t>(mb) * p.rows_total + t.y) * kWeightTileRows + row_in_tile;
+                float* mine = p.partial + un.split * part_floats + unit_off;
+                for (int c0 = 0; c0 < n_mma; c0 += 16) {
+                    float v[16];
+                    load_acc(c0, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (c0 + i < t.z) mine[static_cast<size_t>(c0 + i) * kWeightTileRows] = v[i];
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(sm.tempty + buf));
+                __threadfence();
+                named_bar_sync(1, kEpiThreads);
+                if (ep == 0) {
+                    const int ticket = atomicAdd(p.tickets + un.pair, 1);
+                    const int last = ticket == p.ksplit - 1;
+                    if (last) p.tickets[un.pair] = 0;   // zero for the next call
+                    flags[3] = last;
+                }
+                named_bar_sync(1, kEpiThreads);
+                if (!flags[3]) continue;
+                __threadfence();
+                const float* parts = p.partial + unit_off;
+                for (int c0 = 0; c0 < n_mma; c0 += 16) {
+                    float v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                    for (int q = 0; q < p.ksplit; ++q) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < t.z)
+                                v[i] += __ldcg(parts + q * part_floats +
+                                               static_cast<size_t>(c0 + i) * kWeightTileRows);
                     }
+                    glu_store(c0, v);
+                }
+                continue;
+            }
+
+            for (int c0 = 0; c0 < n_mma; c0 += 16) {
+                float v[16];
+                load_acc(c0, v);
+                if (EPI == kEpiGlu) {
+                    glu_store(c0, v);
                 } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += bias;
                     if (row_ok) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -664,7 +751,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         int local = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-            const int4 t = p.tiles[u / p.n_wblocks];
+            const Unit un = unit_of(u, p, n_st);
+            const int4 t = p.tiles[un.tile];
             if (!tile_ok(t, p)) continue;
             const int sb = local & 1;
             const uint32_t sph = static_cast<uint32_t>(local >> 1) & 1u;
@@ -676,9 +764,11 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             const uint8_t* srow = sm.scales + sb * scale_buf_bytes + r * p.kscale;
             // rows past the matrix: codes are TMA zero-fill and no scale bytes
             // were copied for them; use scale 1 so they stay exactly zero
-            const bool row_ok = (u % p.n_wblocks) * kWeightTileRows + r < p.w_rows;
-            for (int st = (team ^ sbase) & 1; st < n_st; st += 2) {
-                const int use = sbase + st;
+            const bool row_ok = un.mb * kWeightTileRows + r < p.w_rows;
+            const int nsl = un.st_hi - un.st_lo;      // ring slots of this unit
+            for (int i = (team ^ sbase) & 1; i < nsl; i += 2) {
+                const int st = un.st_lo + i;
+                const int use = sbase + i;
                 const int stage = use % stages;
                 const uint32_t phase = static_cast<uint32_t>(use / stages) & 1u;
                 const int aslot = use % astages;
@@ -727,7 +817,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 if (lane == 0) mbar_arrive(smem_u32(sm.afull + aslot));
             }
             if (!ok) break;
-            sbase += n_st;
+            sbase += nsl;
             mbar_arrive(smem_u32(sm.sempty + sb));
         }
     }

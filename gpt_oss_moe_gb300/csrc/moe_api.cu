@@ -99,6 +99,7 @@ moe_status weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K, bo
 // ------------------------------------------------------------ tuning
 
 std::atomic<int> g_token_tile{0};
+std::atomic<int> g_ksplit_off{0};   // 1: never split the GEMMs' K range
 std::atomic<int> g_pdl{1};
 
 // ------------------------------------------------------------ profiling
@@ -467,8 +468,15 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.h = h;
     g.scales = static_cast<const uint8_t*>(gate_up.scale);
     g.kscale = s.H / 32;
-    int grid = L.max_tiles * g.n_wblocks;
-    if (grid > dev.sms) grid = dev.sms;
+    // K split when the units cannot fill two waves (small batches)
+    const int kb_per_slot = mxfp4 ? kMxfp4KbPerStage : 1;
+    const long long tiles_max = max_token_tiles(R, L.max_tiles);
+    const bool split_ok = g_ksplit_off.load() == 0;
+    g.ksplit = split_ok ? gemm_ksplit(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot) : 1;
+    g.partial = reinterpret_cast<float*>(ws + L.gemm_partial);
+    g.tickets = reinterpret_cast<int32_t*>(ws + L.counters) + kSplitTicketOffset;
+    long long units = tiles_max * g.n_wblocks * g.ksplit;
+    int grid = static_cast<int>(units < dev.sms ? units : dev.sms);
     MOE_CUDA(launch_gemm(kEpiGlu, wf, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
     prof_mark("gate_up_glu", stream);
 
@@ -484,8 +492,12 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.top_k = s.top_k;
     g.scales = static_cast<const uint8_t*>(down.scale);
     g.kscale = s.I / 32;
-    grid = L.max_tiles * g.n_wblocks;
-    if (grid > dev.sms) grid = dev.sms;
+    // the down projection adds its K parts through the output's atomics
+    g.ksplit = split_ok ? gemm_ksplit(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot) : 1;
+    g.partial = nullptr;
+    g.tickets = nullptr;
+    units = tiles_max * g.n_wblocks * g.ksplit;
+    grid = static_cast<int>(units < dev.sms ? units : dev.sms);
     MOE_CUDA(launch_gemm(kEpiCombine, wf, g, &tm_wd, &tm_h, grid, smem, stream, pdl));
     prof_mark("down_combine", stream);
 
@@ -519,6 +531,11 @@ moe_status moe_set_tuning(const char* key, int value) {
     if (std::strcmp(key, "token_tile") == 0) {
         if (value != 0 && (value < 16 || value > kMaxTokenTile || value % 16)) return MOE_ERR_ARG;
         g_token_tile.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "ksplit") == 0) {
+        if (value != 0 && value != 1) return MOE_ERR_ARG;
+        g_ksplit_off.store(value);
         return MOE_OK;
     }
     if (std::strcmp(key, "pdl") == 0) {

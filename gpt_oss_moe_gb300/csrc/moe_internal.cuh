@@ -32,7 +32,36 @@ constexpr int kGridCounterWord = 2;
 // still finds them at zero (every call leaves them at zero).
 constexpr int kPairSlots = 304;
 constexpr int kMaxTokenBlocks = (1 << 20) / 32;
-constexpr size_t kCounterBytes = static_cast<size_t>(kPairSlots + kMaxTokenBlocks) * 4;
+
+// GEMM K split for small batches.  When the work units (token tiles x
+// 128-row weight blocks) cannot fill two waves of GB300's 152 SMs, each
+// unit's ring slots are cut into up to kMaxKSplit contiguous parts handled
+// by different CTAs (each part at least 2 slots, none empty).  The down
+// projection adds the parts through its fp32 atomics; gate_up parts store
+// fp32 partial tiles and the last part to arrive (a ticket per unit) adds
+// them in part order before the bias and the GLU.  The split depends on the
+// shape only, and at most kSplitTargetUnits tickets exist, so they too live
+// in the fixed counter region.
+constexpr int kSplitTargetUnits = 304;
+constexpr int kMaxKSplit = 8;
+inline int gemm_ksplit(long long max_units, int n_slots) {
+    if (max_units <= 0 || max_units >= kSplitTargetUnits || n_slots < 4) return 1;
+    long long ks = (kSplitTargetUnits + max_units - 1) / max_units;
+    if (ks > kMaxKSplit) ks = kMaxKSplit;
+    if (ks > n_slots / 2) ks = n_slots / 2;
+    if (ks < 2) return 1;
+    const int per = (n_slots + static_cast<int>(ks) - 1) / static_cast<int>(ks);
+    return (n_slots + per - 1) / per;
+}
+// Upper bound of the token tiles of a call (every tile holds >= 1 row).
+inline long long max_token_tiles(long long R, int max_tiles) {
+    return R < max_tiles ? R : max_tiles;
+}
+
+constexpr size_t kCounterBytes =
+    static_cast<size_t>(kPairSlots + kMaxTokenBlocks + kSplitTargetUnits) * 4;
+// GEMM split tickets: counters + kSplitTicketOffset (ints)
+constexpr int kSplitTicketOffset = kPairSlots + kMaxTokenBlocks;
 
 // K slices of the router: the hidden dimension is cut into `ksplit` slices
 // handled by separate CTAs when there are few (token block, expert group)
@@ -49,7 +78,7 @@ inline int router_ksplit(int pairs, int nchunks) {
 }
 
 struct WsLayout {
-    size_t status, topk_ids, topk_w, blk_cnt, logits, partials, counters, offsets;
+    size_t status, topk_ids, topk_w, blk_cnt, logits, partials, counters, offsets, gemm_partial;
     size_t sorted_assign, assign_row, tiles, x_perm, h, out_acc, total;
     int max_tiles;
 };
@@ -83,6 +112,17 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
     L.x_perm = take(R * H * 2);
     L.h = take(R * I * 2);
     L.out_acc = take(static_cast<size_t>(T) * H * 4);
+    // gate_up K-split partial tiles, fp32 [part][weight block][routed row][128],
+    // sized for the larger split of the bf16 (H/64 slots) and MXFP4 (H/256
+    // slots) rings
+    {
+        const int nwb = (2 * I + kWeightTileRows - 1) / kWeightTileRows;
+        const long long units = max_token_tiles(static_cast<long long>(R), L.max_tiles) * nwb;
+        const int ks_bf16 = gemm_ksplit(units, H / kBlockK);
+        const int ks_mx = gemm_ksplit(units, (H / kBlockK + 3) / 4);
+        const int ks = ks_bf16 > ks_mx ? ks_bf16 : ks_mx;
+        L.gemm_partial = take(ks > 1 ? static_cast<size_t>(ks) * nwb * R * kWeightTileRows * 4 : 0);
+    }
     L.total = o;
     return L;
 }
@@ -157,6 +197,12 @@ struct GemmParams {
     const float* topk_w;
     int top_k;
     int32_t* status;
+    // K split (small batches): parts per unit; gate_up partial tiles
+    // [part][weight block][routed row][128] fp32 and per-unit tickets
+    // (ksplit > 1 only)
+    int ksplit;
+    float* partial;
+    int32_t* tickets;
 };
 
 // Shared memory of one GEMM pipeline stage and of the fixed part (bytes,

@@ -180,7 +180,10 @@ moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
  *                 multiple of 16 in [16, 256] (MXFP4 layers use at most
  *                 128);
  *   "pdl":        1 = launch dependent kernels with programmatic dependent
- *                 launch (default), 0 = plain stream order.
+ *                 launch (default), 0 = plain stream order;
+ *   "ksplit":     0 = split the GEMMs' K range when a small batch leaves
+ *                 SMs idle (default), 1 = never split (every output then
+ *                 sums its K range in one fixed order).
  * Returns MOE_ERR_ARG for an unknown key or value. */
 moe_status moe_set_tuning(const char* key, int value);
 

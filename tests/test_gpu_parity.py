@@ -238,6 +238,50 @@ def test_forward_120b_shape(moe, oracle_lib, layer_120b, T):
     _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample)
 
 
+# ---------------------------------------------------------------- K split
+
+# Few routed rows and a long K range: the units (token tiles x 128-row weight
+# blocks) cannot fill two waves of the GPU, so the GEMMs split each unit's K
+# range into parts (down: added by the output atomics; gate_up: partial tiles
+# summed by the last part before the GLU).  R = T*k rows; parts per unit:
+KSPLIT_CASES = [
+    # E, k, H, I, T, wfmt      gate_up parts x slots / down parts
+    (4, 2, 512, 256, 3, "bf16"),     # 4 x 2 of 8 k-blocks / 2 x 2 of 4
+    (8, 4, 320, 192, 1, "bf16"),     # 2 parts of 3 + 2 k-blocks (uneven); W_d tail
+    (4, 1, 1024, 512, 2, "bf16"),    # 8 x 2 of 16 / 4 x 2 of 8
+    (4, 2, 1024, 512, 3, "mxfp4"),   # 2 parts of 2 ring slots (4 k-blocks each)
+    (8, 4, 2048, 384, 1, "mxfp4"),   # 4 parts of 2 ring slots / down unsplit (2 slots)
+]
+
+
+@pytest.mark.parametrize("case", KSPLIT_CASES, ids=lambda c: "E{}k{}H{}I{}T{}{}".format(*c))
+def test_forward_ksplit(moe, oracle_lib, synth_lib, case):
+    from parity_util import TOL_MXFP4
+    E, k, H, I, T, wfmt = case
+    L = synth_lib.make_layer(E=E, T=T, H=H, I=I, top_k=k, seed=700 + T + H, wfmt=wfmt,
+                             router_w_std=0.05)
+    tol = TOL_MXFP4 if wfmt == "mxfp4" else TOL_BF16
+    _check(moe, oracle_lib, L, tol=tol)
+
+
+def test_ksplit_tickets_reset(moe, oracle_lib, synth_lib):
+    """The gate_up part tickets are left at zero: the same workspace serves a
+    second split call, and a call of another shape, with the same results."""
+    L = synth_lib.make_layer(E=4, T=3, H=512, I=256, top_k=2, seed=7, router_w_std=0.05)
+    L2 = synth_lib.make_layer(E=8, T=1, H=320, I=192, top_k=4, seed=8, router_w_std=0.05)
+    shape = moe.layer_shape(L)
+    shape2 = moe.layer_shape(L2)
+    ws = moe.alloc_workspace(shape) if moe.moe_workspace_bytes(shape) >= moe.moe_workspace_bytes(shape2) \
+        else moe.alloc_workspace(shape2)
+    i1, w1, o1, _ = gpu_forward(moe, L, workspace=ws)
+    i2, w2, o2, _ = gpu_forward(moe, L2, workspace=ws)
+    i3, w3, o3, _ = gpu_forward(moe, L, workspace=ws)
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.equal(i1, i3) and torch.equal(w1, w3)
+    assert torch.allclose(o1, o3, rtol=0, atol=1e-6 * float(o1.abs().max()))
+    _check(moe, oracle_lib, L2)
+
+
 # ---------------------------------------------------------------- MXFP4
 
 MXFP4_CASES = [
@@ -274,8 +318,14 @@ def test_mxfp4_dequant_is_exact(moe, oracle_lib, synth_lib, T):
         Lq, wfmt="bf16", s_gu=None, s_d=None,
         w_gu=oracle_lib.dequant_mxfp4(Lq.w_gu, Lq.s_gu).to(torch.bfloat16).contiguous(),
         w_d=oracle_lib.dequant_mxfp4(Lq.w_d, Lq.s_d).to(torch.bfloat16).contiguous())
-    iq, wq, oq, wsq = gpu_forward(moe, Lq)
-    ib, wb, ob, wsb = gpu_forward(moe, Lb)
+    # one K order in both paths: no K split (it would differ between the
+    # 4-k-block MXFP4 ring and the 1-k-block bf16 ring)
+    moe.moe_set_tuning("ksplit", 1)
+    try:
+        iq, wq, oq, wsq = gpu_forward(moe, Lq)
+        ib, wb, ob, wsb = gpu_forward(moe, Lb)
+    finally:
+        moe.moe_set_tuning("ksplit", 0)
     assert moe.moe_get_device_status(wsq) == 0
     assert torch.equal(iq, ib) and torch.equal(wq, wb)
     assert torch.equal(oq, ob)
