@@ -99,7 +99,7 @@ moe_status weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K, bo
 // ------------------------------------------------------------ tuning
 
 std::atomic<int> g_token_tile{0};
-std::atomic<int> g_ksplit_off{0};   // 1: never split the GEMMs' K range
+std::atomic<int> g_ksplit_mode{0};  // 0: automatic, 1: never split, n >= 2: n parts
 std::atomic<int> g_pdl{1};
 
 // ------------------------------------------------------------ profiling
@@ -471,8 +471,36 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     // K split when the units cannot fill two waves (small batches)
     const int kb_per_slot = mxfp4 ? kMxfp4KbPerStage : 1;
     const long long tiles_max = max_token_tiles(R, L.max_tiles);
-    const bool split_ok = g_ksplit_off.load() == 0;
-    g.ksplit = split_ok ? gemm_ksplit(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot) : 1;
+    const int split_mode = g_ksplit_mode.load();
+    // parts for `slots` ring slots: the model's choice (at most auto_max), or
+    // the forced count (no empty part, at least 2 slots each)
+    const auto parts_of = [](int want, int slots) {
+        if (want > slots / 2) want = slots / 2;
+        if (want < 2) return 1;
+        const int per = (slots + want - 1) / want;
+        return (slots + per - 1) / per;
+    };
+    const auto parts_for = [&](long long units, int slots, int auto_max) {
+        if (split_mode == 1) return 1;
+        if (split_mode >= 2) return parts_of(split_mode, slots);
+        const int m = gemm_ksplit(units, slots, dev.sms);
+        return m > auto_max ? parts_of(auto_max, slots) : m;
+    };
+    // gate_up: at most 2 parts -- each part's epilogue stores, fences and
+    // tickets its partial tile and the last one reloads all of them; at
+    // 20b T=1 (180 units) 2 parts gave 33 us, 3 gave 39, 5 gave 46 (1: 37)
+    g.ksplit = parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, 2);
+    {
+        // no more parts than the partial-tile region holds at R rows
+        const size_t part_bytes = static_cast<size_t>(g.n_wblocks) * R * kWeightTileRows * 4;
+        const size_t cap = part_bytes ? L.gemm_partial_bytes / part_bytes : 0;
+        if (static_cast<size_t>(g.ksplit) > cap) {
+            const int slots = (g.k_blocks + kb_per_slot - 1) / kb_per_slot;
+            const int want = cap < 2 ? 1 : static_cast<int>(cap);
+            const int per = (slots + want - 1) / want;
+            g.ksplit = want < 2 ? 1 : (slots + per - 1) / per;
+        }
+    }
     g.partial = reinterpret_cast<float*>(ws + L.gemm_partial);
     g.tickets = reinterpret_cast<int32_t*>(ws + L.counters) + kSplitTicketOffset;
     long long units = tiles_max * g.n_wblocks * g.ksplit;
@@ -493,7 +521,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.scales = static_cast<const uint8_t*>(down.scale);
     g.kscale = s.I / 32;
     // the down projection adds its K parts through the output's atomics
-    g.ksplit = split_ok ? gemm_ksplit(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot) : 1;
+    g.ksplit = parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, kMaxKSplit);
     g.partial = nullptr;
     g.tickets = nullptr;
     units = tiles_max * g.n_wblocks * g.ksplit;
@@ -534,8 +562,8 @@ moe_status moe_set_tuning(const char* key, int value) {
         return MOE_OK;
     }
     if (std::strcmp(key, "ksplit") == 0) {
-        if (value != 0 && value != 1) return MOE_ERR_ARG;
-        g_ksplit_off.store(value);
+        if (value < 0 || value > kMaxKSplit) return MOE_ERR_ARG;
+        g_ksplit_mode.store(value);
         return MOE_OK;
     }
     if (std::strcmp(key, "pdl") == 0) {

@@ -36,7 +36,9 @@ constexpr int kMaxTokenBlocks = (1 << 20) / 32;
 // GEMM K split for small batches.  When the work units (token tiles x
 // 128-row weight blocks) cannot fill two waves of GB300's 152 SMs, each
 // unit's ring slots are cut into up to kMaxKSplit contiguous parts handled
-// by different CTAs (each part at least 2 slots, none empty).  The down
+// by different CTAs (each part at least 2 slots, none empty); the part count
+// minimises the persistent grid's makespan, ceil(units * parts / SMs) waves
+// of ceil(slots / parts) slots.  The down
 // projection adds the parts through its fp32 atomics; gate_up parts store
 // fp32 partial tiles and the last part to arrive (a ticket per unit) adds
 // them in part order before the bias and the GLU.  The split depends on the
@@ -44,14 +46,24 @@ constexpr int kMaxTokenBlocks = (1 << 20) / 32;
 // in the fixed counter region.
 constexpr int kSplitTargetUnits = 304;
 constexpr int kMaxKSplit = 8;
-inline int gemm_ksplit(long long max_units, int n_slots) {
-    if (max_units <= 0 || max_units >= kSplitTargetUnits || n_slots < 4) return 1;
-    long long ks = (kSplitTargetUnits + max_units - 1) / max_units;
-    if (ks > kMaxKSplit) ks = kMaxKSplit;
-    if (ks > n_slots / 2) ks = n_slots / 2;
-    if (ks < 2) return 1;
-    const int per = (n_slots + static_cast<int>(ks) - 1) / static_cast<int>(ks);
-    return (n_slots + per - 1) / per;
+constexpr int kSplitPartsAlloc = 4;    // partial-tile region: parts at R* rows
+inline bool gemm_may_split(long long max_units, int n_slots) {
+    return max_units > 0 && max_units < kSplitTargetUnits && n_slots >= 4;
+}
+inline int gemm_ksplit(long long max_units, int n_slots, int sms) {
+    if (!gemm_may_split(max_units, n_slots) || sms < 1) return 1;
+    int best = 1;
+    long long best_cost = ((max_units + sms - 1) / sms) * n_slots;
+    for (int ks = 2; ks <= kMaxKSplit && ks <= n_slots / 2; ++ks) {
+        const int per = (n_slots + ks - 1) / ks;
+        const int parts = (n_slots + per - 1) / per;      // no empty part
+        const long long cost = ((max_units * parts + sms - 1) / sms) * per;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = parts;
+        }
+    }
+    return best;
 }
 // Upper bound of the token tiles of a call (every tile holds >= 1 row).
 inline long long max_token_tiles(long long R, int max_tiles) {
@@ -80,6 +92,7 @@ inline int router_ksplit(int pairs, int nchunks) {
 struct WsLayout {
     size_t status, topk_ids, topk_w, blk_cnt, logits, partials, counters, offsets, gemm_partial;
     size_t sorted_assign, assign_row, tiles, x_perm, h, out_acc, total;
+    size_t gemm_partial_bytes;
     int max_tiles;
 };
 
@@ -112,16 +125,26 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
     L.x_perm = take(R * H * 2);
     L.h = take(R * I * 2);
     L.out_acc = take(static_cast<size_t>(T) * H * 4);
-    // gate_up K-split partial tiles, fp32 [part][weight block][routed row][128],
-    // sized for the larger split of the bf16 (H/64 slots) and MXFP4 (H/256
-    // slots) rings
+    // gate_up K-split partial tiles, fp32 [part][weight block][routed row][128].
+    // A call splits only while its unit bound
+    // (token tiles x weight blocks) is below kSplitTargetUnits, which holds
+    // for R up to some R* (the tile bound grows with R); the region holds
+    // kSplitPartsAlloc parts of R* rows whatever T is (a call with R rows may
+    // use as many parts as fit), so a workspace sized for one call of a layer
+    // shape serves every other T of that shape.
     {
         const int nwb = (2 * I + kWeightTileRows - 1) / kWeightTileRows;
-        const long long units = max_token_tiles(static_cast<long long>(R), L.max_tiles) * nwb;
-        const int ks_bf16 = gemm_ksplit(units, H / kBlockK);
-        const int ks_mx = gemm_ksplit(units, (H / kBlockK + 3) / 4);
-        const int ks = ks_bf16 > ks_mx ? ks_bf16 : ks_mx;
-        L.gemm_partial = take(ks > 1 ? static_cast<size_t>(ks) * nwb * R * kWeightTileRows * 4 : 0);
+        const int slots_bf16 = H / kBlockK, slots_mx = (H / kBlockK + 3) / 4;
+        long long rstar = 0;
+        // (units grow by >= nwb per 16 rows, so the loop ends before 16 x 304 rows)
+        for (long long r = 1;; ++r) {
+            const long long mt = r / 16 + (r < E ? r : E) + 1;
+            const long long units = max_token_tiles(r, static_cast<int>(mt)) * nwb;
+            if (!gemm_may_split(units, slots_bf16) && !gemm_may_split(units, slots_mx)) break;
+            rstar = r;
+        }
+        L.gemm_partial_bytes = static_cast<size_t>(kSplitPartsAlloc) * nwb * rstar * kWeightTileRows * 4;
+        L.gemm_partial = take(L.gemm_partial_bytes);
     }
     L.total = o;
     return L;

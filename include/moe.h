@@ -183,7 +183,9 @@ moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
  *                 launch (default), 0 = plain stream order;
  *   "ksplit":     0 = split the GEMMs' K range when a small batch leaves
  *                 SMs idle (default), 1 = never split (every output then
- *                 sums its K range in one fixed order).
+ *                 sums its K range in one fixed order), 2..8 = split every
+ *                 small-batch unit into that many parts (at most one per
+ *                 two ring slots, and as many as the workspace holds).
  * Returns MOE_ERR_ARG for an unknown key or value. */
 moe_status moe_set_tuning(const char* key, int value);
 

@@ -122,8 +122,10 @@ def test_tuning_switches(moe):
     moe.moe_set_tuning("pdl", 1)
     moe.moe_set_tuning("ksplit", 1)
     moe.moe_set_tuning("ksplit", 0)
+    moe.moe_set_tuning("ksplit", 3)
+    moe.moe_set_tuning("ksplit", 0)
     with pytest.raises(moe.MoEError):
-        moe.moe_set_tuning("ksplit", 2)
+        moe.moe_set_tuning("ksplit", 9)
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
