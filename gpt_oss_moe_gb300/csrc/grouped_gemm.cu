@@ -785,13 +785,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const int nk = min(KPS, p.k_blocks - st * KPS);
                 const uint8_t* crow = sm.codes + static_cast<size_t>(stage) * kCodeStageBytes + r * 128;
                 const uint32_t a_tm = a_tm_row + kASlotCols * static_cast<uint32_t>(aslot);
-                for (int jj = 0; jj < nk; ++jj) {
-                    const int kb = st * KPS + jj;
+                // k-block jj of the slot: codes = 16-byte unit jj * 2 + half of the
+                // row (128-byte swizzled), its E8M0 byte; the bf16 values go to
+                // row r, columns 32*jj + 16*half .. +15 of the A slot (word c of
+                // the 16 bytes = K 8c..8c+7 = columns 4c..4c+3)
+                const auto convert_store = [&](int jj, const uint4 cw, uint32_t sbyte) {
                     uint32_t f1, f2;
-                    e8m0_factors(row_ok ? srow[2 * kb + half] : 127u, f1, f2);
-                    // 16-byte unit jj * 2 + half of the row, 128-byte swizzled
-                    const uint32_t unit = static_cast<uint32_t>(jj * 2 + half);
-                    const uint4 cw = *reinterpret_cast<const uint4*>(crow + ((unit ^ swz) << 4));
+                    e8m0_factors(sbyte, f1, f2);
                     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
                     uint32_t v[16];
                     if (f2 == 0x3F803F80u) {
@@ -807,9 +807,28 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                             v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
                         }
                     }
-                    // row r, columns 32*jj + 16*half .. +15 of the A slot (word c
-                    // of the thread's 16 B of codes = K 8c..8c+7 = columns 4c..4c+3)
                     tmem_st16(a_tm + 32u * static_cast<uint32_t>(jj), v);
+                };
+                const auto code_of = [&](int jj) {
+                    return *reinterpret_cast<const uint4*>(
+                        crow + ((static_cast<uint32_t>(jj * 2 + half) ^ swz) << 4));
+                };
+                const auto scale_of = [&](int jj) {
+                    return row_ok ? static_cast<uint32_t>(srow[2 * (st * KPS + jj) + half]) : 127u;
+                };
+                if (nk == KPS) {
+                    // full slot: every load first, then the four expansions
+                    uint4 cw[KPS];
+                    uint32_t sb[KPS];
+#pragma unroll
+                    for (int jj = 0; jj < KPS; ++jj) {
+                        cw[jj] = code_of(jj);
+                        sb[jj] = scale_of(jj);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < KPS; ++jj) convert_store(jj, cw[jj], sb[jj]);
+                } else {
+                    for (int jj = 0; jj < nk; ++jj) convert_store(jj, code_of(jj), scale_of(jj));
                 }
                 tmem_wait_st();
                 tc_fence_before();
