@@ -103,14 +103,14 @@ struct SmemPlan {
 // MXFP4: one ring of `stages` slots, each a code tile + a token tile; the
 // converted bf16 W tiles live in TMEM, not here.
 __device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int astages, int box,
-                                              int wf, int kscale) {
+                                              int bbox, int wf, int kscale) {
     SmemPlan s;
     const uint32_t base = smem_u32(raw);
     uint8_t* p = raw + ((1024u - (base & 1023u)) & 1023u);
     s.a = p;
     p += static_cast<size_t>(wf == 1 ? 0 : stages) * kATileBytes;
     s.b = p;
-    p += static_cast<size_t>(stages) * (wf == 1 ? kMxfp4KbPerStage : 1) * box * 128;
+    p += static_cast<size_t>(stages) * (wf == 1 ? kMxfp4KbPerStage : 1) * bbox * 128;
     s.codes = p;
     s.scales = p;
     if (wf == 1) {
@@ -231,13 +231,22 @@ __device__ __forceinline__ void e8m0_factors(uint32_t s, uint32_t& f1, uint32_t&
     }
 }
 
-template <int EPI, int WF>
+template <int EPI, int WF, int CG>
 __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     grouped_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int KPS = kKbPerStage<WF>;
     const int stages = p.stages, astages = p.astages, box = p.token_box;
+    // CTA pair (CG = 2, bf16 weights): the cluster's two CTAs share each unit
+    // of 256 weight rows; CTA r loads rows 128r.. of the block and half of
+    // the token tile, the even CTA issues M = 256 MMAs over both.
+    constexpr bool kPair = CG == 2;
+    constexpr int kUnitRows = kPair ? 2 * kWeightTileRows : kWeightTileRows;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const int cta0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int ncta = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int bbox = kPair ? box / 2 : box;   // token rows of this CTA's B tile
     // TMEM columns: per MMA issuer two accumulators of acc_stride columns
     // (issuer i, buffer b at (2i + b) * acc_stride), then (MXFP4) astages A
     // slots of 128 columns, each the converted weights of one ring slot
@@ -254,16 +263,17 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     if (stages < 2 || stages > kMaxStages || n_iss < 1 || n_iss > (WF == 1 ? 2 : 1) ||
         p.ksplit < 1 || p.ksplit > kMaxKSplit ||
         (EPI == kEpiGlu && p.ksplit > 1 && (p.partial == nullptr || p.tickets == nullptr)) ||
+        (kPair && (WF != 0 || p.ksplit != 1 || (gridDim.x & 1u) || (box & 15))) ||
         (WF == 1 && (astages < 2 || astages > kMxfp4AStages || 2 * stages < astages + 2 ||
                      a_col0 + kASlotCols * static_cast<uint32_t>(astages) >
                          static_cast<uint32_t>(p.tmem_cols)))) {
         if (threadIdx.x == 0) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
         return;
     }
-    const uint32_t b_bytes = static_cast<uint32_t>(box) * 128u;       // one 64-wide K chunk
+    const uint32_t b_bytes = static_cast<uint32_t>(bbox) * 128u;      // one 64-wide K chunk
     const uint32_t b_stage_bytes = b_bytes * KPS;
     const int n_st = (p.k_blocks + KPS - 1) / KPS;                     // ring slots per unit
-    SmemPlan sm = plan_smem(smem_raw, stages, astages, box, WF, p.kscale);
+    SmemPlan sm = plan_smem(smem_raw, stages, astages, box, bbox, WF, p.kscale);
     volatile int* flags = sm.flags;
     const uint32_t scale_buf_bytes =
         static_cast<uint32_t>((kWeightTileRows * p.kscale + 15) / 16 * 16);
@@ -281,7 +291,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(sm.tfull + b), static_cast<uint32_t>(n_iss));
-            mbar_init(smem_u32(sm.tempty + b), kEpiThreads);
+            // pair: one arrival from each CTA's epilogue, on the even CTA's
+            mbar_init(smem_u32(sm.tempty + b), kPair ? 2u : static_cast<uint32_t>(kEpiThreads));
             mbar_init(smem_u32(sm.sfull + b), 1);
             mbar_init(smem_u32(sm.sempty + b), kConvTeams * kConvThreads);
         }
@@ -298,11 +309,14 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         tma_prefetch_desc(&tmap_x);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(sm.tmem_base), static_cast<uint32_t>(p.tmem_cols));
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_u32(sm.tmem_base), static_cast<uint32_t>(p.tmem_cols));
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
+    // pair: both CTAs' barriers are initialised before either CTA's TMA
+    // loads, MMAs or arrivals reach them
+    if (kPair) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_base;
 
@@ -322,7 +336,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             long long issued = 0;
             int local = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+            for (int u = cta0; u < num_units && ok; u += ncta) {
                 const Unit un = unit_of(u, p, n_st);
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
@@ -353,8 +367,10 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                         break;
                     }
                     const uint32_t fb = smem_u32(sm.full + stage);
-                    // full boxes are counted, zero-filled past K included
-                    mbar_arrive_expect_tx(fb, w_bytes + b_stage_bytes);
+                    // full boxes are counted, zero-filled past K included;
+                    // pair: the even CTA's barrier counts both CTAs' bytes
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(fb, (kPair ? 2u : 1u) * (w_bytes + b_stage_bytes));
                     const uint32_t b_dst = smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
                     if (WF == 1) {
                         // codes of k-blocks 4st..4st+3 (128 B per row), and the
@@ -363,6 +379,17 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                                     &tmap_w, fb, st * KPS * (kBlockK / 2), mb * kWeightTileRows, t.x,
                                     pol_w);
                         tma_load_3d(b_dst, &tmap_x, fb, 0, t.y, st * KPS, pol_x);
+                    } else if (kPair) {
+                        // rows 128 * rank.. of the 256-row block; token rows
+                        // n/2 * rank.. of the tile (each CTA holds N/2 of B)
+                        const uint32_t fb0 = mapa_shared(fb, 0);
+                        const int half_n = ((t.z + 15) & ~15) / 2;
+                        tma_load_3d_pair(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
+                                         &tmap_w, fb0, st * kBlockK,
+                                         mb * kUnitRows + static_cast<int>(rank) * kWeightTileRows,
+                                         t.x, pol_w);
+                        tma_load_2d_pair(b_dst, &tmap_x, fb0, st * kBlockK,
+                                         t.y + static_cast<int>(rank) * half_n, pol_x);
                     } else {
                         tma_load_3d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
                                     &tmap_w, fb, st * kBlockK, mb * kWeightTileRows, t.x, pol_w);
@@ -375,9 +402,10 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && rank == 0) {
                 // Wait (bounded) for the loads still in flight before the CTA
-                // may release its shared memory.
+                // may release its shared memory (pair: the even CTA's
+                // barriers count the odd CTA's loads too).
                 const long long pending = issued < stages ? issued : stages;
                 int s = stage;
                 uint32_t ph = phase;
@@ -397,19 +425,21 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         }
     } else if (WF == 0 && warp == 1) {
         // ------------------------------------------------ MMA issuer (bf16)
-        if (lane == 0) {
+        // pair: the even CTA issues for both; the odd CTA's warp 1 only
+        // allocates and frees its TMEM.
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int astage = 0;
             uint32_t aphase = 0;
             int local = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+            for (int u = cta0; u < num_units && ok; u += ncta) {
                 const Unit un = unit_of(u, p, n_st);
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
                 const uint32_t n_mma = static_cast<uint32_t>((t.z + 15) & ~15);
-                const uint32_t idesc = idesc_bf16_f32(kWeightTileRows, n_mma);
+                const uint32_t idesc = idesc_bf16_f32(kUnitRows, n_mma);
                 const int buf = local & 1;
                 const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
                 ++local;
@@ -440,7 +470,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     for (int jj = 0; jj < nk; ++jj) {
                         const int kb = (st - un.st_lo) * KPS + jj;   // from the part's start
                         const uint32_t b_addr = b_stage + static_cast<uint32_t>(jj) * b_bytes;
-                        if (WF == 1) {
+                        if constexpr (WF == 1) {
 #pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk) {
                                 tc_mma_bf16_ts(d_tmem, a_tm + 32u * jj + 8u * kk,
@@ -452,44 +482,59 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                                 smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes);
 #pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                                tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
-                                            smem_desc_sw128(b_addr + kk * 32), idesc,
-                                            (kb | kk) != 0 ? 1u : 0u);
+                                if constexpr (kPair)
+                                    tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + kk * 32),
+                                                     smem_desc_sw128(b_addr + kk * 32), idesc,
+                                                     (kb | kk) != 0 ? 1u : 0u);
+                                else
+                                    tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
+                                                smem_desc_sw128(b_addr + kk * 32), idesc,
+                                                (kb | kk) != 0 ? 1u : 0u);
                             }
                         }
                     }
-                    if (WF == 1) {
+                    if constexpr (WF == 1) {
                         tc_commit(smem_u32(sm.aempty + astage));
                         if (++astage == astages) {
                             astage = 0;
                             aphase ^= 1u;
                         }
                     }
-                    tc_commit(smem_u32(sm.empty + stage));
+                    // pair: the slot is free in both CTAs
+                    if constexpr (kPair)
+                        tc_commit_pair_mc(smem_u32(sm.empty + stage), 3);
+                    else
+                        tc_commit(smem_u32(sm.empty + stage));
                     if (++stage == stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(sm.tfull + buf));
+                if constexpr (kPair)
+                    tc_commit_pair_mc(smem_u32(sm.tfull + buf), 3);
+                else
+                    tc_commit(smem_u32(sm.tfull + buf));
             }
             // Every MMA issued so far has finished once this arrives.
-            tc_commit(smem_u32(sm.drain));
+            if constexpr (kPair)
+                tc_commit_pair(smem_u32(sm.drain));
+            else
+                tc_commit(smem_u32(sm.drain));
             mbar_wait(smem_u32(sm.drain), 0, nullptr);
         }
     } else if (WF == 1 && (warp == 1 || warp == kSecondIssuerWarp)) {
         // ------------------------------------------------ MMA issuers (MXFP4)
         // Issuer `is` takes ring slots st = is, is + n_iss, ... of each unit.
         const int is = warp == 1 ? 0 : 1;
-        if (lane == 0 && is < n_iss) {
+        if constexpr (WF == 1) if (lane == 0 && is < n_iss) {
             int local = 0;
             int sbase = 0;                        // ring use of the unit's first slot
             // ring positions of use `cur`, advanced (not divided) to each use
             int cur = 0, stage = 0, astage = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+            for (int u = cta0; u < num_units && ok; u += ncta) {
                 const Unit un = unit_of(u, p, n_st);
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
@@ -572,7 +617,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int row_in_tile = quad * 32 + lane;
         int local = 0;
-        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        for (int u = cta0; u < num_units; u += ncta) {
             const Unit un = unit_of(u, p, n_st);
             const int4 t = p.tiles[un.tile];
             if (!tile_ok(t, p)) {
@@ -604,7 +649,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             if (flags[1 + buf]) break;
             tc_fence_after();
 
-            const int wrow = mb * kWeightTileRows + row_in_tile;
+            const int wrow = mb * kUnitRows + static_cast<int>(rank) * kWeightTileRows + row_in_tile;
             const bool row_ok = wrow < p.w_rows;
             // the bias enters once: down adds it with part 0, gate_up after the sum
             const float bias =
@@ -648,7 +693,9 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     const float gate = odd ? recv : v[i];
                     const float up = odd ? v[8 + i] : recv;
                     const int c = c0 + i + (odd ? 8 : 0);
-                    if (c < t.z)
+                    // rows past 2I exist only in the last 256-row block of
+                    // CTA pairs (gate and up rows share their validity)
+                    if (c < t.z && row_ok)
                         hrow0[static_cast<size_t>(c) * hstride] =
                             __float2bfloat16_rn(clamped_glu(gate, up));
                 }
@@ -722,7 +769,14 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(sm.tempty + buf));
+            if (kPair) {
+                // one arrival per CTA, on the even CTA's barrier, once all
+                // 128 threads' TMEM loads are done
+                named_bar_sync(1, kEpiThreads);
+                if (ep == 0) mbar_arrive_cluster(mapa_shared(smem_u32(sm.tempty + buf), 0));
+            } else {
+                mbar_arrive(smem_u32(sm.tempty + buf));
+            }
         }
     } else if (WF == 1) {
         // ------------------------------------------------ MXFP4 converters
@@ -750,7 +804,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         int sbase = 0;                            // ring use of the unit's first slot
         int local = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        for (int u = cta0; u < num_units && ok; u += ncta) {
             const Unit un = unit_of(u, p, n_st);
             const int4 t = p.tiles[un.tile];
             if (!tile_ok(t, p)) continue;
@@ -843,43 +897,77 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
 
     tc_fence_before();
     __syncthreads();
+    // pair: the even CTA's MMAs have drained (into both CTAs' TMEM) and the
+    // odd CTA's arrivals on its barriers have landed before either CTA frees
+    // TMEM or exits
+    if (kPair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+        tmem_dealloc<CG>(tmem_base, static_cast<uint32_t>(p.tmem_cols));
     }
 }
 
-template <int EPI, int WF>
+template <int EPI, int WF, int CG>
 cudaError_t launch_gemm_t(const GemmParams& p, const CUtensorMap* tmap_w, const CUtensorMap* tmap_x,
                           int grid, size_t smem, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreadsOf<WF>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (CG == 2) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, WF>,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, WF, CG>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI, WF>, p, *tmap_w, *tmap_x);
+    if (CG == 2) {
+        // A persistent grid of pairs: no more pairs than fit at once (the
+        // SMs of a GPU partition may not all pair up), and an even count.
+        cfg.numAttrs = na;
+        cfg.gridDim = dim3(2);
+        int clusters = 0;
+        err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<EPI, WF, CG>, &cfg);
+        if (err != cudaSuccess) return err;
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        grid &= ~1;
+        if (grid > 2 * clusters) grid = 2 * clusters;
+        if (grid < 2) grid = 2;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.numAttrs = na;
+    cfg.gridDim = dim3(grid);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI, WF, CG>, p, *tmap_w, *tmap_x);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(int epi, int wf, const GemmParams& p, const CUtensorMap* tmap_w,
+cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUtensorMap* tmap_w,
                         const CUtensorMap* tmap_x, int grid, size_t smem, cudaStream_t s,
                         bool pdl) {
     if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
+    if (cg == 2) {
+        if (wf != 0) return cudaErrorInvalidValue;
+        return epi == kEpiGlu
+                   ? launch_gemm_t<kEpiGlu, 0, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl)
+                   : launch_gemm_t<kEpiCombine, 0, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl);
+    }
     if (epi == kEpiGlu)
-        return wf == 1 ? launch_gemm_t<kEpiGlu, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
-                       : launch_gemm_t<kEpiGlu, 0>(p, tmap_w, tmap_x, grid, smem, s, pdl);
-    return wf == 1 ? launch_gemm_t<kEpiCombine, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
-                   : launch_gemm_t<kEpiCombine, 0>(p, tmap_w, tmap_x, grid, smem, s, pdl);
+        return wf == 1 ? launch_gemm_t<kEpiGlu, 1, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
+                       : launch_gemm_t<kEpiGlu, 0, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl);
+    return wf == 1 ? launch_gemm_t<kEpiCombine, 1, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
+                   : launch_gemm_t<kEpiCombine, 0, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl);
 }
 
 // fp32 -> bf16 (round to nearest even) of the combined output.

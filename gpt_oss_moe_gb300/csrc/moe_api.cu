@@ -101,6 +101,11 @@ moe_status weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K, bo
 std::atomic<int> g_token_tile{0};
 std::atomic<int> g_ksplit_mode{0};  // 0: automatic, 1: never split, n >= 2: n parts
 std::atomic<int> g_pdl{1};
+std::atomic<int> g_pair_mode{0};   // 0: automatic, 1: never, 2: always (bf16 weights)
+// bf16 token boxes from which the GEMMs run on CTA pairs (automatic mode):
+// measured on gpt-oss-20b, pairs are 3 % slower at a 128-row box (T = 128),
+// even at 256 (T = 256) and 2-5 % faster at T >= 512
+constexpr int kPairMinBox = 256;
 
 // ------------------------------------------------------------ profiling
 //
@@ -381,10 +386,16 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     const int box = auto_token_tile(s);
     const bool pdl = g_pdl.load() != 0;
 
+    // CTA pairs (bf16, wide token boxes): M = 256 MMAs over two SMs, each SM
+    // loading 128 weight rows and half of the token tile, so a ring slot
+    // holds 32 KB instead of 48 KB (box 256) for the same tensor work.
+    const int pair_mode = g_pair_mode.load();
+    const bool pair = !mxfp4 && (pair_mode == 2 || (pair_mode == 0 && box >= kPairMinBox));
+    const int bbox = pair ? box / 2 : box;     // token rows of one CTA's B tile
     // Pipeline depth: as many stages as the shared memory allows (2..12).
     const int wf = mxfp4 ? 1 : 0;
     const int kscale_max = (s.H > s.I ? s.H : s.I) / 32;
-    const size_t stage_bytes = gemm_stage_bytes(box, wf);
+    const size_t stage_bytes = gemm_stage_bytes(bbox, wf);
     const size_t budget = static_cast<size_t>(dev.max_smem) - 1024;
     // MXFP4: per MMA issuer two accumulators of round_up(box, 32) TMEM
     // columns, then A slots of 128 columns, all in 512.  Two issuers (one N
@@ -431,7 +442,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
         }
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(R)};
         const cuuint64_t str[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t boxd[2] = {64, static_cast<cuuint32_t>(box)};
+        const cuuint32_t boxd[2] = {64, static_cast<cuuint32_t>(bbox)};
         return make_tmap(m, base, 2, dims, str, boxd);
     };
     MOE_TRY(token_tmap(&tm_x, x_perm, s.H));
@@ -460,8 +471,11 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.rows_total = R;
     g.status = status;
 
+    const int unit_rows = pair ? 2 * kWeightTileRows : kWeightTileRows;
+    const int cg = pair ? 2 : 1;
+
     // gate_up + bias + GLU -> h
-    g.n_wblocks = 2 * s.I / kWeightTileRows;
+    g.n_wblocks = (2 * s.I + unit_rows - 1) / unit_rows;
     g.k_blocks = s.H / kBlockK;
     g.w_rows = 2 * s.I;
     g.bias = static_cast<const __nv_bfloat16*>(gate_up.bias);
@@ -489,7 +503,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     // gate_up: at most 2 parts -- each part's epilogue stores, fences and
     // tickets its partial tile and the last one reloads all of them; at
     // 20b T=1 (180 units) 2 parts gave 33 us, 3 gave 39, 5 gave 46 (1: 37)
-    g.ksplit = parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, 2);
+    g.ksplit = pair ? 1 : parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, 2);
     {
         // no more parts than the partial-tile region holds at R rows
         const size_t part_bytes = static_cast<size_t>(g.n_wblocks) * R * kWeightTileRows * 4;
@@ -504,12 +518,13 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.partial = reinterpret_cast<float*>(ws + L.gemm_partial);
     g.tickets = reinterpret_cast<int32_t*>(ws + L.counters) + kSplitTicketOffset;
     long long units = tiles_max * g.n_wblocks * g.ksplit;
-    int grid = static_cast<int>(units < dev.sms ? units : dev.sms);
-    MOE_CUDA(launch_gemm(kEpiGlu, wf, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
+    long long ctas = units * cg;
+    int grid = static_cast<int>(ctas < dev.sms ? ctas : dev.sms);
+    MOE_CUDA(launch_gemm(kEpiGlu, wf, cg, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
     prof_mark("gate_up_glu", stream);
 
     // down + bias + weighted combine -> out (fp32 accumulation)
-    g.n_wblocks = (s.H + kWeightTileRows - 1) / kWeightTileRows;
+    g.n_wblocks = (s.H + unit_rows - 1) / unit_rows;
     g.k_blocks = s.I / kBlockK;
     g.w_rows = s.H;
     g.bias = static_cast<const __nv_bfloat16*>(down.bias);
@@ -521,12 +536,13 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.scales = static_cast<const uint8_t*>(down.scale);
     g.kscale = s.I / 32;
     // the down projection adds its K parts through the output's atomics
-    g.ksplit = parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, kMaxKSplit);
+    g.ksplit = pair ? 1 : parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, kMaxKSplit);
     g.partial = nullptr;
     g.tickets = nullptr;
     units = tiles_max * g.n_wblocks * g.ksplit;
-    grid = static_cast<int>(units < dev.sms ? units : dev.sms);
-    MOE_CUDA(launch_gemm(kEpiCombine, wf, g, &tm_wd, &tm_h, grid, smem, stream, pdl));
+    ctas = units * cg;
+    grid = static_cast<int>(ctas < dev.sms ? ctas : dev.sms);
+    MOE_CUDA(launch_gemm(kEpiCombine, wf, cg, g, &tm_wd, &tm_h, grid, smem, stream, pdl));
     prof_mark("down_combine", stream);
 
     if (!out_is_fp32) {
@@ -564,6 +580,11 @@ moe_status moe_set_tuning(const char* key, int value) {
     if (std::strcmp(key, "ksplit") == 0) {
         if (value < 0 || value > kMaxKSplit) return MOE_ERR_ARG;
         g_ksplit_mode.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "pair") == 0) {
+        if (value < 0 || value > 2) return MOE_ERR_ARG;
+        g_pair_mode.store(value);
         return MOE_OK;
     }
     if (std::strcmp(key, "pdl") == 0) {

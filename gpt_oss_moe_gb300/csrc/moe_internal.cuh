@@ -199,7 +199,7 @@ enum EpilogueKind { kEpiGlu = 0, kEpiCombine = 1 };
 struct GemmParams {
     const int4* tiles;           // token tiles from the permutation kernel
     const int32_t* num_tiles;    // device count of tiles
-    int n_wblocks;               // weight-row blocks of 128 per expert
+    int n_wblocks;               // weight-row blocks per expert (128 rows; CTA pairs: 256)
     int k_blocks;                // K / 64
     int w_rows;                  // weight rows per expert (2I or H)
     int token_box;               // token rows per TMA box (= MMA N bound)
@@ -261,7 +261,9 @@ int router_stage_multiple();
 cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tmap_x,
                           const CUtensorMap* tmap_wr, size_t smem, cudaStream_t s);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s, bool pdl);
-cudaError_t launch_gemm(int epi, int wf, const GemmParams& p, const CUtensorMap* tmap_w,
+// cg = 2 (bf16 only): CTA pairs (clusters of 2) on 256-row weight blocks,
+// each CTA holding token_box / 2 rows of every token tile; `grid` counts CTAs.
+cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUtensorMap* tmap_w,
                         const CUtensorMap* tmap_x, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, size_t n, cudaStream_t s,

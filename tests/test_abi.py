@@ -126,6 +126,11 @@ def test_tuning_switches(moe):
     moe.moe_set_tuning("ksplit", 0)
     with pytest.raises(moe.MoEError):
         moe.moe_set_tuning("ksplit", 9)
+    for v in (1, 2, 0):
+        moe.moe_set_tuning("pair", v)
+    for v in (-1, 3):
+        with pytest.raises(moe.MoEError):
+            moe.moe_set_tuning("pair", v)
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

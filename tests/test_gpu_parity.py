@@ -282,6 +282,51 @@ def test_ksplit_tickets_reset(moe, oracle_lib, synth_lib):
     _check(moe, oracle_lib, L2)
 
 
+PAIR_CASES = [
+    # E, k, H, I, T, token_tile   (bf16 GEMMs forced onto CTA pairs)
+    (8, 2, 128, 128, 1, 0),          # one 16-column tile: 8 token rows per CTA
+    (8, 4, 320, 192, 37, 0),         # 2I = 384: the odd CTA's rows of the last
+                                     # gate_up block are all past the matrix;
+                                     # H = 320: down's last block has 64 rows
+    (8, 4, 448, 256, 200, 48),       # H = 448: the odd CTA holds 64 rows of
+                                     # down's last block; 24 token rows per CTA
+    (4, 2, 192, 64, 700, 0),         # several 256-row token tiles per expert
+    (8, 4, 256, 256, 200, 16),       # smallest box: 8 token rows per CTA
+    (16, 4, 256, 384, 300, 0),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "E{}k{}H{}I{}T{}tile{}".format(*c))
+def test_forward_cta_pairs(moe, oracle_lib, synth_lib, case):
+    E, k, H, I, T, tile = case
+    L = synth_lib.make_layer(E=E, T=T, H=H, I=I, top_k=k, seed=800 + T + H, router_w_std=0.05)
+    moe.moe_set_tuning("pair", 2)
+    moe.moe_set_tuning("token_tile", tile)
+    try:
+        _check(moe, oracle_lib, L)
+    finally:
+        moe.moe_set_tuning("pair", 0)
+        moe.moe_set_tuning("token_tile", 0)
+
+
+def test_cta_pairs_match_single(moe, synth_lib):
+    """Pairs and single CTAs sum every output over K in the same order: the
+    routing is identical and the outputs agree to fp32 rounding of the
+    combine's atomics."""
+    L = synth_lib.make_layer(E=32, T=256, H=2880, I=2880, top_k=4, seed=811, router_w_std=0.05)
+    outs = []
+    for mode in (1, 2):
+        moe.moe_set_tuning("pair", mode)
+        try:
+            outs.append(gpu_forward(moe, L))
+        finally:
+            moe.moe_set_tuning("pair", 0)
+    (i1, w1, o1, ws1), (i2, w2, o2, ws2) = outs
+    assert moe.moe_get_device_status(ws1) == 0 and moe.moe_get_device_status(ws2) == 0
+    assert torch.equal(i1, i2) and torch.equal(w1, w2)
+    assert torch.allclose(o1, o2, rtol=0, atol=1e-5 * float(o1.abs().max()))
+
+
 # ---------------------------------------------------------------- MXFP4
 
 MXFP4_CASES = [
