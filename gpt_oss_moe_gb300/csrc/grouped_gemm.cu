@@ -23,8 +23,10 @@
 //               MXFP4: the W tile arrives as packed E2M1 codes [128 x 32 B]
 //               (unswizzled), and once per unit one bulk copy brings the
 //               unit's E8M0 scales [128 x K/32 B] (double-buffered).
-//   warp 1      TMEM owner + MMA issuer (one lane): 4 x (128 x N x 16)
-//               tcgen05.mma per slot into one of two TMEM accumulators.
+//   warp 1      TMEM owner + MMA issuer: the warp walks the ring, one
+//               elected lane issues 4 x (128 x N x 16) tcgen05.mma per slot
+//               into one of two TMEM accumulators (CTA pairs: 256 x N x 16
+//               from the even CTA).
 //   warps 2..5  epilogue (128 threads): tcgen05.ld of the accumulator, one
 //               TMEM lane (= weight row) per thread, 16 token columns at a
 //               time, then
@@ -265,6 +267,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         (EPI == kEpiGlu && p.ksplit > 1 && (p.partial == nullptr || p.tickets == nullptr)) ||
         (kPair && (WF != 0 || p.ksplit != 1 || (gridDim.x & 1u) || (box & 15))) ||
         (WF == 1 && (astages < 2 || astages > kMxfp4AStages || 2 * stages < astages + 2 ||
+                     (n_iss == 2 && (astages & 1)) ||
                      a_col0 + kASlotCols * static_cast<uint32_t>(astages) >
                          static_cast<uint32_t>(p.tmem_cols)))) {
         if (threadIdx.x == 0) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
@@ -425,13 +428,15 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         }
     } else if (WF == 0 && warp == 1) {
         // ------------------------------------------------ MMA issuer (bf16)
-        // pair: the even CTA issues for both; the odd CTA's warp 1 only
-        // allocates and frees its TMEM.
-        if (lane == 0 && rank == 0) {
+        // The whole warp walks the loop, so the barrier waits and the
+        // descriptors are warp-uniform, and one elected lane issues the MMAs
+        // and commits: 4 MMAs + commit then take ~170 SM cycles, against
+        // ~450 when a lone lane walks the loop.  Pair: the even CTA issues
+        // for both; the odd CTA's warp 1 only allocates and frees its TMEM.
+        if (rank == 0) {
+            const bool leader = elect_one();
             int stage = 0;
             uint32_t phase = 0;
-            int astage = 0;
-            uint32_t aphase = 0;
             int local = 0;
             bool ok = true;
             for (int u = cta0; u < num_units && ok; u += ncta) {
@@ -443,91 +448,75 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const int buf = local & 1;
                 const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
                 ++local;
-                if (!mbar_wait(smem_u32(sm.tempty + buf), tph ^ 1u, flags)) {
-                    raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                if (!warp_wait(smem_u32(sm.tempty + buf), tph ^ 1u, flags)) {
+                    if (leader) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * acc_stride;
-                for (int st = un.st_lo; st < un.st_hi && ok; ++st) {
-                    const int nk = min(KPS, p.k_blocks - st * KPS);
-                    // bf16: the slot's tiles have landed.  MXFP4: its A slot
-                    // is converted (which implies the codes and token chunks
-                    // landed).  One wait per slot: a wait issued behind
-                    // in-flight MMAs costs about as much as four N = 16 MMAs.
-                    const uint32_t ready =
-                        WF == 1 ? smem_u32(sm.afull + astage) : smem_u32(sm.full + stage);
-                    if (!mbar_wait(ready, WF == 1 ? aphase : phase, flags)) {
-                        raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                for (int st = un.st_lo; st < un.st_hi; ++st) {
+                    if (!warp_wait(smem_u32(sm.full + stage), phase, flags)) {
+                        if (leader) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b_stage =
-                        smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
-                    const uint32_t a_tm = tmem_base + a_col0 + kASlotCols * static_cast<uint32_t>(astage);
-                    for (int jj = 0; jj < nk; ++jj) {
-                        const int kb = (st - un.st_lo) * KPS + jj;   // from the part's start
-                        const uint32_t b_addr = b_stage + static_cast<uint32_t>(jj) * b_bytes;
-                        if constexpr (WF == 1) {
+                    // K steps of 16: +32 bytes along the swizzled rows, +2 in
+                    // the descriptors' start-address field (address >> 4)
+                    const uint64_t ad =
+                        smem_desc_sw128(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes));
+                    const uint64_t bd =
+                        smem_desc_sw128(smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes));
+                    const uint32_t acc0 = st != un.st_lo ? 1u : 0u;   // the part's first k-block
+                    if (leader) {
 #pragma unroll
-                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                                tc_mma_bf16_ts(d_tmem, a_tm + 32u * jj + 8u * kk,
-                                               smem_desc_sw128(b_addr + kk * 32), idesc,
-                                               (kb | kk) != 0 ? 1u : 0u);
-                            }
-                        } else {
-                            const uint32_t a_addr =
-                                smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes);
-#pragma unroll
-                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                                if constexpr (kPair)
-                                    tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + kk * 32),
-                                                     smem_desc_sw128(b_addr + kk * 32), idesc,
-                                                     (kb | kk) != 0 ? 1u : 0u);
-                                else
-                                    tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
-                                                smem_desc_sw128(b_addr + kk * 32), idesc,
-                                                (kb | kk) != 0 ? 1u : 0u);
-                            }
+                        for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                            const uint32_t acc = kk == 0 ? acc0 : 1u;
+                            if constexpr (kPair)
+                                tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
+                            else
+                                tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
                         }
+                        // pair: the slot is free in both CTAs
+                        if constexpr (kPair)
+                            tc_commit_pair_mc(smem_u32(sm.empty + stage), 3);
+                        else
+                            tc_commit(smem_u32(sm.empty + stage));
                     }
-                    if constexpr (WF == 1) {
-                        tc_commit(smem_u32(sm.aempty + astage));
-                        if (++astage == astages) {
-                            astage = 0;
-                            aphase ^= 1u;
-                        }
-                    }
-                    // pair: the slot is free in both CTAs
-                    if constexpr (kPair)
-                        tc_commit_pair_mc(smem_u32(sm.empty + stage), 3);
-                    else
-                        tc_commit(smem_u32(sm.empty + stage));
+                    __syncwarp();
                     if (++stage == stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if constexpr (kPair)
-                    tc_commit_pair_mc(smem_u32(sm.tfull + buf), 3);
-                else
-                    tc_commit(smem_u32(sm.tfull + buf));
+                if (leader) {
+                    if constexpr (kPair)
+                        tc_commit_pair_mc(smem_u32(sm.tfull + buf), 3);
+                    else
+                        tc_commit(smem_u32(sm.tfull + buf));
+                }
+                __syncwarp();
             }
             // Every MMA issued so far has finished once this arrives.
-            if constexpr (kPair)
-                tc_commit_pair(smem_u32(sm.drain));
-            else
-                tc_commit(smem_u32(sm.drain));
-            mbar_wait(smem_u32(sm.drain), 0, nullptr);
+            if (leader) {
+                if constexpr (kPair)
+                    tc_commit_pair(smem_u32(sm.drain));
+                else
+                    tc_commit(smem_u32(sm.drain));
+                mbar_wait(smem_u32(sm.drain), 0, nullptr);
+            }
+            __syncwarp();
         }
     } else if (WF == 1 && (warp == 1 || warp == kSecondIssuerWarp)) {
         // ------------------------------------------------ MMA issuers (MXFP4)
-        // Issuer `is` takes ring slots st = is, is + n_iss, ... of each unit.
+        // Issuer `is` takes ring slots st = is, is + n_iss, ... of each unit;
+        // as for bf16, its whole warp walks the loop and one elected lane
+        // issues.
         const int is = warp == 1 ? 0 : 1;
-        if constexpr (WF == 1) if (lane == 0 && is < n_iss) {
+        if constexpr (WF == 1) if (is < n_iss) {
+            const bool leader = elect_one();
             int local = 0;
             int sbase = 0;                        // ring use of the unit's first slot
             // ring positions of use `cur`, advanced (not divided) to each use
@@ -543,8 +532,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const int buf = local & 1;
                 const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
                 ++local;
-                if (!mbar_wait(smem_u32(sm.tempty + buf), tph ^ 1u, flags)) {
-                    raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                if (!warp_wait(smem_u32(sm.tempty + buf), tph ^ 1u, flags)) {
+                    if (leader) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                     ok = false;
                     break;
                 }
@@ -557,20 +546,18 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                             stage = 0;
                             phase ^= 1u;
                         }
-                        if (WF == 1 && ++astage == astages) {
+                        if (++astage == astages) {
                             astage = 0;
                             aphase ^= 1u;
                         }
                     }
                     const int nk = min(KPS, p.k_blocks - st * KPS);
-                    // bf16: the slot's tiles have landed.  MXFP4: its A slot
-                    // is converted (which implies the codes and token chunks
-                    // landed).  One wait per slot: a wait issued behind
-                    // in-flight MMAs costs about as much as four N = 16 MMAs.
-                    const uint32_t ready =
-                        WF == 1 ? smem_u32(sm.afull + astage) : smem_u32(sm.full + stage);
-                    if (!mbar_wait(ready, WF == 1 ? aphase : phase, flags)) {
-                        raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                    // The slot's A slot is converted (which implies its codes
+                    // and token chunks landed).  One wait per slot: a wait
+                    // issued behind in-flight MMAs costs about as much as four
+                    // N = 16 MMAs.
+                    if (!warp_wait(smem_u32(sm.afull + astage), aphase, flags)) {
+                        if (leader) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                         ok = false;
                         break;
                     }
@@ -578,38 +565,33 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     const uint32_t b_stage =
                         smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
                     const uint32_t a_tm = tmem_base + a_col0 + kASlotCols * static_cast<uint32_t>(astage);
-                    for (int jj = 0; jj < nk; ++jj) {
-                        // the issuer's first MMA of the unit starts its sum
-                        const bool first = st == un.st_lo + is && jj == 0;
-                        const uint32_t b_addr = b_stage + static_cast<uint32_t>(jj) * b_bytes;
-                        if (WF == 1) {
+                    if (leader) {
+                        for (int jj = 0; jj < nk; ++jj) {
+                            // the issuer's first MMA of the unit starts its sum
+                            const bool first = st == un.st_lo + is && jj == 0;
+                            const uint64_t bd =
+                                smem_desc_sw128(b_stage + static_cast<uint32_t>(jj) * b_bytes);
 #pragma unroll
-                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                                tc_mma_bf16_ts(d_tmem, a_tm + 32u * jj + 8u * kk,
-                                               smem_desc_sw128(b_addr + kk * 32), idesc,
+                            for (int kk = 0; kk < kBlockK / 16; ++kk)
+                                tc_mma_bf16_ts(d_tmem, a_tm + 32u * jj + 8u * kk, bd + 2 * kk, idesc,
                                                (first && kk == 0) ? 0u : 1u);
-                            }
-                        } else {
-                            const uint32_t a_addr =
-                                smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes);
-#pragma unroll
-                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                                tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
-                                            smem_desc_sw128(b_addr + kk * 32), idesc,
-                                            (first && kk == 0) ? 0u : 1u);
-                            }
                         }
+                        tc_commit(smem_u32(sm.aempty + astage));
+                        tc_commit(smem_u32(sm.empty + stage));
                     }
-                    if (WF == 1) tc_commit(smem_u32(sm.aempty + astage));
-                    tc_commit(smem_u32(sm.empty + stage));
+                    __syncwarp();
                 }
                 if (!ok) break;
                 sbase += un.st_hi - un.st_lo;
-                tc_commit(smem_u32(sm.tfull + buf));
+                if (leader) tc_commit(smem_u32(sm.tfull + buf));
+                __syncwarp();
             }
             // Every MMA this issuer issued has finished once this arrives.
-            tc_commit(smem_u32(sm.drain + is));
-            mbar_wait(smem_u32(sm.drain + is), 0, nullptr);
+            if (leader) {
+                tc_commit(smem_u32(sm.drain + is));
+                mbar_wait(smem_u32(sm.drain + is), 0, nullptr);
+            }
+            __syncwarp();
         }
     } else if (warp < 6) {
         // ------------------------------------------------ epilogue
@@ -784,13 +766,20 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         // the slot use g): a team converts the slot's (up to) 4 k-blocks into
         // A slot g % astages in TMEM, then each warp arrives once on its
         // barrier.  Barrier waits cost tens of nanoseconds even when ready,
-        // so they are taken once per slot, not per k-block.  A wait never
-        // passes two phases early: a team at use g has finished g-2, which
-        // needed the MMAs of use g-2-astages, so (MMAs completing in order)
-        // every use up to g-2-astages is complete -- the use before the
-        // previous one of g's A slot (astages >= 2) and of g's code slot
-        // (2 x stages >= astages + 2).  Arrivals for use g come only after
-        // the MMAs of use g-astages, i.e. after that phase was consumed.
+        // so they are taken once per slot, not per k-block.  No wait runs
+        // two phases early (a parity wait would then pass at once):
+        //  - code slot of use g: the team has converted g-2, so the producer,
+        //    which loads in use order, has loaded every use up to g-2, which
+        //    includes g - stages (stages >= 2);
+        //  - A slot of use g: the team has waited for the MMAs of g-2-astages.
+        //    MMAs complete in order only per issuer, so with two issuers
+        //    astages is even: all uses of one A slot then belong to one team
+        //    and one issuer, and g - 2 x astages <= g-2-astages is complete.
+        //    The issuer at use g has consumed g-2 (two issuers; g-1 with
+        //    one), so this team (or the other one, converting in order) has
+        //    converted g - astages.
+        // Arrivals for use g come only after the MMAs of use g-astages, i.e.
+        // after that phase was consumed.
         // A warp may touch only its own TMEM lane quadrant (warp % 4), so
         // the warp's rows are that quadrant's 32 rows.
         const int cw_idx = warp - 6;              // 0..15

@@ -407,6 +407,10 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
         n_iss = 2 * 2 * acc + 2 * 128 <= 512 ? 2 : 1;
         astages = (512 - 2 * n_iss * acc) / 128;
         if (astages > kMxfp4AStages) astages = kMxfp4AStages;
+        // two issuers: an even count, so that every A slot is always used by
+        // the same issuer and converter team (their barrier phases then
+        // advance in order)
+        if (n_iss == 2) astages &= ~1;
         if (astages < 2) return MOE_ERR_UNSUPPORTED;
     }
     const size_t fixed = gemm_fixed_bytes(box, wf, kscale_max);

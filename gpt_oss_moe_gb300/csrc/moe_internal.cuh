@@ -233,8 +233,9 @@ struct GemmParams {
 // stage holds kMxfp4KbPerStage k-blocks (codes [128 x 128 B] + that many
 // 64-wide token chunks); its converted weights take an A slot of 128 TMEM
 // columns after the two accumulators -- up to kMxfp4AStages slots, as many
-// as fit in 512 columns (3 for token tiles up to 64 rows, 2 for 128) --
-// and token tiles are at most kMxfp4MaxTokenTile rows.
+// as fit in 512 columns and, with two MMA issuers, an even count (2 for every
+// token tile up to 128 rows) -- and token tiles are at most
+// kMxfp4MaxTokenTile rows.
 constexpr int kMxfp4AStages = 3;
 constexpr int kMxfp4MaxTokenTile = 128;
 constexpr int kMxfp4KbPerStage = 4;     // k-blocks of 64 per MXFP4 ring slot
