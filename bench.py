@@ -380,8 +380,13 @@ def main():
         roof = {"bound": "hbm", "achieved": gu_alg / (gu_ms * 1e-3) / 1e9, "peak": bw,
                 "unit": "GB/s"}
     else:
+        # a kernel timed inside a long run of steps runs under the power
+        # cap: its peak is the sustained GEMM rate, a short run's the burst
+        long_run = elapsed_ms >= 100.0
         roof = {"bound": "tensor", "achieved": gu_flops / (gu_ms * 1e-3) / 1e12,
-                "peak": tf_burst, "unit": "TFLOP/s"}
+                "peak": tf_sust if long_run else tf_burst, "unit": "TFLOP/s"}
+        roof["frac_of_burst"] = roof["achieved"] / tf_burst
+        peak_kind += ", sustained bf16 GEMM rate" if long_run else ", burst bf16 GEMM rate"
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic("gate_up_glu", wl_key)
     roof["kernel"] = "gate_up_glu (tcgen05 grouped GEMM + fused bias/GLU)"
@@ -401,7 +406,9 @@ def main():
                   "hbm_gbs": layer_bytes / step_s / 1e9,
                   "hbm_frac": layer_bytes / step_s / 1e9 / bw,
                   "tflops": layer_flops / step_s / 1e12,
-                  "tensor_frac": layer_flops / step_s / 1e12 / tf_burst},
+                  "tensor_frac": layer_flops / step_s / 1e12 /
+                                 (tf_sust if elapsed_ms >= 100.0 else tf_burst),
+                  "tensor_frac_of_burst": layer_flops / step_s / 1e12 / tf_burst},
         "kernels_ms": {n: round(v, 5) for n, v in kernels},
         "kernel_timing": {"method": "CUDA events around every kernel, second timed region "
                                     "of the same K steps",
