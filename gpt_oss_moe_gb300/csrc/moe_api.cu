@@ -282,7 +282,7 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
 
     PermuteParams pp{};
     pp.topk_ids = r.ids;
-    pp.blk_base = rp.blk_cnt;
+    pp.blk_cnt = rp.blk_cnt;
     pp.offsets = r.offsets;
     pp.x = static_cast<const __nv_bfloat16*>(hidden);
     pp.T = s.T;
@@ -291,7 +291,10 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     pp.top_k = s.top_k;
     pp.nblocks = nb;
     const int rows_per_block = (s.T < kRouterTokens ? s.T : kRouterTokens) * s.top_k;
-    int g = (x_perm || zero_out) ? (2 * dev.sms + nb - 1) / nb : 1;
+    // CTAs per token block: as many as keep the grid within one wave (two
+    // permutation CTAs fit on an SM); rounding up left a second wave that
+    // started 18 us late at T = 4096
+    int g = (x_perm || zero_out) ? (2 * dev.sms) / nb : 1;
     if (g > 32) g = 32;
     if (g > rows_per_block) g = rows_per_block;
     pp.gather_split = g < 1 ? 1 : g;

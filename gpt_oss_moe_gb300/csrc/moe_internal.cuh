@@ -71,17 +71,23 @@ inline long long max_token_tiles(long long R, int max_tiles) {
 }
 
 constexpr size_t kCounterBytes =
-    static_cast<size_t>(kPairSlots + kMaxTokenBlocks + kSplitTargetUnits) * 4;
+    static_cast<size_t>(kPairSlots + kMaxTokenBlocks + kSplitTargetUnits + kMaxExperts) * 4;
 // GEMM split tickets: counters + kSplitTicketOffset (ints)
 constexpr int kSplitTicketOffset = kPairSlots + kMaxTokenBlocks;
+// Per-expert assignment totals, summed by the router's token blocks and
+// read (then zeroed) by the last one: counters + kExpertTotalsOffset (ints)
+constexpr int kExpertTotalsOffset = kPairSlots + kMaxTokenBlocks + kSplitTargetUnits;
 
 // K slices of the router: the hidden dimension is cut into `ksplit` slices
 // handled by separate CTAs when there are few (token block, expert group)
-// pairs, so that a small batch still spreads its loads over ~2 CTAs per SM
-// (sized for GB300's 152 SMs; each slice keeps at least 4 chunks of 64).
+// pairs, so that a small batch still spreads its loads over ~2 CTAs per SM,
+// but never so many that the grid needs a second wave (two router CTAs fit
+// on an SM; sized for GB300's 152 SMs; each slice keeps at least 4 chunks of
+// 64).  Measured at T = 4096: 3 slices (384 CTAs) left the last CTAs
+// starting 8 us after the first.
 inline int router_ksplit(int pairs, int nchunks) {
     if (pairs < 1 || nchunks < 1) return 1;
-    int ks = (304 + pairs - 1) / pairs;
+    int ks = 304 / pairs;                            // one wave of 2 CTAs per SM
     const int cap = nchunks / 4 > 1 ? nchunks / 4 : 1;
     if (ks > cap) ks = cap;
     if (ks < 1) ks = 1;
@@ -161,11 +167,10 @@ struct RouterParams {
     int stages;                  // TMA ring depth
     float* logits;               // [nblocks, 32, E] when egroups > 1
     float* partials;             // [nblocks, egroups, ksplit, 32, 32] when ksplit > 1
-    int32_t* counters;           // [kPairSlots] + [kMaxTokenBlocks], zero between calls
+    int32_t* counters;           // fixed counter region, zero between calls
     int32_t* topk_ids;           // [T, k]
     float* topk_w;               // [T, k]
-    int32_t* blk_cnt;            // [E, nblocks]: counts, then (after the
-                                 // last block) the exclusive prefix per expert
+    int32_t* blk_cnt;            // [E, nblocks]: assignments per expert and token block
     int32_t* offsets;            // [E+1]
     int4* tiles;                 // GEMM token tiles (expert, first row, rows, 0)
     int max_tiles;
@@ -177,7 +182,7 @@ struct RouterParams {
 
 struct PermuteParams {
     const int32_t* topk_ids;     // [T, k]
-    const int32_t* blk_base;     // [E, nblocks] exclusive prefix per expert
+    const int32_t* blk_cnt;      // [E, nblocks] assignments per expert and token block
     const int32_t* offsets;      // [E+1]
     const __nv_bfloat16* x;      // [T, H]
     int T, H, E, top_k, nblocks;

@@ -4,11 +4,13 @@
 //
 // The T*k assignments a = t*k + j are placed in rows sorted by
 // (expert, a) ascending -- a stable counting sort.  The router kernel left,
-// per expert e and 32-token block b, the number of rows of e that earlier
-// blocks own (blk_base[e][b]) and the expert offsets.  CTA (b, y):
-//   1. ranks block b's assignments per expert in order of a (warp match),
-//      so row(a) = offsets[e] + blk_base[e][b] + rank; the y == 0 CTA
-//      writes sorted_assign / assign_row;
+// per expert e and 32-token block b, the block's count of e (blk_cnt[e][b])
+// and the expert offsets.  CTA (b, y):
+//   1. sums the counts of the earlier blocks, base(e) = sum over b' < b of
+//      blk_cnt[e][b'] (a warp per expert, loads in flight together), and ranks
+//      block b's assignments per expert in order of a (warp match), so
+//      row(a) = offsets[e] + base(e) + rank; the y == 0 CTA writes
+//      sorted_assign / assign_row;
 //   2. copies its share (1/gather_split) of those assignments' activation
 //      rows into x_perm[row] -- the contiguous per-expert operand of the
 //      gate_up GEMM -- one warp per row, 16-byte loads kept in flight.
@@ -47,11 +49,39 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E, k = p.top_k, b = blockIdx.x;
 
-    if (tid < E) {
-        base[tid] = __ldcg(p.offsets + tid) +
-                    __ldcg(p.blk_base + static_cast<size_t>(tid) * p.nblocks + b);
-        running[tid] = 0;
+    // base(e) = offsets[e] + rows of e that earlier token blocks own.  Warp
+    // w sums experts w, w + 8, ... (its lanes stride the blocks b' < b of
+    // the expert's row of blk_cnt), eight experts and two blocks per lane in
+    // flight, then a warp reduction: no atomics, and with few blocks every
+    // load (offsets included) is in flight at once.
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kExpertBatch = 8;
+    for (int e0 = warp; e0 < E; e0 += kWarps * kExpertBatch) {
+        int sum[kExpertBatch], off[kExpertBatch];
+#pragma unroll
+        for (int m = 0; m < kExpertBatch; ++m) {
+            const int e = e0 + m * kWarps;
+            off[m] = e < E ? __ldcg(p.offsets + e) : 0;
+            sum[m] = 0;
+        }
+#pragma unroll 2
+        for (int j = lane; j < b; j += 32) {
+#pragma unroll
+            for (int m = 0; m < kExpertBatch; ++m) {
+                const int e = e0 + m * kWarps;
+                if (e < E) sum[m] += __ldcg(p.blk_cnt + static_cast<size_t>(e) * p.nblocks + j);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kExpertBatch; ++m) {
+            int v = sum[m];
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+            const int e = e0 + m * kWarps;
+            if (lane == 0 && e < E) base[e] = off[m] + v;
+        }
     }
+    if (tid < E) running[tid] = 0;
     __syncthreads();
 
     // Stable ranks of this block's assignments (warp 0, 32 at a time).
