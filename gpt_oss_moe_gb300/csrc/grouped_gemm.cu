@@ -55,6 +55,8 @@
 // MOE_DEV_WAIT_TIMEOUT in the status word and makes all roles leave their
 // loops; the producer then waits (bounded) for the loads it still has in
 // flight, the MMA issuer for its last MMAs, and TMEM is freed before exit.
+#include <type_traits>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "../../include/moe.h"
@@ -792,6 +794,10 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         const uint32_t swz = static_cast<uint32_t>(r & 7);
         int sbase = 0;                            // ring use of the unit's first slot
         int local = 0;
+        // ring positions of use `cur`, advanced (not divided: a division by
+        // the runtime ring sizes costs dozens of instructions) to each use
+        int cur = 0, stage = 0, aslot = 0;
+        uint32_t phase = 0, aphase = 0;
         bool ok = true;
         for (int u = cta0; u < num_units && ok; u += ncta) {
             const Unit un = unit_of(u, p, n_st);
@@ -811,11 +817,16 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             const int nsl = un.st_hi - un.st_lo;      // ring slots of this unit
             for (int i = (team ^ sbase) & 1; i < nsl; i += 2) {
                 const int st = un.st_lo + i;
-                const int use = sbase + i;
-                const int stage = use % stages;
-                const uint32_t phase = static_cast<uint32_t>(use / stages) & 1u;
-                const int aslot = use % astages;
-                const uint32_t aphase = static_cast<uint32_t>(use / astages) & 1u;
+                for (const int use = sbase + i; cur < use; ++cur) {
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    if (++aslot == astages) {
+                        aslot = 0;
+                        aphase ^= 1u;
+                    }
+                }
                 // the outcome is made warp-uniform: the lanes must not split
                 // before the warp's single arrival below
                 const bool got = mbar_wait(smem_u32(sm.full + stage), phase, flags) &&
@@ -832,23 +843,24 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 // row (128-byte swizzled), its E8M0 byte; the bf16 values go to
                 // row r, columns 32*jj + 16*half .. +15 of the A slot (word c of
                 // the 16 bytes = K 8c..8c+7 = columns 4c..4c+3)
-                const auto convert_store = [&](int jj, const uint4 cw, uint32_t sbyte) {
+                // k-block jj: E2M1 codes to bf16 times 2^(s-127), stored to TMEM.
+                // kTwo: the bf16 scale factor needs two multiplies (s > 128).
+                const auto convert_store = [&](auto two_tag, int jj, const uint4 cw, uint32_t sbyte) {
+                    constexpr bool kTwo = decltype(two_tag)::value;
                     uint32_t f1, f2;
-                    e8m0_factors(sbyte, f1, f2);
+                    if (kTwo) {
+                        e8m0_factors(sbyte, f1, f2);
+                    } else {
+                        const uint32_t h = (sbyte + 126u) << 7;     // 2^(s-1), s <= 128
+                        f1 = h | (h << 16);
+                        f2 = 0x3F803F80u;
+                    }
                     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
                     uint32_t v[16];
-                    if (f2 == 0x3F803F80u) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 q = e2m1x8_to_bf16<false>(words[c], f1, f2);
-                            v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 q = e2m1x8_to_bf16<true>(words[c], f1, f2);
-                            v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
-                        }
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 q = e2m1x8_to_bf16<kTwo>(words[c], f1, f2);
+                        v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
                     }
                     tmem_st16(a_tm + 32u * static_cast<uint32_t>(jj), v);
                 };
@@ -859,19 +871,29 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const auto scale_of = [&](int jj) {
                     return row_ok ? static_cast<uint32_t>(srow[2 * (st * KPS + jj) + half]) : 127u;
                 };
-                if (nk == KPS) {
-                    // full slot: every load first, then the four expansions
-                    uint4 cw[KPS];
-                    uint32_t sb[KPS];
+                // every load first, then the expansions; whether any lane of
+                // the warp needs the second scale factor is decided once per
+                // slot (a per-lane, per-k-block choice cost ~17 instructions
+                // per k-block)
+                uint4 cw[KPS];
+                uint32_t sb[KPS];
+                bool big = false;
 #pragma unroll
-                    for (int jj = 0; jj < KPS; ++jj) {
+                for (int jj = 0; jj < KPS; ++jj) {
+                    if (jj < nk) {
                         cw[jj] = code_of(jj);
                         sb[jj] = scale_of(jj);
+                        big |= sb[jj] > 128u;
                     }
+                }
+                if (__any_sync(0xffffffffu, big)) {
 #pragma unroll
-                    for (int jj = 0; jj < KPS; ++jj) convert_store(jj, cw[jj], sb[jj]);
+                    for (int jj = 0; jj < KPS; ++jj)
+                        if (jj < nk) convert_store(std::true_type{}, jj, cw[jj], sb[jj]);
                 } else {
-                    for (int jj = 0; jj < nk; ++jj) convert_store(jj, code_of(jj), scale_of(jj));
+#pragma unroll
+                    for (int jj = 0; jj < KPS; ++jj)
+                        if (jj < nk) convert_store(std::false_type{}, jj, cw[jj], sb[jj]);
                 }
                 tmem_wait_st();
                 tc_fence_before();

@@ -352,13 +352,15 @@ def test_forward_mxfp4_small_shapes(moe, oracle_lib, synth_lib, case):
         moe.moe_set_tuning("token_tile", 0)
 
 
-@pytest.mark.parametrize("T", [3, 300])
-def test_mxfp4_dequant_is_exact(moe, oracle_lib, synth_lib, T):
+@pytest.mark.parametrize("T,scale_lo,scale_hi", [(3, 116, 126), (300, 116, 126), (300, 124, 136)])
+def test_mxfp4_dequant_is_exact(moe, oracle_lib, synth_lib, T, scale_lo, scale_hi):
     """In-kernel dequantisation is exact: with top-1 routing each output
     element is a single combine term (weight 1), so the MXFP4 path must equal
-    bit for bit the bf16 path run on the oracle's dequantised weights."""
+    bit for bit the bf16 path run on the oracle's dequantised weights.  Scale
+    bytes above 128 (factors above 2) take the kernel's two-multiply path,
+    mixed with one-multiply lanes in the same warps."""
     Lq = synth_lib.make_layer(E=4, T=T, H=320, I=192, top_k=1, seed=9, wfmt="mxfp4",
-                              scale_lo=116, scale_hi=126)
+                              scale_lo=scale_lo, scale_hi=scale_hi)
     Lb = dataclasses.replace(
         Lq, wfmt="bf16", s_gu=None, s_d=None,
         w_gu=oracle_lib.dequant_mxfp4(Lq.w_gu, Lq.s_gu).to(torch.bfloat16).contiguous(),
