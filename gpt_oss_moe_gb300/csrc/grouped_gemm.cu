@@ -513,9 +513,11 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         }
     } else if (WF == 1 && (warp == 1 || warp == kSecondIssuerWarp)) {
         // ------------------------------------------------ MMA issuers (MXFP4)
-        // Issuer `is` takes ring slots st = is, is + n_iss, ... of each unit;
-        // as for bf16, its whole warp walks the loop and one elected lane
-        // issues.
+        // Issuer `is` takes the ring slots whose use (the ring position counted
+        // over the CTA's units) has parity `is`, so that an A slot and a
+        // converter team always meet the same issuer -- their barrier phases
+        // then advance in order even when a unit has an odd slot count; as
+        // for bf16, its whole warp walks the loop and one elected lane issues.
         const int is = warp == 1 ? 0 : 1;
         if constexpr (WF == 1) if (is < n_iss) {
             const bool leader = elect_one();
@@ -542,7 +544,10 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 tc_fence_after();
                 const uint32_t d_tmem =
                     tmem_base + static_cast<uint32_t>(2 * is + buf) * acc_stride;
-                for (int st = un.st_lo + is; st < un.st_hi && ok; st += n_iss) {
+                // issuer `is` takes the unit's slots of use parity `is` (the
+                // parity of its A slot and converter team in every unit)
+                const int off = n_iss == 2 ? ((is ^ sbase) & 1) : 0;
+                for (int st = un.st_lo + off; st < un.st_hi && ok; st += n_iss) {
                     for (const int use = sbase + (st - un.st_lo); cur < use; ++cur) {
                         if (++stage == stages) {
                             stage = 0;
@@ -570,7 +575,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     if (leader) {
                         for (int jj = 0; jj < nk; ++jj) {
                             // the issuer's first MMA of the unit starts its sum
-                            const bool first = st == un.st_lo + is && jj == 0;
+                            const bool first = st == un.st_lo + off && jj == 0;
                             const uint64_t bd =
                                 smem_desc_sw128(b_stage + static_cast<uint32_t>(jj) * b_bytes);
 #pragma unroll
@@ -601,6 +606,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int row_in_tile = quad * 32 + lane;
         int local = 0;
+        int sbase = 0;                            // ring use of the unit's first slot
         for (int u = cta0; u < num_units; u += ncta) {
             const Unit un = unit_of(u, p, n_st);
             const int4 t = p.tiles[un.tile];
@@ -643,11 +649,21 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                    static_cast<uint32_t>(buf) * acc_stride;
             const int n_mma = (t.z + 15) & ~15;
-            const int n_acc = min(n_iss, un.st_hi - un.st_lo);   // issuers that had ring slots
+            // issuers that had ring slots in this unit (MXFP4 issuer i takes
+            // the slots of use parity i)
+            const int nsl = un.st_hi - un.st_lo;
+            const bool has0 = n_iss == 1 || nsl > (sbase & 1);
+            const bool has1 = n_iss == 2 && nsl > ((1 ^ sbase) & 1);
+            sbase += nsl;
             // This part's accumulator, 16 token columns from c0 (both issuers added).
             auto load_acc = [&](int c0, float (&v)[16]) {
-                tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
-                if (n_acc > 1) {
+                if (has0) {
+                    tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                }
+                if (has1) {
                     float v2[16];
                     tmem_ld16(taddr + 2u * acc_stride + static_cast<uint32_t>(c0), v2);
 #pragma unroll

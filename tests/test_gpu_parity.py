@@ -264,6 +264,19 @@ def test_forward_ksplit(moe, oracle_lib, synth_lib, case):
     _check(moe, oracle_lib, L, tol=tol)
 
 
+@pytest.mark.parametrize("parts", [3, 8])
+def test_forward_fixed_ksplit(moe, oracle_lib, synth_lib, parts):
+    """The K split forced to 3 and 8 parts ("ksplit" 2..8), beside the
+    automatic choice the cases above use (gate_up takes as many parts as
+    the partial-tile region holds)."""
+    L = synth_lib.make_layer(E=8, T=3, H=1024, I=512, top_k=2, seed=733, router_w_std=0.05)
+    moe.moe_set_tuning("ksplit", parts)
+    try:
+        _check(moe, oracle_lib, L)
+    finally:
+        moe.moe_set_tuning("ksplit", 0)
+
+
 def test_ksplit_tickets_reset(moe, oracle_lib, synth_lib):
     """The gate_up part tickets are left at zero: the same workspace serves a
     second split call, and a call of another shape, with the same results."""
@@ -376,6 +389,22 @@ def test_mxfp4_dequant_is_exact(moe, oracle_lib, synth_lib, T, scale_lo, scale_h
     assert moe.moe_get_device_status(wsq) == 0
     assert torch.equal(iq, ib) and torch.equal(wq, wb)
     assert torch.equal(oq, ob)
+
+
+@pytest.mark.parametrize("ksplit", [1, 0])
+def test_mxfp4_odd_ring_slots_per_unit(moe, oracle_lib, synth_lib, ksplit):
+    """K = 640 is 10 k-blocks, 3 ring slots per unit (down: K = 320, 2
+    slots): consecutive units start at ring uses of both parities, and the
+    two MMA issuers must still each keep their own A slot.  ksplit 1 runs
+    whole units, 0 the automatic K split."""
+    from parity_util import TOL_MXFP4
+    L = synth_lib.make_layer(E=8, T=37, H=640, I=320, top_k=4, seed=640, wfmt="mxfp4",
+                             router_w_std=0.05)
+    moe.moe_set_tuning("ksplit", ksplit)
+    try:
+        _check(moe, oracle_lib, L, tol=TOL_MXFP4)
+    finally:
+        moe.moe_set_tuning("ksplit", 0)
 
 
 @pytest.fixture(scope="module")
