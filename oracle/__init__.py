@@ -65,6 +65,11 @@ def lib():
             L.oracle_e2m1.restype = f
             L.oracle_e8m0.argtypes = [ctypes.c_uint8]
             L.oracle_e8m0.restype = f
+            L.oracle_e4m3.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3.restype = f
+            L.oracle_e4m3_round.argtypes = [f]
+            L.oracle_e4m3_round.restype = ctypes.c_uint8
+            L.oracle_fp8_quantize_row.argtypes = [vp, i, vp, vp]
             L.oracle_router_logits.argtypes = [P, vp, i]
             L.oracle_topk_softmax.argtypes = [vp, i, i, i, vp, vp]
             L.oracle_permute.argtypes = [vp, i, i, i, vp, vp, vp]
@@ -87,7 +92,7 @@ def _ptr(t):
 def _layer_struct(layer):
     """Build the C struct from a synth.Layer (keeps the tensors alive)."""
     s = OracleLayer(layer.T, layer.H, layer.I, layer.E, layer.top_k,
-                    0 if layer.wfmt == "bf16" else 1,
+                    {"bf16": 0, "mxfp4": 1, "fp8": 2}[layer.wfmt],
                     _ptr(layer.x), _ptr(layer.wr), _ptr(layer.br),
                     _ptr(layer.w_gu), _ptr(layer.s_gu), _ptr(layer.b_gu),
                     _ptr(layer.w_d), _ptr(layer.s_d), _ptr(layer.b_d))
@@ -108,6 +113,25 @@ def e2m1(code: int) -> float:
 
 def e8m0(s: int) -> float:
     return lib().oracle_e8m0(s)
+
+
+def e4m3(code: int) -> float:
+    return lib().oracle_e4m3(code)
+
+
+def e4m3_round(v: float) -> int:
+    return lib().oracle_e4m3_round(v)
+
+
+def fp8_quantize_row(x: torch.Tensor):
+    """One token's bf16 activations -> (e4m3 codes uint8[n], scale)."""
+    x = x.contiguous()
+    assert x.dtype == torch.bfloat16 and x.dim() == 1
+    codes = torch.empty(x.numel(), dtype=torch.uint8)
+    scale = ctypes.c_float(0.0)
+    lib().oracle_fp8_quantize_row(x.data_ptr(), x.numel(), codes.data_ptr(),
+                                  ctypes.byref(scale))
+    return codes, scale.value
 
 
 def router_logits(layer, threads: int = 0) -> torch.Tensor:

@@ -25,7 +25,8 @@
 //     weighted_sum over the top-4 only; non-selected experts are skipped,
 //     not multiplied by zero.
 //   * §5 "量化" (quantization): MXFP4 = E2M1 values with one UE8M0 scale per
-//     32 elements.
+//     32 elements; FP8 W8A8 = E4M3 weights with one scalar scale per expert,
+//     E4M3 activations, the scales applied after the product.
 //
 // Readings where the page leaves a step open (each is listed in the design
 // notes of the repository):
@@ -42,6 +43,14 @@
 //     the high nibble; the 32-element scale blocks run along the input (K)
 //     dimension of each output row; value = e2m1(code) * 2^(scale - 127).
 //   * the permutation sorts assignments a = t*k + j by (expert, a) ascending.
+//   * FP8 W8A8: weight = e4m3(code) * scale[e] (one fp32 scale per expert and
+//     matrix); each token's activations are quantised with their own scale,
+//     s = max|x| / 448 (1 when the row is all zero): code = e4m3 nearest to
+//     x * (448 / max|x|), ties to the even code, magnitudes beyond 448
+//     saturating to 448; h is quantised with the fixed scale 1/8 (the GLU
+//     clamps keep h in [-42, 56), so h * 8 never exceeds 448).  A gate_up row
+//     is (sum_k e4m3(w) * e4m3(xq)) * (scale[e] * s) + bias; a down row is
+//     (sum_j e4m3(w) * e4m3(hq)) * (scale[e] * 1/8) + bias.
 //
 // Parity pins (tests/test_oracle_pins.py): brute force over all k-subsets,
 // closed-form special cases of top-k/softmax, permutation closed forms,
@@ -82,6 +91,46 @@ inline float e2m1_value(unsigned code) {
     return s ? -mag : mag;
 }
 
+// E4M3 (OCP FP8, "fn" variant): sign, 4 exponent bits (bias 7), 3 mantissa
+// bits; exponent field 0 holds the subnormals m * 2^-9; the all-ones code
+// (exponent 15, mantissa 7) is NaN; the largest finite magnitude is 448.
+inline float e4m3_value(uint8_t code) {
+    const unsigned s = code >> 7, ex = (code >> 3) & 0xFu, m = code & 7u;
+    if (ex == 15 && m == 7) return std::nanf("");
+    const float mag = (ex == 0) ? std::ldexp(static_cast<float>(m), -9)
+                                : std::ldexp(1.0f + static_cast<float>(m) / 8.0f,
+                                             static_cast<int>(ex) - 7);
+    return s ? -mag : mag;
+}
+
+// The e4m3 code nearest to v: a search over the 127 non-negative finite
+// codes (their values increase with the code), ties to the even code; a
+// magnitude beyond 448 gives 448 (saturation); the sign is kept.
+inline uint8_t e4m3_round(float v) {
+    if (std::isnan(v)) return 0x7F;
+    const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+    const float a = std::fabs(v);
+    int best = 0;
+    float best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const float d = std::fabs(e4m3_value(static_cast<uint8_t>(c)) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return static_cast<uint8_t>(sign | best);
+}
+
+// One token's activations to e4m3 with their own scale (FP8 W8A8 reading).
+inline float fp8_quantize_row(const uint16_t* x, int n, uint8_t* codes) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) amax = std::fmax(amax, std::fabs(bf16_value(x[i])));
+    const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
+    for (int i = 0; i < n; ++i) codes[i] = e4m3_round(bf16_value(x[i]) * inv);
+    return amax > 0.0f ? amax / 448.0f : 1.0f;
+}
+
 // UE8M0: an unsigned power-of-two exponent with bias 127.
 inline float e8m0_value(uint8_t s) {
     return std::ldexp(1.0f, static_cast<int>(s) - 127);
@@ -92,6 +141,9 @@ inline float weight_at(int wfmt, const void* w, const uint8_t* s, size_t row,
                        size_t col, size_t cols) {
     if (wfmt == 0) {
         return bf16_value(static_cast<const uint16_t*>(w)[row * cols + col]);
+    }
+    if (wfmt == 2) {   // FP8: the code's value; the expert scale comes later
+        return e4m3_value(static_cast<const uint8_t*>(w)[row * cols + col]);
     }
     const uint8_t* codes = static_cast<const uint8_t*>(w);
     uint8_t byte = codes[row * (cols / 2) + col / 2];
@@ -142,6 +194,44 @@ void topk_softmax_row(const float* logit, int E, int k, int32_t* ids,
     for (int j = 0; j < k; ++j) w[j] = ex[j] / denom;
 }
 
+// FP8 W8A8 form of expert_ffn (the readings above): quantised token row,
+// code products summed in fp32, then the scales, then the bias.
+void expert_ffn_fp8(const oracle_layer* L, int e, const uint16_t* xr, float* h_out,
+                    float* y_out) {
+    const int H = L->H, I = L->I;
+    const size_t n_gu = static_cast<size_t>(2) * I;
+    std::vector<uint8_t> xq(H);
+    const float xs = fp8_quantize_row(xr, H, xq.data());
+    std::vector<float> xv(H);
+    for (int k = 0; k < H; ++k) xv[k] = e4m3_value(xq[k]);
+    const float* sw_gu = static_cast<const float*>(L->s_gu);
+    const float* sw_d = static_cast<const float*>(L->s_d);
+    const float gu_scale = sw_gu[e] * xs;
+    const size_t gu_row0 = static_cast<size_t>(e) * n_gu;
+    std::vector<float> gu(n_gu);
+    for (size_t n = 0; n < n_gu; ++n) {
+        float acc = 0.0f;
+        for (int k = 0; k < H; ++k)
+            acc += weight_at(2, L->w_gu, nullptr, gu_row0 + n, k, H) * xv[k];
+        gu[n] = acc * gu_scale + bf16_value(L->b_gu[gu_row0 + n]);
+    }
+    std::vector<float> h(I), hv(I);
+    for (int j = 0; j < I; ++j) {
+        const float gate = gu[2 * j], up = gu[2 * j + 1];
+        h[j] = glu(gate, up);
+        hv[j] = e4m3_value(e4m3_round(h[j] * 8.0f));
+    }
+    if (h_out) std::memcpy(h_out, h.data(), sizeof(float) * I);
+    const float d_scale = sw_d[e] * 0.125f;
+    const size_t d_row0 = static_cast<size_t>(e) * H;
+    for (int n = 0; n < H; ++n) {
+        float acc = 0.0f;
+        for (int j = 0; j < I; ++j)
+            acc += weight_at(2, L->w_d, nullptr, d_row0 + n, j, I) * hv[j];
+        y_out[n] = acc * d_scale + bf16_value(L->b_d[d_row0 + n]);
+    }
+}
+
 // One expert applied to one token: gate_up + bias -> GLU -> down + bias.
 // h_out may be null; y_out receives H values.
 void expert_ffn(const oracle_layer* L, int e, int t, float* h_out,
@@ -151,10 +241,14 @@ void expert_ffn(const oracle_layer* L, int e, int t, float* h_out,
     const uint16_t* xr = L->x + static_cast<size_t>(t) * H;
     std::vector<float> xf(H);
     for (int k = 0; k < H; ++k) xf[k] = bf16_value(xr[k]);
+    if (L->wfmt == 2) {
+        expert_ffn_fp8(L, e, xr, h_out, y_out);
+        return;
+    }
 
     // gate_up rows of expert e, then the per-pair GLU.
     const size_t gu_row0 = static_cast<size_t>(e) * n_gu;
-    const uint8_t* s_gu = L->s_gu;
+    const uint8_t* s_gu = static_cast<const uint8_t*>(L->s_gu);
     std::vector<float> gu(n_gu);
     for (size_t n = 0; n < n_gu; ++n) {
         float acc = 0.0f;
@@ -167,11 +261,12 @@ void expert_ffn(const oracle_layer* L, int e, int t, float* h_out,
     if (h_out) std::memcpy(h_out, h.data(), sizeof(float) * I);
 
     // down rows of expert e.
+    const uint8_t* s_d = static_cast<const uint8_t*>(L->s_d);
     const size_t d_row0 = static_cast<size_t>(e) * H;
     for (int n = 0; n < H; ++n) {
         float acc = 0.0f;
         for (int j = 0; j < I; ++j)
-            acc += weight_at(L->wfmt, L->w_d, L->s_d, d_row0 + n, j, I) * h[j];
+            acc += weight_at(L->wfmt, L->w_d, s_d, d_row0 + n, j, I) * h[j];
         y_out[n] = acc + bf16_value(L->b_d[d_row0 + n]);
     }
 }
@@ -201,6 +296,17 @@ float oracle_glu(float gate, float up) { return glu(gate, up); }
 float oracle_e2m1(unsigned code) { return e2m1_value(code & 0xFu); }
 
 float oracle_e8m0(uint8_t s) { return e8m0_value(s); }
+
+float oracle_e4m3(uint8_t code) { return e4m3_value(code); }
+
+uint8_t oracle_e4m3_round(float v) { return e4m3_round(v); }
+
+// One token row of n bf16 activations to e4m3 codes; *scale receives its
+// scale (max|x| / 448, or 1 for an all-zero row).
+int oracle_fp8_quantize_row(const uint16_t* x, int n, uint8_t* codes, float* scale) {
+    *scale = fp8_quantize_row(x, n, codes);
+    return 0;
+}
 
 // logits[T, E] (fp32).
 int oracle_router_logits(const oracle_layer* L, float* logits, int threads) {

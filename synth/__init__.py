@@ -17,6 +17,12 @@ the 120b-shaped layer keeps the same widths with 128 experts):
 * MXFP4: e2m1 codes uniform over the 16 nibble values, two per byte, and one
   E8M0 scale byte per 32 consecutive input elements with exponent uniform in
   [-8, -4] (bytes 119..123).
+* FP8 (W8A8 weights): e4m3 codes drawn field by field -- sign uniform,
+  exponent field uniform in [5, 9] (magnitudes 0.25 .. 7.5), mantissa
+  uniform over its 8 values -- and one fp32 scale per expert and matrix,
+  w_std / 3 times a factor uniform in [0.75, 1.25], so that the weights'
+  spread matches the bf16 recipe.  Activations stay bf16 here; the layer
+  quantises them itself.
 """
 from __future__ import annotations
 
@@ -37,6 +43,9 @@ _lib = None
 # Stream ids: one independent random stream per tensor.
 S_X, S_WR, S_BR, S_WGU, S_BGU, S_WD, S_BD = 1, 2, 3, 4, 5, 6, 7
 S_GU_CODES, S_GU_SCALES, S_D_CODES, S_D_SCALES = 8, 9, 10, 11
+# FP8 code fields (sign, exponent, mantissa) and per-expert scales
+S_F8_GU_SIGN, S_F8_GU_EXP, S_F8_GU_MAN, S_F8_GU_SCALE = 12, 13, 14, 15
+S_F8_D_SIGN, S_F8_D_EXP, S_F8_D_MAN, S_F8_D_SCALE = 16, 17, 18, 19
 
 
 def build(force: bool = False) -> str:
@@ -114,17 +123,36 @@ class Layer:
     I: int
     E: int
     top_k: int
-    wfmt: str                      # "bf16" or "mxfp4"
+    wfmt: str                      # "bf16", "mxfp4" or "fp8"
     x: torch.Tensor                # [T, H] bf16
     wr: torch.Tensor               # [E, H] bf16
     br: torch.Tensor               # [E] bf16
-    w_gu: torch.Tensor             # [E, 2I, H] bf16 | [E, 2I, H/2] u8
+    w_gu: torch.Tensor             # [E, 2I, H] bf16 | [E, 2I, H/2] u8 | [E, 2I, H] u8 e4m3
     b_gu: torch.Tensor             # [E, 2I] bf16
-    w_d: torch.Tensor              # [E, H, I] bf16 | [E, H, I/2] u8
+    w_d: torch.Tensor              # [E, H, I] bf16 | [E, H, I/2] u8 | [E, H, I] u8 e4m3
     b_d: torch.Tensor              # [E, H] bf16
-    s_gu: Optional[torch.Tensor] = None   # [E, 2I, H/32] u8 (mxfp4)
-    s_d: Optional[torch.Tensor] = None    # [E, H, I/32] u8 (mxfp4)
+    s_gu: Optional[torch.Tensor] = None   # [E, 2I, H/32] u8 (mxfp4) | [E] fp32 (fp8)
+    s_d: Optional[torch.Tensor] = None    # [E, H, I/32] u8 (mxfp4) | [E] fp32 (fp8)
     meta: dict = field(default_factory=dict)
+
+
+def fp8_codes(shape, seed, streams, exp_lo=5, exp_hi=9, pin=False) -> torch.Tensor:
+    """e4m3 bytes: sign, exponent field and mantissa drawn independently
+    (the exponent range keeps clear of the NaN code 0x7F/0xFF)."""
+    sign = uniform_u8(shape, seed, streams[0], 0, 1)
+    ex = uniform_u8(shape, seed, streams[1], exp_lo, exp_hi)
+    man = uniform_u8(shape, seed, streams[2], 0, 7)
+    out = _empty(shape, torch.uint8, pin)
+    out.copy_((sign << 7) | (ex << 3) | man)
+    return out
+
+
+def fp8_expert_scales(E, seed, stream, w_std, pin=False) -> torch.Tensor:
+    """One fp32 scale per expert: w_std / 3 times a factor in [0.75, 1.25]."""
+    u = uniform_u8((E,), seed, stream, 0, 255).to(torch.float32)
+    out = _empty((E,), torch.float32, pin)
+    out.copy_((w_std / 3.0) * (0.75 + 0.5 * u / 255.0))
+    return out
 
 
 def make_x(T, H, seed, p_outlier=0.0, outlier_scale=20.0, pin=False):
@@ -141,7 +169,7 @@ def make_layer(E: int, T: int, H: int = 2880, I: int = 2880, top_k: int = 4,
                router_w_std: Optional[float] = None,
                scale_lo: int = 119, scale_hi: int = 123,
                pin: bool = False, with_experts: bool = True) -> Layer:
-    if wfmt not in ("bf16", "mxfp4"):
+    if wfmt not in ("bf16", "mxfp4", "fp8"):
         raise ValueError(f"unknown weight format {wfmt!r}")
     rws = w_std if router_w_std is None else router_w_std
     x = make_x(T, H, seed, p_outlier, outlier_scale, pin)
@@ -160,6 +188,11 @@ def make_layer(E: int, T: int, H: int = 2880, I: int = 2880, top_k: int = 4,
     elif wfmt == "bf16":
         w_gu = normal_bf16((E, 2 * I, H), seed, S_WGU, 0.0, w_std, pin=pin)
         w_d = normal_bf16((E, H, I), seed, S_WD, 0.0, w_std, pin=pin)
+    elif wfmt == "fp8":
+        w_gu = fp8_codes((E, 2 * I, H), seed, (S_F8_GU_SIGN, S_F8_GU_EXP, S_F8_GU_MAN), pin=pin)
+        s_gu = fp8_expert_scales(E, seed, S_F8_GU_SCALE, w_std, pin)
+        w_d = fp8_codes((E, H, I), seed, (S_F8_D_SIGN, S_F8_D_EXP, S_F8_D_MAN), pin=pin)
+        s_d = fp8_expert_scales(E, seed, S_F8_D_SCALE, w_std, pin)
     else:
         if H % 32 or I % 32:
             raise ValueError("MXFP4 needs H and I multiples of 32")
@@ -187,6 +220,8 @@ WORKLOADS = {
     "120b_shape": dict(E=128, seed=3, Ts=(1, 8, 64, 512, 4096, 8192),
                        wfmt="bf16"),
     "20b_mxfp4": dict(E=32, seed=4, Ts=(1, 64, 512), wfmt="mxfp4"),
+    # FP8 W8A8 (the pages' quantised serving path, next after the five above)
+    "20b_fp8": dict(E=32, seed=5, Ts=(1, 64, 512, 4096), wfmt="fp8"),
 }
 
 

@@ -26,13 +26,21 @@ MUTATIONS = {
     "gate_lower_clamp_added": ("if (gate > 7.0f) gate = 7.0f;",
                                "if (gate > 7.0f) gate = 7.0f; if (gate < -7.0f) gate = -7.0f;"),
     "up_plus_one_dropped": ("return (up + 1.0f) * g;", "return up * g;"),
-    "down_transposed": ("weight_at(L->wfmt, L->w_d, L->s_d, d_row0 + n, j, I)",
-                        "weight_at(L->wfmt, L->w_d, L->s_d, d_row0 + j, n, I)"),
+    "down_transposed": ("weight_at(L->wfmt, L->w_d, s_d, d_row0 + n, j, I)",
+                        "weight_at(L->wfmt, L->w_d, s_d, d_row0 + j, n, I)"),
     "combine_weight_dropped": ("acc += w[static_cast<size_t>(p) * k + j] *\n                       y[",
                                "acc += 1.0f *\n                       y["),
     "router_bias_dropped": ("return acc + bf16_value(L->br[e]);", "return acc;"),
     "nibble_order_swapped": ("(col & 1) ? (byte >> 4) : (byte & 0xFu)",
                              "(col & 1) ? (byte & 0xFu) : (byte >> 4)"),
+    "fp8_act_scale_wrong": ("const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;",
+                            "const float inv = amax > 0.0f ? 240.0f / amax : 1.0f;"),
+    "fp8_h_scale_wrong": ("hv[j] = e4m3_value(e4m3_round(h[j] * 8.0f));",
+                          "hv[j] = e4m3_value(e4m3_round(h[j] * 4.0f));"),
+    "fp8_ties_to_odd": ("(d == best_d && (c & 1) == 0)", "(d == best_d && (c & 1) == 1)"),
+    "fp8_no_saturation": ("for (int c = 0; c <= 0x7E; ++c) {", "for (int c = 0; c <= 0x7D; ++c) {"),
+    "fp8_weight_scale_twice": ("const float gu_scale = sw_gu[e] * xs;",
+                               "const float gu_scale = sw_gu[e] * sw_gu[e] * xs;"),
     "scale_bias_off_by_one": ("static_cast<int>(s) - 127", "static_cast<int>(s) - 128"),
     "softmax_over_all_experts": ("    for (int j = 0; j < k; ++j) w[j] = ex[j] / denom;",
                                  "    for (int e = 0; e < E; ++e) if (!taken[e]) denom += std::exp(logit[e] - m);\n"

@@ -372,3 +372,121 @@ def test_mxfp4_layer_equals_bf16_layer_on_dequantised_weights(oracle_lib, synth_
     Lb.w_d = wd.to(torch.bfloat16).contiguous()
     a, b = oracle_lib.forward(Lq), oracle_lib.forward(Lb)
     assert all(torch.equal(p, q) for p, q in zip(a, b))
+
+
+# --------------------------------------------------------------------------
+# FP8 W8A8 (E4M3 weights with per-expert scales, per-token E4M3 activations)
+
+
+def _torch_e4m3_codes(v: torch.Tensor) -> torch.Tensor:
+    """Library rounding to e4m3 (round to nearest even; NaN past 464)."""
+    return v.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def test_e4m3_decode_matches_library_for_all_codes():
+    import oracle
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float32)
+    for c in range(256):
+        v = oracle.e4m3(c)
+        if c in (0x7F, 0xFF):
+            assert v != v                          # NaN
+        else:
+            assert v == ref[c].item(), hex(c)
+    # the format's landmarks
+    assert oracle.e4m3(0x7E) == 448.0 and oracle.e4m3(0x01) == 2.0 ** -9
+    assert oracle.e4m3(0x08) == 2.0 ** -6 and oracle.e4m3(0x38) == 1.0
+
+
+def test_e4m3_rounding_matches_library_within_range():
+    import oracle
+    g = torch.Generator().manual_seed(8)
+    # magnitudes from the subnormal range to 464, both signs
+    mag = torch.exp2(torch.rand(4000, generator=g) * 18.0 - 12.0).clamp(max=464.0)
+    sgn = torch.where(torch.rand(4000, generator=g) < 0.5, -1.0, 1.0)
+    vals = (mag * sgn).to(torch.float32)
+    # plus every midpoint between adjacent codes (ties go to the even code)
+    pos = torch.tensor([oracle.e4m3(c) for c in range(0x7F)], dtype=torch.float64)
+    mids = ((pos[:-1] + pos[1:]) / 2).to(torch.float32)
+    vals = torch.cat([vals, mids, -mids])
+    ref = _torch_e4m3_codes(vals)
+    got = torch.tensor([oracle.e4m3_round(v) for v in vals.tolist()], dtype=torch.uint8)
+    assert torch.equal(got, ref)
+
+
+def test_e4m3_rounding_saturates_beyond_448():
+    import oracle
+    for v in (464.0, 470.0, 480.0, 1.0e4, 3.0e38):
+        assert oracle.e4m3_round(v) == 0x7E and oracle.e4m3_round(-v) == 0xFE
+
+
+def test_fp8_row_quantisation_rules(oracle_lib):
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randn(200, generator=g) * 3).to(torch.bfloat16)
+    x[17] = -25.0                                   # the row's largest magnitude
+    codes, scale = oracle_lib.fp8_quantize_row(x)
+    xf = x.float()
+    amax = xf.abs().max()
+    assert scale == (amax / 448.0).item()
+    assert codes[17].item() == 0xFE                 # -448 exactly
+    # every code is the library rounding of x * (448 / max|x|)
+    assert torch.equal(codes, _torch_e4m3_codes(xf * (448.0 / amax)))
+    zero_codes, zero_scale = oracle_lib.fp8_quantize_row(torch.zeros(8, dtype=torch.bfloat16))
+    assert zero_scale == 1.0 and zero_codes.eq(0).all()
+
+
+def _fp64_fp8_layer(L):
+    """Independent fp64 brute force of the FP8 W8A8 layer: e4m3 decoding and
+    rounding by the library, scales applied after the product."""
+    dec = lambda c: c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    x = L.x.float()
+    wr, br = L.wr.float().double().numpy(), L.br.float().double().numpy()
+    logits = x.double().numpy() @ wr.T + br
+    wgu, wd = dec(L.w_gu), dec(L.w_d)
+    sgu, sd = L.s_gu.double().numpy(), L.s_d.double().numpy()
+    bgu, bd = L.b_gu.float().double().numpy(), L.b_d.float().double().numpy()
+    out = np.zeros((L.T, L.H))
+    sels = []
+    for t in range(L.T):
+        order = sorted(range(L.E), key=lambda e: (-logits[t, e], e))
+        sel = order[: L.top_k]
+        z = np.exp(logits[t, sel] - logits[t, sel[0]])
+        w = z / z.sum()
+        amax = x[t].abs().max()
+        xq = dec(_torch_e4m3_codes(x[t] * (448.0 / amax)))
+        xs = float(amax) / 448.0
+        for j, e in enumerate(sel):
+            gu = (wgu[e] @ xq) * (sgu[e] * xs) + bgu[e]
+            gate, up = np.minimum(gu[0::2], 7.0), np.clip(gu[1::2], -7.0, 7.0)
+            h = (up + 1.0) * gate / (1.0 + np.exp(-1.702 * gate))
+            hq = dec(_torch_e4m3_codes(torch.from_numpy(h * 8.0)))
+            out[t] += w[j] * ((wd[e] @ hq) * (sd[e] * 0.125) + bd[e])
+        sels.append(sel)
+    return sels, out
+
+
+def test_fp8_layer_matches_fp64_brute_force(oracle_lib, synth_lib):
+    L = synth_lib.make_layer(E=4, T=6, H=64, I=64, top_k=2, seed=31, wfmt="fp8",
+                             router_w_std=0.3)
+    sels, ref = _fp64_fp8_layer(L)
+    ids, w, out = oracle_lib.forward(L)
+    assert ids.tolist() == sels
+    # fp32 vs fp64 sums can move an h value across an e4m3 rounding boundary;
+    # one such flip changes an output by ~|w_d| * |h| / 16
+    err = np.abs(out.double().numpy() - ref).max()
+    assert err <= 2e-3 * np.abs(ref).max()
+
+
+def test_fp8_scales_apply_after_the_product(oracle_lib, synth_lib):
+    """The expert scale multiplies the finished sum: with zero biases,
+    doubling one expert's down scale doubles its output exactly (a power-of-
+    two factor applied to an fp32 sum), and h does not change."""
+    L = synth_lib.make_layer(E=2, T=2, H=64, I=64, top_k=1, seed=5, wfmt="fp8")
+    L.b_gu = torch.zeros_like(L.b_gu)
+    L.b_d = torch.zeros_like(L.b_d)
+    h1, y1 = oracle_lib.expert_ffn(L, 1, 0)
+    L.s_d = L.s_d.clone()
+    L.s_d[1] *= 2.0
+    h2, y2 = oracle_lib.expert_ffn(L, 1, 0)
+    assert torch.equal(h1, h2)
+    assert torch.equal(y2, 2.0 * y1) and y1.abs().max() > 0
