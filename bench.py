@@ -40,6 +40,9 @@ GU_BYTES = lambda H, I: 2 * I * H * 2 + 2 * I * 2          # noqa: E731
 D_BYTES = lambda H, I: H * I * 2 + H * 2                    # noqa: E731
 GU_BYTES_MXFP4 = lambda H, I: 2 * I * H // 2 + 2 * I * H // 32 + 2 * I * 2  # noqa: E731
 D_BYTES_MXFP4 = lambda H, I: H * I // 2 + H * I // 32 + H * 2               # noqa: E731
+# FP8 W8A8: one E4M3 byte per weight, the bf16 biases and one fp32 scale
+GU_BYTES_FP8 = lambda H, I: 2 * I * H + 2 * I * 2 + 4                   # noqa: E731
+D_BYTES_FP8 = lambda H, I: H * I + H * 2 + 4                            # noqa: E731
 
 DESCRIPTIONS = {
     "20b_t8": "gpt-oss-20b MoE layer, T={T}, bf16, seed 0",
@@ -49,6 +52,7 @@ DESCRIPTIONS = {
     "120b_shape": "gpt-oss-120b-shaped MoE layer (128 experts top-4), T={T}, bf16, "
                   "near-uniform routing, seed 3",
     "20b_mxfp4": "gpt-oss-20b MoE layer, MXFP4 expert weights, T={T}, seed 4",
+    "20b_fp8": "gpt-oss-20b MoE layer, FP8 W8A8 (E4M3 weights, per-expert scales; per-token E4M3 activations), T={T}, seed 5",
 }
 
 
@@ -203,7 +207,8 @@ def base_record(args, n_gpus, workload_desc, layer):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if layer.wfmt == "bf16" else "mxfp4-weights/bf16-activations",
+        "dtype": {"bf16": "bf16", "mxfp4": "mxfp4-weights/bf16-activations",
+                  "fp8": "e4m3-weights/e4m3-activations"}[layer.wfmt],
         "data": "synthetic: seeded gpt-oss-shaped layer, random-init weights (no checkpoint)",
         "config": {"workload": workload_desc, "T": layer.T, "H": layer.H, "I": layer.I,
                    "E": layer.E, "top_k": layer.top_k, "weights": layer.wfmt,
@@ -367,9 +372,18 @@ def main():
     R = T * k
     if layer.wfmt == "bf16":
         gu_b, d_b = GU_BYTES(H, I), D_BYTES(H, I)
+    elif layer.wfmt == "fp8":
+        gu_b, d_b = GU_BYTES_FP8(H, I), D_BYTES_FP8(H, I)
     else:
         gu_b, d_b = GU_BYTES_MXFP4(H, I), D_BYTES_MXFP4(H, I)
-    gu_alg = U * gu_b + R * H * 2 + R * I * 2
+    # activation and h bytes per element: E4M3 codes for FP8 W8A8, else bf16
+    ab = 1 if layer.wfmt == "fp8" else 2
+    gu_alg = U * gu_b + R * H * ab + R * I * ab
+    if layer.wfmt == "fp8":
+        # an E4M3 contraction's peak: the measured bf16 rate x the nominal
+        # dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+        tf_burst, tf_sust = 2.0 * tf_burst, 2.0 * tf_sust
+        peak_kind += ", x2 nominal fp8/bf16 ratio"
     gu_ms = kmap.get("gate_up_glu")
     flops_tok = 2 * (2 * I) * H + 2 * H * I
     gu_flops = R * 2 * (2 * I) * H

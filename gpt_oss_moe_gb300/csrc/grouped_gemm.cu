@@ -241,6 +241,9 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                         const __grid_constant__ CUtensorMap tmap_x) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int KPS = kKbPerStage<WF>;
+    // K elements per k-block (one 128-byte swizzled row of an operand tile):
+    // 64 bf16, or 128 E4M3 codes (WF = 2)
+    constexpr int kKB = WF == 2 ? kBlockKFp8 : kBlockK;
     const int stages = p.stages, astages = p.astages, box = p.token_box;
     // CTA pair (CG = 2, bf16 weights): the cluster's two CTAs share each unit
     // of 256 weight rows; CTA r loads rows 128r.. of the block and half of
@@ -390,15 +393,15 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                         const uint32_t fb0 = mapa_shared(fb, 0);
                         const int half_n = ((t.z + 15) & ~15) / 2;
                         tma_load_3d_pair(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
-                                         &tmap_w, fb0, st * kBlockK,
+                                         &tmap_w, fb0, st * kKB,
                                          mb * kUnitRows + static_cast<int>(rank) * kWeightTileRows,
                                          t.x, pol_w);
-                        tma_load_2d_pair(b_dst, &tmap_x, fb0, st * kBlockK,
+                        tma_load_2d_pair(b_dst, &tmap_x, fb0, st * kKB,
                                          t.y + static_cast<int>(rank) * half_n, pol_x);
                     } else {
                         tma_load_3d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
-                                    &tmap_w, fb, st * kBlockK, mb * kWeightTileRows, t.x, pol_w);
-                        tma_load_2d(b_dst, &tmap_x, fb, st * kBlockK, t.y, pol_x);
+                                    &tmap_w, fb, st * kKB, mb * kWeightTileRows, t.x, pol_w);
+                        tma_load_2d(b_dst, &tmap_x, fb, st * kKB, t.y, pol_x);
                     }
                     ++issued;
                     if (++stage == stages) {
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 }
             }
         }
-    } else if (WF == 0 && warp == 1) {
+    } else if (WF != 1 && warp == 1) {
         // ------------------------------------------------ MMA issuer (bf16)
         // The whole warp walks the loop, so the barrier waits and the
         // descriptors are warp-uniform, and one elected lane issues the MMAs
@@ -446,7 +449,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
                 const uint32_t n_mma = static_cast<uint32_t>((t.z + 15) & ~15);
-                const uint32_t idesc = idesc_bf16_f32(kUnitRows, n_mma);
+                const uint32_t idesc = WF == 2 ? idesc_e4m3_f32(kUnitRows, n_mma)
+                                               : idesc_bf16_f32(kUnitRows, n_mma);
                 const int buf = local & 1;
                 const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
                 ++local;
@@ -475,8 +479,11 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
 #pragma unroll
                         for (int kk = 0; kk < kBlockK / 16; ++kk) {
                             const uint32_t acc = kk == 0 ? acc0 : 1u;
+                            // one MMA per 32 bytes of K (16 bf16, 32 E4M3)
                             if constexpr (kPair)
                                 tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
+                            else if constexpr (WF == 2)
+                                tc_mma_e4m3(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
                             else
                                 tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
                         }
@@ -626,6 +633,10 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     sm.meta_tok[c] = a / p.top_k;
                     sm.meta_w[c] = p.topk_w[a];
                 }
+            } else if (WF == 2) {
+                // FP8 gate_up: the activation scale of each routed row
+                named_bar_sync(1, kEpiThreads);   // previous unit done with meta
+                for (int c = ep; c < t.z; c += kEpiThreads) sm.meta_w[c] = p.xscale[t.y + c];
             }
             // One thread waits; the decision is broadcast so all 128 agree.
             // The slot alternates so it is never rewritten before every
@@ -646,6 +657,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 row_ok && (EPI == kEpiGlu || un.split == 0)
                     ? __bfloat162float(p.bias[static_cast<size_t>(t.x) * p.w_rows + wrow])
                     : 0.f;
+            // FP8: the expert's weight scale (applied to the finished sum)
+            const float wsc = WF == 2 ? p.wscale[t.x] : 1.f;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                    static_cast<uint32_t>(buf) * acc_stride;
             const int n_mma = (t.z + 15) & ~15;
@@ -684,8 +697,16 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                                   (hcol & 63)
                             : p.h + static_cast<size_t>(t.y) * hcols + hcol;
                 const size_t hstride = WF == 1 ? 64 : static_cast<size_t>(hcols);
+                // FP8: h as E4M3 codes of h / kFp8HScale, [T*k, I] bytes
+                uint8_t* h8row0 = p.h8 + static_cast<size_t>(t.y) * hcols + hcol;
+                if (WF == 2) {
+                    // the sum of code products times weight scale x row scale
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] += bias;
+                    for (int i = 0; i < 16; ++i) v[i] = v[i] * (wsc * sm.meta_w[c0 + i]) + bias;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += bias;
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float send = odd ? v[i] : v[8 + i];
@@ -695,9 +716,14 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     const int c = c0 + i + (odd ? 8 : 0);
                     // rows past 2I exist only in the last 256-row block of
                     // CTA pairs (gate and up rows share their validity)
-                    if (c < t.z && row_ok)
-                        hrow0[static_cast<size_t>(c) * hstride] =
-                            __float2bfloat16_rn(clamped_glu(gate, up));
+                    if (c < t.z && row_ok) {
+                        if (WF == 2)
+                            h8row0[static_cast<size_t>(c) * hcols] = static_cast<uint8_t>(
+                                cvt_e4m3x2(clamped_glu(gate, up) * (1.f / kFp8HScale), 0.f));
+                        else
+                            hrow0[static_cast<size_t>(c) * hstride] =
+                                __float2bfloat16_rn(clamped_glu(gate, up));
+                    }
                 }
             };
 
@@ -754,8 +780,15 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 if (EPI == kEpiGlu) {
                     glu_store(c0, v);
                 } else {
+                    if (WF == 2) {
+                        // FP8 down: weight scale x the h codes' scale
+                        const float dsc = wsc * p.hscale;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] += bias;
+                        for (int i = 0; i < 16; ++i) v[i] = v[i] * dsc + bias;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] += bias;
+                    }
                     if (row_ok) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -990,6 +1023,10 @@ cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUte
                    ? launch_gemm_t<kEpiGlu, 0, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl)
                    : launch_gemm_t<kEpiCombine, 0, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl);
     }
+    if (wf == 2)
+        return epi == kEpiGlu
+                   ? launch_gemm_t<kEpiGlu, 2, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
+                   : launch_gemm_t<kEpiCombine, 2, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl);
     if (epi == kEpiGlu)
         return wf == 1 ? launch_gemm_t<kEpiGlu, 1, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
                        : launch_gemm_t<kEpiGlu, 0, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl);

@@ -86,7 +86,17 @@ moe_status make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_
 // 3-D map over one expert weight bank [E, rows, K]: bf16 values (box 64 K
 // elements x 128 rows x 1 expert) or MXFP4 codes (K/2 bytes per row; box
 // 128 bytes = kMxfp4KbPerStage k-blocks x 128 rows x 1 expert).
-moe_status weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K, bool mxfp4) {
+moe_status weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K, bool mxfp4,
+                       bool fp8 = false) {
+    if (fp8) {
+        // E4M3 codes [E, rows, K], one byte each: box 128 K x 128 rows
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
+                                    static_cast<cuuint64_t>(E)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(K),
+                                   static_cast<cuuint64_t>(K) * static_cast<cuuint64_t>(rows)};
+        const cuuint32_t boxd[3] = {static_cast<cuuint32_t>(kBlockKFp8), 128u, 1u};
+        return make_tmap(m, w, 3, dims, str, boxd, true);
+    }
     const cuuint64_t row_bytes = mxfp4 ? static_cast<cuuint64_t>(K) / 2
                                        : static_cast<cuuint64_t>(K) * 2;
     const cuuint64_t dims[3] = {mxfp4 ? static_cast<cuuint64_t>(K) / 2 : static_cast<cuuint64_t>(K),
@@ -155,7 +165,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 moe_status check_shape(const moe_shape* s) {
     if (!s) return MOE_ERR_ARG;
-    if (s->wfmt != MOE_W_BF16 && s->wfmt != MOE_W_MXFP4) return MOE_ERR_ARG;
+    if (s->wfmt != MOE_W_BF16 && s->wfmt != MOE_W_MXFP4 && s->wfmt != MOE_W_FP8) return MOE_ERR_ARG;
     if (s->T < 0 || s->T > (1 << 20)) return MOE_ERR_SHAPE;
     if (s->H <= 0 || s->H % 64 || s->H > 32768) return MOE_ERR_SHAPE;
     if (s->I <= 0 || s->I % 64 || s->I > 32768) return MOE_ERR_SHAPE;
@@ -303,6 +313,8 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     pp.assign_row = reinterpret_cast<int32_t*>(ws + L.assign_row);
     pp.x_perm = x_perm;
     pp.mx_layout = s.wfmt == MOE_W_MXFP4 ? 1 : 0;
+    pp.fp8 = s.wfmt == MOE_W_FP8 ? 1 : 0;
+    pp.x_scale = reinterpret_cast<float*>(ws + L.x_scale);
     pp.status = status;
     MOE_CUDA(launch_permute(pp, stream, g_pdl.load() != 0));
     prof_mark(x_perm ? "permute_gather" : "permute", stream);
@@ -372,7 +384,8 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     MOE_TRY(check_ptr(out));
     MOE_TRY(check_ptr(workspace));
     const bool mxfp4 = s.wfmt == MOE_W_MXFP4;
-    if (mxfp4) {
+    const bool fp8 = s.wfmt == MOE_W_FP8;
+    if (mxfp4 || fp8) {
         MOE_TRY(check_ptr(gate_up.scale));
         MOE_TRY(check_ptr(down.scale));
     }
@@ -393,10 +406,11 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     // loading 128 weight rows and half of the token tile, so a ring slot
     // holds 32 KB instead of 48 KB (box 256) for the same tensor work.
     const int pair_mode = g_pair_mode.load();
-    const bool pair = !mxfp4 && (pair_mode == 2 || (pair_mode == 0 && box >= kPairMinBox));
+    const bool pair = !mxfp4 && !fp8 &&
+                      (pair_mode == 2 || (pair_mode == 0 && box >= kPairMinBox));
     const int bbox = pair ? box / 2 : box;     // token rows of one CTA's B tile
     // Pipeline depth: as many stages as the shared memory allows (2..12).
-    const int wf = mxfp4 ? 1 : 0;
+    const int wf = mxfp4 ? 1 : fp8 ? 2 : 0;
     const int kscale_max = (s.H > s.I ? s.H : s.I) / 32;
     const size_t stage_bytes = gemm_stage_bytes(bbox, wf);
     const size_t budget = static_cast<size_t>(dev.max_smem) - 1024;
@@ -434,8 +448,8 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
 
     // Tensor maps (host-side descriptors; cheap to build per call).
     CUtensorMap tm_wgu, tm_x, tm_wd, tm_h;
-    MOE_TRY(weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H, mxfp4));
-    MOE_TRY(weight_tmap(&tm_wd, down.w, s.E, s.H, s.I, mxfp4));
+    MOE_TRY(weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H, mxfp4, fp8));
+    MOE_TRY(weight_tmap(&tm_wd, down.w, s.E, s.H, s.I, mxfp4, fp8));
     // Token operands: bf16 layers read [R, K] row-major, one 64-wide K chunk
     // per box; MXFP4 layers read the chunk-major [K/64, R, 64] layout the
     // gather and the GLU epilogue write, kMxfp4KbPerStage chunks per box.
@@ -446,6 +460,14 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
             const cuuint64_t str[2] = {128, static_cast<cuuint64_t>(R) * 128};
             const cuuint32_t boxd[3] = {64, static_cast<cuuint32_t>(box), kMxfp4KbPerStage};
             return make_tmap(m, base, 3, dims, str, boxd);
+        }
+        if (fp8) {
+            // E4M3 codes [R, K], one byte each: box 128 K x box rows
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(R)};
+            const cuuint64_t str[1] = {static_cast<cuuint64_t>(K)};
+            const cuuint32_t boxd[2] = {static_cast<cuuint32_t>(kBlockKFp8),
+                                        static_cast<cuuint32_t>(bbox)};
+            return make_tmap(m, base, 2, dims, str, boxd, true);
         }
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(R)};
         const cuuint64_t str[1] = {static_cast<cuuint64_t>(K) * 2};
@@ -483,11 +505,17 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
 
     // gate_up + bias + GLU -> h
     g.n_wblocks = (2 * s.I + unit_rows - 1) / unit_rows;
-    g.k_blocks = s.H / kBlockK;
+    // k-blocks of 64 bf16 / E4M3: 128 (a K tail past the last full block is
+    // zero-filled by TMA)
+    g.k_blocks = fp8 ? (s.H + kBlockKFp8 - 1) / kBlockKFp8 : s.H / kBlockK;
     g.w_rows = 2 * s.I;
     g.bias = static_cast<const __nv_bfloat16*>(gate_up.bias);
     g.h = h;
     g.scales = static_cast<const uint8_t*>(gate_up.scale);
+    g.wscale = fp8 ? static_cast<const float*>(gate_up.scale) : nullptr;
+    g.xscale = reinterpret_cast<const float*>(ws + L.x_scale);
+    g.h8 = reinterpret_cast<uint8_t*>(h);
+    g.hscale = kFp8HScale;
     g.kscale = s.H / 32;
     // K split when the units cannot fill two waves (small batches)
     const int kb_per_slot = mxfp4 ? kMxfp4KbPerStage : 1;
@@ -532,7 +560,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
 
     // down + bias + weighted combine -> out (fp32 accumulation)
     g.n_wblocks = (s.H + unit_rows - 1) / unit_rows;
-    g.k_blocks = s.I / kBlockK;
+    g.k_blocks = fp8 ? (s.I + kBlockKFp8 - 1) / kBlockKFp8 : s.I / kBlockK;
     g.w_rows = s.H;
     g.bias = static_cast<const __nv_bfloat16*>(down.bias);
     g.h = nullptr;
@@ -541,6 +569,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.topk_w = r.w;
     g.top_k = s.top_k;
     g.scales = static_cast<const uint8_t*>(down.scale);
+    g.wscale = fp8 ? static_cast<const float*>(down.scale) : nullptr;
     g.kscale = s.I / 32;
     // the down projection adds its K parts through the output's atomics
     g.ksplit = pair ? 1 : parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, kMaxKSplit);

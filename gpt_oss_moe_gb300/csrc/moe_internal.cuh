@@ -15,6 +15,8 @@ constexpr int kRouterTokens = 32;      // tokens per router / permutation block
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int kBlockK = 64;            // K elements per pipeline stage (128 B of bf16)
+constexpr int kBlockKFp8 = 128;        // E4M3: K elements per stage (128 B)
+constexpr float kFp8HScale = 0.125f;   // FP8 h codes = e4m3(h / kFp8HScale)
 constexpr int kWeightTileRows = 128;   // MMA M: weight rows per tile
 constexpr int kMaxTokenTile = 256;     // MMA N upper bound
 
@@ -97,7 +99,7 @@ inline int router_ksplit(int pairs, int nchunks) {
 
 struct WsLayout {
     size_t status, topk_ids, topk_w, blk_cnt, logits, partials, counters, offsets, gemm_partial;
-    size_t sorted_assign, assign_row, tiles, x_perm, h, out_acc, total;
+    size_t sorted_assign, assign_row, tiles, x_perm, x_scale, h, out_acc, total;
     size_t gemm_partial_bytes;
     int max_tiles;
 };
@@ -128,7 +130,8 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
     L.sorted_assign = take(R * 4);
     L.assign_row = take(R * 4);
     L.tiles = take(static_cast<size_t>(L.max_tiles) * 16);
-    L.x_perm = take(R * H * 2);
+    L.x_perm = take(R * H * 2);            // bf16, or E4M3 codes (FP8)
+    L.x_scale = take(R * 4);               // FP8: scale of each routed row
     L.h = take(R * I * 2);
     L.out_acc = take(static_cast<size_t>(T) * H * 4);
     // gate_up K-split partial tiles, fp32 [part][weight block][routed row][128].
@@ -194,6 +197,8 @@ struct PermuteParams {
     int mx_layout;               // MXFP4 operand layout: chunk-major
                                  // [H/64][T*k][64], each group of 8 columns
                                  // in the order 0,4,1,5,2,6,3,7
+    int fp8;                     // FP8 W8A8: x_perm holds E4M3 codes [T*k, H]
+    float* x_scale;              // FP8: [T*k] scale of each routed row's codes
     int32_t* status;
 };
 
@@ -219,6 +224,13 @@ struct GemmParams {
     const __nv_bfloat16* bias;   // [E, w_rows]
     // kEpiGlu: h[row, w_rows/2] bf16
     __nv_bfloat16* h;
+    // FP8 W8A8 (WF = 2): per-expert weight scales [E]; gate_up: the scale of
+    // each routed row's activation codes [T*k] and h written as E4M3 codes
+    // [T*k, w_rows/2] (scale kFp8HScale); down: the scale of the h codes
+    const float* wscale;
+    const float* xscale;
+    uint8_t* h8;
+    float hscale;
     // kEpiCombine: out[t, w_rows] += w * y
     float* out;
     const int32_t* sorted_assign;

@@ -17,7 +17,9 @@
 //      With MXFP4 weights x_perm takes the layout that GEMM reads: chunk-
 //      major [H/64][T*k][64] (one TMA box then spans several 64-wide K
 //      chunks), each group of 8 columns in the order 0,4,1,5,2,6,3,7 (the
-//      order in which the GEMM expands E2M1 codes).
+//      order in which the GEMM expands E2M1 codes).  With FP8 W8A8 weights
+//      the row is quantised on the way: E4M3 codes of x * (448 / max|x|)
+//      with the token's own max|x|, and the row's scale max|x| / 448.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "../../include/moe.h"
@@ -36,6 +38,29 @@ __device__ __forceinline__ uint4 kperm8(const uint4 v) {
     r.z = __byte_perm(v.y, v.w, 0x5410);
     r.w = __byte_perm(v.y, v.w, 0x7632);
     return r;
+}
+
+// Largest magnitude of eight bf16 values (exact, in fp32).
+__device__ __forceinline__ float absmax8(const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+    }
+    return m;
+}
+
+// Eight bf16 values times `inv` to eight E4M3 codes, in element order.
+__device__ __forceinline__ uint2 e4m3x8(const uint4 v, float inv) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        c[i] = cvt_e4m3x2(__uint_as_float(w[i] << 16) * inv,
+                          __uint_as_float(w[i] & 0xFFFF0000u) * inv);
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p) {
@@ -137,6 +162,20 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
             const int row = rows_s[la];
             if (row < 0) continue;
             const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>((a0 + la) / k) * p.H);
+            if (p.fp8) {
+                // FP8 W8A8: the token's own scale, max|x| / 448, then the row
+                // as E4M3 codes of x * (448 / max|x|) (1 for an all-zero row)
+                float m = 0.f;
+                for (int v = lane; v < vec_per_row; v += 32) m = fmaxf(m, absmax8(src[v]));
+#pragma unroll
+                for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+                const float inv = m > 0.f ? 448.0f / m : 1.0f;
+                if (lane == 0) p.x_scale[row] = m > 0.f ? m / 448.0f : 1.0f;
+                uint2* dst8 = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.x_perm) +
+                                                       static_cast<size_t>(row) * p.H);
+                for (int v = lane; v < vec_per_row; v += 32) dst8[v] = e4m3x8(src[v], inv);
+                continue;
+            }
             uint4* dst = reinterpret_cast<uint4*>(p.x_perm + static_cast<size_t>(row) * p.H);
             // chunk-major: vector v (8 columns) of the row goes to chunk v/8
             uint4* dst_mx = reinterpret_cast<uint4*>(p.x_perm) + static_cast<size_t>(row) * 8;

@@ -259,6 +259,18 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs (kind::f8f6f4, K = 32 per
+// instruction: 32 bytes of a 128-byte swizzled row), fp32 accumulator.
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulator.  With
 // M = 128, A row i sits in TMEM lane i and its K elements run along the
 // columns, two bf16 per 32-bit column (even K in the low half); one MMA
@@ -360,6 +372,22 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t
          | (1u << 10)           // B = bf16
          | ((N >> 3) << 17)
          | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format 0, both
+// K-major), fp32 D.
+__host__ __device__ __forceinline__ uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+    return (1u << 4)            // D = f32
+         | ((N >> 3) << 17)
+         | ((M >> 4) << 24);
+}
+
+// Two fp32 values to two E4M3 codes (round to nearest even, magnitudes past
+// 448 saturating to 448): lo -> bits 0..7, hi -> bits 8..15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // ---------------------------------------------------------------- PDL

@@ -60,10 +60,18 @@ typedef enum {
 /* Expert weight storage format. */
 typedef enum {
     MOE_W_BF16 = 0,   /* bf16 values */
-    MOE_W_MXFP4 = 1   /* OCP MX FP4: E2M1 codes, two per byte (element 2i in
+    MOE_W_MXFP4 = 1,  /* OCP MX FP4: E2M1 codes, two per byte (element 2i in
                          the low nibble of byte i), plus one E8M0 scale byte
                          (value 2^(s-127)) per 32 consecutive input elements
                          of each output row (§5 "量化") */
+    MOE_W_FP8 = 2     /* FP8 W8A8 (§5 "量化"): E4M3 codes ("fn": max 448),
+                         one byte per weight, [E, N, K] like bf16, and
+                         moe_weight.scale = fp32 [E], one scale per expert,
+                         applied to the finished products.  The layer
+                         quantises the activations itself: each token with
+                         its own scale max|x| / 448 (round to nearest even,
+                         saturating), h with the fixed scale 1/8 (the GLU
+                         clamps keep |h| * 8 <= 448) */
 } moe_wfmt;
 
 /* Layer shape.  T tokens, hidden size H, expert intermediate size I,
@@ -75,9 +83,11 @@ typedef struct {
 
 /* One expert weight bank.
  *   gate_up: w bf16 [E, 2I, H] (row 2j = gate_j, row 2j+1 = up_j) or MXFP4
- *            codes u8 [E, 2I, H/2] with scale u8 [E, 2I, H/32];
+ *            codes u8 [E, 2I, H/2] with scale u8 [E, 2I, H/32] or FP8 codes
+ *            u8 [E, 2I, H] with scale fp32 [E];
  *            bias bf16 [E, 2I].
- *   down:    w bf16 [E, H, I] or codes u8 [E, H, I/2], scale u8 [E, H, I/32];
+ *   down:    w bf16 [E, H, I] or codes u8 [E, H, I/2], scale u8 [E, H, I/32],
+ *            or FP8 codes u8 [E, H, I] with scale fp32 [E];
  *            bias bf16 [E, H].
  * scale is NULL for bf16 weights. */
 typedef struct {

@@ -407,6 +407,56 @@ def test_mxfp4_odd_ring_slots_per_unit(moe, oracle_lib, synth_lib, ksplit):
         moe.moe_set_tuning("ksplit", 0)
 
 
+# ---------------------------------------------------------------- FP8 W8A8
+
+FP8_CASES = [
+    # E, k, H, I, T, token_tile
+    (8, 2, 128, 128, 1, 0),
+    (8, 4, 320, 192, 37, 0),        # K tails: 320 = 2.5 and 192 = 1.5 k-blocks of 128
+    (4, 2, 192, 64, 700, 0),        # several token tiles per expert
+    (8, 4, 256, 256, 200, 48),
+    (32, 4, 2880, 2880, 5, 0),      # 2880 = 22.5 k-blocks
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=lambda c: "E{}k{}H{}I{}T{}tile{}".format(*c))
+def test_forward_fp8_small_shapes(moe, oracle_lib, synth_lib, case):
+    E, k, H, I, T, tile = case
+    L = synth_lib.make_layer(E=E, T=T, H=H, I=I, top_k=k, seed=500 + T, wfmt="fp8",
+                             router_w_std=0.05)
+    moe.moe_set_tuning("token_tile", tile)
+    try:
+        _check(moe, oracle_lib, L)
+    finally:
+        moe.moe_set_tuning("token_tile", 0)
+
+
+def test_fp8_outliers_and_zero_rows(moe, oracle_lib, synth_lib):
+    """Per-token scales: a token with 20x outliers and an all-zero token
+    (scale 1, every code 0) beside ordinary ones."""
+    L = synth_lib.make_layer(E=8, T=20, H=256, I=128, top_k=2, seed=511, wfmt="fp8",
+                             router_w_std=0.05, p_outlier=0.05)
+    L.x = L.x.clone()
+    L.x[3] = 0
+    _check(moe, oracle_lib, L)
+
+
+@pytest.fixture(scope="module")
+def layer_20b_fp8(synth_lib):
+    L = synth_lib.make_workload("20b_fp8", 512)
+    return L, to_device(L)
+
+
+@pytest.mark.parametrize("T", [1, 64, 512])
+def test_forward_20b_fp8(moe, oracle_lib, layer_20b_fp8, T):
+    L, dev = layer_20b_fp8
+    sample = None
+    if T > 64:
+        g = torch.Generator().manual_seed(T)
+        sample = [0, T - 1] + torch.randint(0, T, (30,), generator=g).tolist()
+    _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample)
+
+
 @pytest.fixture(scope="module")
 def layer_20b_mxfp4(synth_lib):
     L = synth_lib.make_workload("20b_mxfp4", 512)
