@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     if (stages < 2 || stages > kMaxStages || n_iss < 1 || n_iss > (WF == 1 ? 2 : 1) ||
         p.ksplit < 1 || p.ksplit > kMaxKSplit ||
         (EPI == kEpiGlu && p.ksplit > 1 && (p.partial == nullptr || p.tickets == nullptr)) ||
-        (kPair && (WF != 0 || p.ksplit != 1 || (gridDim.x & 1u) || (box & 15))) ||
+        (kPair && (WF == 1 || p.ksplit != 1 || (gridDim.x & 1u) || (box & 15))) ||
         (WF == 1 && (astages < 2 || astages > kMxfp4AStages || 2 * stages < astages + 2 ||
                      (n_iss == 2 && (astages & 1)) ||
                      a_col0 + kASlotCols * static_cast<uint32_t>(astages) >
@@ -480,7 +480,9 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                         for (int kk = 0; kk < kBlockK / 16; ++kk) {
                             const uint32_t acc = kk == 0 ? acc0 : 1u;
                             // one MMA per 32 bytes of K (16 bf16, 32 E4M3)
-                            if constexpr (kPair)
+                            if constexpr (kPair && WF == 2)
+                                tc_mma_e4m3_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
+                            else if constexpr (kPair)
                                 tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
                             else if constexpr (WF == 2)
                                 tc_mma_e4m3(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
@@ -1018,7 +1020,11 @@ cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUte
                         bool pdl) {
     if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
     if (cg == 2) {
-        if (wf != 0) return cudaErrorInvalidValue;
+        if (wf == 1) return cudaErrorInvalidValue;
+        if (wf == 2)
+            return epi == kEpiGlu
+                       ? launch_gemm_t<kEpiGlu, 2, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl)
+                       : launch_gemm_t<kEpiCombine, 2, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl);
         return epi == kEpiGlu
                    ? launch_gemm_t<kEpiGlu, 0, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl)
                    : launch_gemm_t<kEpiCombine, 0, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl);

@@ -111,11 +111,15 @@ moe_status weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K, bo
 std::atomic<int> g_token_tile{0};
 std::atomic<int> g_ksplit_mode{0};  // 0: automatic, 1: never split, n >= 2: n parts
 std::atomic<int> g_pdl{1};
-std::atomic<int> g_pair_mode{0};   // 0: automatic, 1: never, 2: always (bf16 weights)
+std::atomic<int> g_pair_mode{0};   // 0: automatic, 1: never, 2: always (bf16 and FP8 weights)
 // bf16 token boxes from which the GEMMs run on CTA pairs (automatic mode):
 // measured on gpt-oss-20b, pairs are 3 % slower at a 128-row box (T = 128),
 // even at 256 (T = 256) and 2-5 % faster at T >= 512
 constexpr int kPairMinBox = 256;
+// FP8 layers (box 256) on gpt-oss-20b: pairs are 10-12 % faster while the
+// mean routed rows per expert stay below 128 (T = 256, 512), even at 128
+// (T = 1024) and 4 % slower at 512 (T = 4096).
+constexpr long long kFp8PairMaxMeanRows = 128;
 
 // ------------------------------------------------------------ profiling
 //
@@ -402,12 +406,14 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     const int box = auto_token_tile(s);
     const bool pdl = g_pdl.load() != 0;
 
-    // CTA pairs (bf16, wide token boxes): M = 256 MMAs over two SMs, each SM
+    // CTA pairs (bf16 or FP8, wide token boxes): M = 256 MMAs over two SMs, each SM
     // loading 128 weight rows and half of the token tile, so a ring slot
     // holds 32 KB instead of 48 KB (box 256) for the same tensor work.
     const int pair_mode = g_pair_mode.load();
-    const bool pair = !mxfp4 && !fp8 &&
-                      (pair_mode == 2 || (pair_mode == 0 && box >= kPairMinBox));
+    const bool pair_auto =
+        box >= kPairMinBox &&
+        (!fp8 || static_cast<long long>(R) < kFp8PairMaxMeanRows * s.E);
+    const bool pair = !mxfp4 && (pair_mode == 2 || (pair_mode == 0 && pair_auto));
     const int bbox = pair ? box / 2 : box;     // token rows of one CTA's B tile
     // Pipeline depth: as many stages as the shared memory allows (2..12).
     const int wf = mxfp4 ? 1 : fp8 ? 2 : 0;

@@ -307,6 +307,17 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc
         : "memory");
 }
 
+// CTA pair, E4M3 inputs (kind::f8f6f4, K = 32 per instruction).
+__device__ __forceinline__ void tc_mma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // CTA pair: arrives once on `bar` of this CTA / of every CTA in `cta_mask`
 // (same offset) when the pair MMAs issued so far by this thread completed.
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {

@@ -196,10 +196,11 @@ moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
  *                 sums its K range in one fixed order), 2..8 = split every
  *                 small-batch unit into that many parts (at most one per
  *                 two ring slots, and as many as the workspace holds);
- *   "pair":       0 = run the bf16 GEMMs on CTA pairs (M = 256 MMAs over two
- *                 SMs, 256-row weight blocks) when the token box is 256
- *                 rows (default), 1 = never, 2 = always (bf16
- *                 weights; the K range is then never split).
+ *   "pair":       0 = run the bf16 and FP8 GEMMs on CTA pairs (M = 256 MMAs
+ *                 over two SMs, 256-row weight blocks) when the token box is
+ *                 256 rows and, for FP8, T * top_k < 128 * E (default),
+ *                 1 = never, 2 = always (bf16 and FP8 weights; the K range
+ *                 is then never split).
  * Returns MOE_ERR_ARG for an unknown key or value. */
 moe_status moe_set_tuning(const char* key, int value);
 

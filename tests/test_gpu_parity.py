@@ -431,6 +431,21 @@ def test_forward_fp8_small_shapes(moe, oracle_lib, synth_lib, case):
         moe.moe_set_tuning("token_tile", 0)
 
 
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "E{}k{}H{}I{}T{}tile{}".format(*c))
+def test_forward_fp8_cta_pairs(moe, oracle_lib, synth_lib, case):
+    """FP8 GEMMs forced onto CTA pairs (M = 256 kind::f8f6f4 MMAs)."""
+    E, k, H, I, T, tile = case
+    L = synth_lib.make_layer(E=E, T=T, H=H, I=I, top_k=k, seed=820 + T + H, wfmt="fp8",
+                             router_w_std=0.05)
+    moe.moe_set_tuning("pair", 2)
+    moe.moe_set_tuning("token_tile", tile)
+    try:
+        _check(moe, oracle_lib, L)
+    finally:
+        moe.moe_set_tuning("pair", 0)
+        moe.moe_set_tuning("token_tile", 0)
+
+
 def test_fp8_outliers_and_zero_rows(moe, oracle_lib, synth_lib):
     """Per-token scales: a token with 20x outliers and an all-zero token
     (scale 1, every code 0) beside ordinary ones."""
