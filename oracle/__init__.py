@@ -70,6 +70,7 @@ def lib():
             L.oracle_e4m3_round.argtypes = [f]
             L.oracle_e4m3_round.restype = ctypes.c_uint8
             L.oracle_fp8_quantize_row.argtypes = [vp, i, vp, vp]
+            L.oracle_mx_quantize_row.argtypes = [vp, i, vp, vp]
             L.oracle_router_logits.argtypes = [P, vp, i]
             L.oracle_topk_softmax.argtypes = [vp, i, i, i, vp, vp]
             L.oracle_permute.argtypes = [vp, i, i, i, vp, vp, vp]
@@ -92,7 +93,7 @@ def _ptr(t):
 def _layer_struct(layer):
     """Build the C struct from a synth.Layer (keeps the tensors alive)."""
     s = OracleLayer(layer.T, layer.H, layer.I, layer.E, layer.top_k,
-                    {"bf16": 0, "mxfp4": 1, "fp8": 2}[layer.wfmt],
+                    {"bf16": 0, "mxfp4": 1, "fp8": 2, "mxfp4_mxfp8": 3}[layer.wfmt],
                     _ptr(layer.x), _ptr(layer.wr), _ptr(layer.br),
                     _ptr(layer.w_gu), _ptr(layer.s_gu), _ptr(layer.b_gu),
                     _ptr(layer.w_d), _ptr(layer.s_d), _ptr(layer.b_d))
@@ -132,6 +133,19 @@ def fp8_quantize_row(x: torch.Tensor):
     lib().oracle_fp8_quantize_row(x.data_ptr(), x.numel(), codes.data_ptr(),
                                   ctypes.byref(scale))
     return codes, scale.value
+
+
+def mx_quantize_row(x: torch.Tensor):
+    """One token's bf16 activations (a multiple of 32) -> MXFP8 (e4m3 codes
+    uint8[n], UE8M0 block scales uint8[n / 32])."""
+    x = x.contiguous()
+    assert x.dtype == torch.bfloat16 and x.dim() == 1 and x.numel() % 32 == 0
+    codes = torch.empty(x.numel(), dtype=torch.uint8)
+    scales = torch.empty(x.numel() // 32, dtype=torch.uint8)
+    rc = lib().oracle_mx_quantize_row(x.data_ptr(), x.numel(), codes.data_ptr(),
+                                      scales.data_ptr())
+    assert rc == 0
+    return codes, scales
 
 
 def router_logits(layer, threads: int = 0) -> torch.Tensor:

@@ -51,6 +51,16 @@
 //     clamps keep h in [-42, 56), so h * 8 never exceeds 448).  A gate_up row
 //     is (sum_k e4m3(w) * e4m3(xq)) * (scale[e] * s) + bias; a down row is
 //     (sum_j e4m3(w) * e4m3(hq)) * (scale[e] * 1/8) + bias.
+//   * MXFP4 weights with MXFP8 activations (the native block-scaled form of
+//     §5's MXFP4): weights as MXFP4 above; each token's activations are cut
+//     into blocks of 32 consecutive elements, each block quantised by the
+//     OCP Microscaling (MX) v1.0 conversion rule: shared scale
+//     X = 2^(floor(log2 max|x|) - 8) (8 = the largest exponent of E4M3),
+//     clamped to [2^-127, 2^127] (2^-127 for an all-zero block), elements =
+//     e4m3 nearest to x / X, ties to even, saturating at 448.  h is E4M3 with
+//     every block scale 1/8, as in the FP8 reading.  A gate_up row is
+//     sum_k w(k) * e4m3(xq_k) * X(k) + bias, a down row
+//     sum_j w(j) * e4m3(hq_j) / 8 + bias, both in fp32.
 //
 // Parity pins (tests/test_oracle_pins.py): brute force over all k-subsets,
 // closed-form special cases of top-k/softmax, permutation closed forms,
@@ -129,6 +139,26 @@ inline float fp8_quantize_row(const uint16_t* x, int n, uint8_t* codes) {
     const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
     for (int i = 0; i < n; ++i) codes[i] = e4m3_round(bf16_value(x[i]) * inv);
     return amax > 0.0f ? amax / 448.0f : 1.0f;
+}
+
+// One block of 32 activations to MXFP8 (OCP MX v1.0 conversion: shared
+// exponent floor(log2 max|x|) minus E4M3's largest exponent 8, clamped to
+// the UE8M0 range; elements rounded to e4m3 after division by the scale).
+// Returns the UE8M0 byte of the block's scale.
+inline uint8_t mx_quantize_block(const uint16_t* x, uint8_t* codes) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) amax = std::fmax(amax, std::fabs(bf16_value(x[i])));
+    int shared = -127;
+    if (amax > 0.0f) {
+        int ex = 0;
+        std::frexp(amax, &ex);            // amax = m * 2^ex, m in [0.5, 1)
+        shared = (ex - 1) - 8;            // floor(log2 amax) - 8
+        if (shared < -127) shared = -127;
+        if (shared > 127) shared = 127;
+    }
+    for (int i = 0; i < 32; ++i)
+        codes[i] = e4m3_round(std::ldexp(bf16_value(x[i]), -shared));
+    return static_cast<uint8_t>(shared + 127);
 }
 
 // UE8M0: an unsigned power-of-two exponent with bias 127.
@@ -232,6 +262,46 @@ void expert_ffn_fp8(const oracle_layer* L, int e, const uint16_t* xr, float* h_o
     }
 }
 
+// MXFP4-weight / MXFP8-activation form of expert_ffn (the readings above).
+void expert_ffn_mx(const oracle_layer* L, int e, const uint16_t* xr, float* h_out,
+                   float* y_out) {
+    const int H = L->H, I = L->I;
+    const size_t n_gu = static_cast<size_t>(2) * I;
+    std::vector<uint8_t> xq(H);
+    std::vector<float> xv(H);
+    for (int b = 0; b < H / 32; ++b) {
+        const uint8_t sx = mx_quantize_block(xr + 32 * b, xq.data() + 32 * b);
+        for (int i = 0; i < 32; ++i)
+            xv[32 * b + i] = e4m3_value(xq[32 * b + i]) * e8m0_value(sx);
+    }
+    const uint8_t* s_gu = static_cast<const uint8_t*>(L->s_gu);
+    const uint8_t* s_d = static_cast<const uint8_t*>(L->s_d);
+    const size_t gu_row0 = static_cast<size_t>(e) * n_gu;
+    const uint16_t* bias_gu = L->b_gu + gu_row0;
+    std::vector<float> gu(n_gu);
+    for (size_t n = 0; n < n_gu; ++n) {
+        float acc = 0.0f;
+        for (int k = 0; k < H; ++k)
+            acc += weight_at(1, L->w_gu, s_gu, gu_row0 + n, k, H) * xv[k];
+        gu[n] = acc + bf16_value(bias_gu[n]);
+    }
+    std::vector<float> h(I), hv(I);
+    for (int j = 0; j < I; ++j) {
+        const float gate = gu[2 * j], up = gu[2 * j + 1];
+        h[j] = glu(gate, up);
+        hv[j] = e4m3_value(e4m3_round(h[j] * 8.0f)) * 0.125f;
+    }
+    if (h_out) std::memcpy(h_out, h.data(), sizeof(float) * I);
+    const size_t d_row0 = static_cast<size_t>(e) * H;
+    const uint16_t* bias_d = L->b_d + d_row0;
+    for (int n = 0; n < H; ++n) {
+        float acc = 0.0f;
+        for (int j = 0; j < I; ++j)
+            acc += weight_at(1, L->w_d, s_d, d_row0 + n, j, I) * hv[j];
+        y_out[n] = acc + bf16_value(bias_d[n]);
+    }
+}
+
 // One expert applied to one token: gate_up + bias -> GLU -> down + bias.
 // h_out may be null; y_out receives H values.
 void expert_ffn(const oracle_layer* L, int e, int t, float* h_out,
@@ -243,6 +313,10 @@ void expert_ffn(const oracle_layer* L, int e, int t, float* h_out,
     for (int k = 0; k < H; ++k) xf[k] = bf16_value(xr[k]);
     if (L->wfmt == 2) {
         expert_ffn_fp8(L, e, xr, h_out, y_out);
+        return;
+    }
+    if (L->wfmt == 3) {
+        expert_ffn_mx(L, e, xr, h_out, y_out);
         return;
     }
 
@@ -305,6 +379,14 @@ uint8_t oracle_e4m3_round(float v) { return e4m3_round(v); }
 // scale (max|x| / 448, or 1 for an all-zero row).
 int oracle_fp8_quantize_row(const uint16_t* x, int n, uint8_t* codes, float* scale) {
     *scale = fp8_quantize_row(x, n, codes);
+    return 0;
+}
+
+// One token row of n bf16 activations (n a multiple of 32) to MXFP8: codes
+// [n] e4m3 and scales [n / 32] UE8M0 bytes.
+int oracle_mx_quantize_row(const uint16_t* x, int n, uint8_t* codes, uint8_t* scales) {
+    if (n % 32) return -1;
+    for (int b = 0; b < n / 32; ++b) scales[b] = mx_quantize_block(x + 32 * b, codes + 32 * b);
     return 0;
 }
 

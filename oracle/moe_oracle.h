@@ -14,15 +14,16 @@ extern "C" {
 #endif
 
 typedef struct {
-    int T, H, I, E, top_k, wfmt;  /* wfmt: 0 = bf16, 1 = MXFP4, 2 = FP8 W8A8 */
+    int T, H, I, E, top_k, wfmt;  /* 0 = bf16, 1 = MXFP4, 2 = FP8 W8A8,
+                                     3 = MXFP4 weights, MXFP8 activations */
     const uint16_t* x;            /* [T, H] bf16 */
     const uint16_t* wr;           /* [E, H] bf16 */
     const uint16_t* br;           /* [E] bf16 */
     const void* w_gu;             /* bf16 [E, 2I, H] | u8 [E, 2I, H/2] | e4m3 [E, 2I, H] */
-    const void* s_gu;             /* u8 [E, 2I, H/32] (MXFP4) | fp32 [E] (FP8) */
+    const void* s_gu;             /* u8 [E, 2I, H/32] (MXFP4, 3) | fp32 [E] (FP8) */
     const uint16_t* b_gu;         /* [E, 2I] bf16 */
     const void* w_d;              /* bf16 [E, H, I] | u8 [E, H, I/2] | e4m3 [E, H, I] */
-    const void* s_d;              /* u8 [E, H, I/32] (MXFP4) | fp32 [E] (FP8) */
+    const void* s_d;              /* u8 [E, H, I/32] (MXFP4, 3) | fp32 [E] (FP8) */
     const uint16_t* b_d;          /* [E, H] bf16 */
 } oracle_layer;
 
@@ -33,6 +34,7 @@ float oracle_e8m0(uint8_t s);
 float oracle_e4m3(uint8_t code);
 uint8_t oracle_e4m3_round(float v);
 int oracle_fp8_quantize_row(const uint16_t* x, int n, uint8_t* codes, float* scale);
+int oracle_mx_quantize_row(const uint16_t* x, int n, uint8_t* codes, uint8_t* scales);
 int oracle_router_logits(const oracle_layer* L, float* logits, int threads);
 int oracle_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids,
                         float* w);

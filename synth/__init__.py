@@ -123,7 +123,7 @@ class Layer:
     I: int
     E: int
     top_k: int
-    wfmt: str                      # "bf16", "mxfp4" or "fp8"
+    wfmt: str                      # "bf16", "mxfp4", "fp8" or "mxfp4_mxfp8"
     x: torch.Tensor                # [T, H] bf16
     wr: torch.Tensor               # [E, H] bf16
     br: torch.Tensor               # [E] bf16
@@ -169,7 +169,7 @@ def make_layer(E: int, T: int, H: int = 2880, I: int = 2880, top_k: int = 4,
                router_w_std: Optional[float] = None,
                scale_lo: int = 119, scale_hi: int = 123,
                pin: bool = False, with_experts: bool = True) -> Layer:
-    if wfmt not in ("bf16", "mxfp4", "fp8"):
+    if wfmt not in ("bf16", "mxfp4", "fp8", "mxfp4_mxfp8"):
         raise ValueError(f"unknown weight format {wfmt!r}")
     rws = w_std if router_w_std is None else router_w_std
     x = make_x(T, H, seed, p_outlier, outlier_scale, pin)
@@ -222,6 +222,8 @@ WORKLOADS = {
     "20b_mxfp4": dict(E=32, seed=4, Ts=(1, 64, 512), wfmt="mxfp4"),
     # FP8 W8A8 (the pages' quantised serving path, next after the five above)
     "20b_fp8": dict(E=32, seed=5, Ts=(1, 64, 512, 4096), wfmt="fp8"),
+    # MXFP4 weights (the same as 20b_mxfp4: seed 4) with MXFP8 activations
+    "20b_mxfp4_mxfp8": dict(E=32, seed=4, Ts=(1, 64, 512, 4096), wfmt="mxfp4_mxfp8"),
 }
 
 

@@ -41,6 +41,12 @@ MUTATIONS = {
     "fp8_no_saturation": ("for (int c = 0; c <= 0x7E; ++c) {", "for (int c = 0; c <= 0x7D; ++c) {"),
     "fp8_weight_scale_twice": ("const float gu_scale = sw_gu[e] * xs;",
                                "const float gu_scale = sw_gu[e] * sw_gu[e] * xs;"),
+    "mx_shared_exponent_off_by_one": ("shared = (ex - 1) - 8;", "shared = ex - 8;"),
+    "mx_low_clamp_missing": ("if (shared < -127) shared = -127;", ""),
+    "mx_block_scale_dropped": ("xv[32 * b + i] = e4m3_value(xq[32 * b + i]) * e8m0_value(sx);",
+                               "xv[32 * b + i] = e4m3_value(xq[32 * b + i]);"),
+    "mx_h_scale_wrong": ("hv[j] = e4m3_value(e4m3_round(h[j] * 8.0f)) * 0.125f;",
+                         "hv[j] = e4m3_value(e4m3_round(h[j] * 8.0f)) * 0.25f;"),
     "scale_bias_off_by_one": ("static_cast<int>(s) - 127", "static_cast<int>(s) - 128"),
     "softmax_over_all_experts": ("    for (int j = 0; j < k; ++j) w[j] = ex[j] / denom;",
                                  "    for (int e = 0; e < E; ++e) if (!taken[e]) denom += std::exp(logit[e] - m);\n"

@@ -490,3 +490,114 @@ def test_fp8_scales_apply_after_the_product(oracle_lib, synth_lib):
     h2, y2 = oracle_lib.expert_ffn(L, 1, 0)
     assert torch.equal(h1, h2)
     assert torch.equal(y2, 2.0 * y1) and y1.abs().max() > 0
+
+
+# ------------------------------------------- MXFP4 weights, MXFP8 activations
+
+def _mx_expected(block: torch.Tensor):
+    """OCP MX v1.0 conversion of one bf16 block of 32, written with torch ops:
+    shared exponent floor(log2 max|x|) - 8 clamped to [-127, 127] (-127 for
+    a zero block), elements by the library's e4m3 rounding, saturated."""
+    xf = block.double()
+    amax = xf.abs().max().item()
+    shared = -127 if amax == 0 else max(-127, min(127, math.floor(math.log2(amax)) - 8))
+    v = (xf * 2.0 ** (-shared)).clamp(-448.0, 448.0).float()
+    return _torch_e4m3_codes(v), shared + 127
+
+
+def test_mx_quantisation_closed_forms(oracle_lib):
+    def q(vals):
+        x = torch.zeros(32, dtype=torch.bfloat16)
+        x[: len(vals)] = torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)
+        return oracle_lib.mx_quantize_row(x)
+    codes, scales = q([1.0])                 # 1 = 2^0: scale 2^-8, 1 -> 256
+    assert scales.tolist() == [119] and codes[0].item() == 0x78
+    codes, scales = q([480.0, -3.0])         # floor(log2 480) = 8: scale 1; 480 saturates
+    assert scales.tolist() == [127] and codes[0].item() == 0x7E and codes[1].item() == 0xC4
+    codes, scales = q([])                    # all zero: smallest scale, zero codes
+    assert scales.tolist() == [0] and codes.eq(0).all()
+    codes, scales = q([2.0 ** -130])         # scale clamps at 2^-127: 2^-130 -> 2^-3
+    assert scales.tolist() == [0] and codes[0].item() == 0x20
+    codes, scales = q([0.75, 0.5])           # floor(log2 0.75) = -1: scale 2^-9
+    assert scales.tolist() == [118] and codes[0].item() == 0x7C and codes[1].item() == 0x78
+
+
+def test_mx_quantisation_matches_library_rounding(oracle_lib):
+    g = torch.Generator().manual_seed(12)
+    x = (torch.randn(32 * 40, generator=g) * torch.exp(torch.randn(32 * 40, generator=g) * 3))
+    x[5 * 32: 6 * 32] = 0.0
+    x = x.to(torch.bfloat16)
+    codes, scales = oracle_lib.mx_quantize_row(x)
+    for b in range(40):
+        ec, es = _mx_expected(x[32 * b: 32 * (b + 1)])
+        assert scales[b].item() == es, b
+        assert torch.equal(codes[32 * b: 32 * (b + 1)], ec), b
+
+
+def _fp64_mx_layer(L):
+    """Independent fp64 brute force of the MXFP4-weight / MXFP8-activation
+    layer: MXFP4 weights from the E2M1 table, activations by the MX rule above,
+    h as e4m3 of h * 8."""
+    dec = lambda c: c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    tab = np.array(E2M1_TABLE)
+
+    def dequant(codes, scales, K):
+        lo, hi = codes & 0xF, codes >> 4
+        q = torch.stack([lo, hi], dim=-1).reshape(*codes.shape[:-1], K).long().numpy()
+        s = np.repeat(2.0 ** (scales.double().numpy() - 127), 32, axis=-1)
+        return tab[q] * s
+
+    x = L.x.float()
+    wr, br = L.wr.float().double().numpy(), L.br.float().double().numpy()
+    logits = x.double().numpy() @ wr.T + br
+    wgu, wd = dequant(L.w_gu, L.s_gu, L.H), dequant(L.w_d, L.s_d, L.I)
+    bgu, bd = L.b_gu.float().double().numpy(), L.b_d.float().double().numpy()
+    out = np.zeros((L.T, L.H))
+    sels = []
+    for t in range(L.T):
+        order = sorted(range(L.E), key=lambda e: (-logits[t, e], e))
+        sel = order[: L.top_k]
+        z = np.exp(logits[t, sel] - logits[t, sel[0]])
+        w = z / z.sum()
+        xq = np.zeros(L.H)
+        for b in range(L.H // 32):
+            c, s = _mx_expected(L.x[t, 32 * b: 32 * (b + 1)])
+            xq[32 * b: 32 * (b + 1)] = dec(c) * 2.0 ** (s - 127)
+        for j, e in enumerate(sel):
+            gu = wgu[e] @ xq + bgu[e]
+            gate, up = np.minimum(gu[0::2], 7.0), np.clip(gu[1::2], -7.0, 7.0)
+            h = (up + 1.0) * gate / (1.0 + np.exp(-1.702 * gate))
+            hq = dec(_torch_e4m3_codes(torch.from_numpy(h * 8.0))) * 0.125
+            out[t] += w[j] * (wd[e] @ hq + bd[e])
+        sels.append(sel)
+    return sels, out
+
+
+def test_mx_layer_matches_fp64_brute_force(oracle_lib, synth_lib):
+    L = synth_lib.make_layer(E=4, T=6, H=64, I=64, top_k=2, seed=33, wfmt="mxfp4_mxfp8",
+                             router_w_std=0.3)
+    sels, ref = _fp64_mx_layer(L)
+    ids, w, out = oracle_lib.forward(L)
+    assert ids.tolist() == sels
+    err = np.abs(out.double().numpy() - ref).max()
+    assert err <= 2e-3 * np.abs(ref).max()
+
+
+def test_mx_layer_with_exact_activations_equals_mxfp4_layer(oracle_lib, synth_lib):
+    """Activations that MXFP8 holds exactly give the MXFP4 (bf16-activation)
+    layer's h bit for bit: x = m / 8 with |m| <= 14 and every block's largest
+    magnitude 1.75, so the block scale is 2^-8 and x / scale = 32 m, at most
+    448 and within e4m3's 4 significant bits."""
+    L = synth_lib.make_layer(E=2, T=2, H=64, I=64, top_k=1, seed=9, wfmt="mxfp4_mxfp8")
+    g = torch.Generator().manual_seed(4)
+    x = torch.randint(-14, 15, (2, 64), generator=g).float() * 0.125
+    x[:, 0] = 1.75
+    x[:, 32] = -1.75
+    L.x = x.to(torch.bfloat16)
+    codes, scales = oracle_lib.mx_quantize_row(L.x[0])
+    assert scales.tolist() == [119, 119]
+    h_mx, _ = oracle_lib.expert_ffn(L, 1, 0)
+    L4 = synth_lib.make_layer(E=2, T=2, H=64, I=64, top_k=1, seed=9, wfmt="mxfp4")
+    L4.x = L.x
+    h_4, _ = oracle_lib.expert_ffn(L4, 1, 0)
+    assert torch.equal(h_mx, h_4)
