@@ -21,7 +21,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgpt_oss_moe.so")
 
-MOE_W_BF16, MOE_W_MXFP4, MOE_W_FP8 = 0, 1, 2
+MOE_W_BF16, MOE_W_MXFP4, MOE_W_FP8, MOE_W_MXFP4_MXFP8 = 0, 1, 2, 3
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_BAD_TILE = 0x1, 0x2, 0x4
 
 # Every function the C header declares, in order (checked by the tests).
@@ -220,4 +220,5 @@ def layer_shape(layer, T=None) -> moe_shape:
     """Shape of a synthetic layer object (fields T, H, I, E, top_k, wfmt)."""
     return make_shape(layer.T if T is None else T, layer.H, layer.I, layer.E,
                       layer.top_k,
-                      {"bf16": MOE_W_BF16, "mxfp4": MOE_W_MXFP4, "fp8": MOE_W_FP8}[layer.wfmt])
+                      {"bf16": MOE_W_BF16, "mxfp4": MOE_W_MXFP4, "fp8": MOE_W_FP8,
+                       "mxfp4_mxfp8": MOE_W_MXFP4_MXFP8}[layer.wfmt])

@@ -78,8 +78,14 @@ constexpr uint32_t kASlotCols = 32u * kMxfp4KbPerStage;    // TMEM columns of on
 constexpr int kMaxStages = 24;
 constexpr int kBarBytes = 768;
 
+// MXFP4 x MXFP8: bytes one weight slot moves from global memory (128 rows
+// x 64 B of codes; shared memory receives them padded to 128 B per row)
+constexpr uint32_t kMxCodeTxBytes = kWeightTileRows * 64;
+constexpr int kMxScaleWarps = 4;        // MXFP4 x MXFP8: warps 6..9 write the scales
+
 template <int WF>
-constexpr int kThreadsOf = WF == 1 ? 192 + kConvTeams * kConvThreads + 32 : 192;
+constexpr int kThreadsOf = WF == 1 ? 192 + kConvTeams * kConvThreads + 32
+                         : WF == 3 ? 192 + kMxScaleWarps * 32 : 192;
 constexpr int kSecondIssuerWarp = 6 + kConvTeams * kConvThreads / 32;    // MXFP4: warp 22
 
 struct SmemPlan {
@@ -242,8 +248,9 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     extern __shared__ uint8_t smem_raw[];
     constexpr int KPS = kKbPerStage<WF>;
     // K elements per k-block (one 128-byte swizzled row of an operand tile):
-    // 64 bf16, or 128 E4M3 codes (WF = 2)
-    constexpr int kKB = WF == 2 ? kBlockKFp8 : kBlockK;
+    // 64 bf16, or 128 E4M3 codes (WF = 2; WF = 3: 128 E4M3 token codes and
+    // 128 E2M1 weight codes, padded to a byte each in shared memory)
+    constexpr int kKB = WF >= 2 ? kBlockKFp8 : kBlockK;
     const int stages = p.stages, astages = p.astages, box = p.token_box;
     // CTA pair (CG = 2, bf16 weights): the cluster's two CTAs share each unit
     // of 256 weight rows; CTA r loads rows 128r.. of the block and half of
@@ -262,15 +269,22 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     // accumulators (a thread issues an N <= 64 MMA only every ~23 ns, the
     // tensor core takes them faster); the epilogue adds the two.
     const int n_iss = p.n_iss;
-    const uint32_t acc_stride = WF == 1 ? static_cast<uint32_t>((box + 31) & ~31)
-                                        : static_cast<uint32_t>(p.tmem_cols) / 2u;
+    const uint32_t acc_stride = (WF == 1 || WF == 3) ? static_cast<uint32_t>((box + 31) & ~31)
+                                                     : static_cast<uint32_t>(p.tmem_cols) / 2u;
     const uint32_t a_col0 = 2u * static_cast<uint32_t>(n_iss) * acc_stride;
+    // MXFP4 x MXFP8: after the two accumulators, 8 scale columns per ring
+    // slot: A (weight rows, column sf + row / 32) at +0..3, B (token rows,
+    // column sf + 4 + row / 32, lanes row % 32) at +4..7
+    const uint32_t sf_col0 = 2u * acc_stride;
     // ring sizes the converter teams rely on and the TMEM plan (uniform
     // exit, nothing started)
     if (stages < 2 || stages > kMaxStages || n_iss < 1 || n_iss > (WF == 1 ? 2 : 1) ||
         p.ksplit < 1 || p.ksplit > kMaxKSplit ||
         (EPI == kEpiGlu && p.ksplit > 1 && (p.partial == nullptr || p.tickets == nullptr)) ||
-        (kPair && (WF == 1 || p.ksplit != 1 || (gridDim.x & 1u) || (box & 15))) ||
+        (kPair && (WF == 1 || WF == 3 || p.ksplit != 1 || (gridDim.x & 1u) || (box & 15))) ||
+        (WF == 3 && (box > 128 || p.mx_cmax < 0 ||
+                     sf_col0 + 8u * static_cast<uint32_t>(stages) >
+                         static_cast<uint32_t>(p.tmem_cols))) ||
         (WF == 1 && (astages < 2 || astages > kMxfp4AStages || 2 * stages < astages + 2 ||
                      (n_iss == 2 && (astages & 1)) ||
                      a_col0 + kASlotCols * static_cast<uint32_t>(astages) >
@@ -290,7 +304,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            mbar_init(smem_u32(sm.full + s), 1);
+            // MXFP4 x MXFP8: the producer's arrival + one per scale warp
+            mbar_init(smem_u32(sm.full + s), WF == 3 ? 1 + kMxScaleWarps : 1);
             mbar_init(smem_u32(sm.empty + s), 1);
         }
         for (int s = 0; s < astages; ++s) {
@@ -338,7 +353,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            const uint32_t w_bytes = WF == 1 ? kCodeStageBytes : kATileBytes;
+            const uint32_t w_bytes = WF == 1 ? kCodeStageBytes : WF == 3 ? kMxCodeTxBytes : kATileBytes;
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -387,6 +402,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                                     &tmap_w, fb, st * KPS * (kBlockK / 2), mb * kWeightTileRows, t.x,
                                     pol_w);
                         tma_load_3d(b_dst, &tmap_x, fb, 0, t.y, st * KPS, pol_x);
+                    } else if (WF == 3) {
+                        // E2M1 codes of K 64c..64c+127 (c = 2 st, or the last
+                        // chunk starting 64 early), padded by TMA to 128 B rows
+                        tma_load_4d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
+                                    &tmap_w, fb, 0, min(2 * st, p.mx_cmax),
+                                    mb * kWeightTileRows, t.x, pol_w);
+                        tma_load_2d(b_dst, &tmap_x, fb, st * kKB, t.y, pol_x);
                     } else if (kPair) {
                         // rows 128 * rank.. of the 256-row block; token rows
                         // n/2 * rank.. of the tile (each CTA holds N/2 of B)
@@ -449,8 +471,9 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
                 const uint32_t n_mma = static_cast<uint32_t>((t.z + 15) & ~15);
-                const uint32_t idesc = WF == 2 ? idesc_e4m3_f32(kUnitRows, n_mma)
-                                               : idesc_bf16_f32(kUnitRows, n_mma);
+                const uint32_t idesc = WF == 3   ? idesc_mx_e2m1_e4m3(kUnitRows, n_mma, 0)
+                                       : WF == 2 ? idesc_e4m3_f32(kUnitRows, n_mma)
+                                                 : idesc_bf16_f32(kUnitRows, n_mma);
                 const int buf = local & 1;
                 const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
                 ++local;
@@ -475,6 +498,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     const uint64_t bd =
                         smem_desc_sw128(smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes));
                     const uint32_t acc0 = st != un.st_lo ? 1u : 0u;   // the part's first k-block
+                    const uint32_t sfa = tmem_base + sf_col0 + 8u * static_cast<uint32_t>(stage);
                     if (leader) {
 #pragma unroll
                         for (int kk = 0; kk < kBlockK / 16; ++kk) {
@@ -486,6 +510,11 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                                 tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
                             else if constexpr (WF == 2)
                                 tc_mma_e4m3(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
+                            else if constexpr (WF == 3)   // scale byte kk of the slot's cells
+                                tc_mma_mx(d_tmem, ad + 2 * kk, bd + 2 * kk,
+                                          idesc | (static_cast<uint32_t>(kk) << 4) |
+                                              (static_cast<uint32_t>(kk) << 29),
+                                          sfa, sfa + 4u, acc);
                             else
                                 tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
                         }
@@ -699,8 +728,15 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                                   (hcol & 63)
                             : p.h + static_cast<size_t>(t.y) * hcols + hcol;
                 const size_t hstride = WF == 1 ? 64 : static_cast<size_t>(hcols);
-                // FP8: h as E4M3 codes of h / kFp8HScale, [T*k, I] bytes
-                uint8_t* h8row0 = p.h8 + static_cast<size_t>(t.y) * hcols + hcol;
+                // FP8: h as E4M3 codes of h / kFp8HScale, [T*k, I] bytes;
+                // MXFP4 x MXFP8: the same codes in the padded layout
+                // [T*k, h_pad], column hcol at mx_pos (the gap zeroed by the
+                // threads of the last 64 columns)
+                const size_t h8stride = WF == 3 ? static_cast<size_t>(p.h_pad)
+                                                : static_cast<size_t>(hcols);
+                uint8_t* h8row0 = p.h8 + static_cast<size_t>(t.y) * h8stride +
+                                  (WF == 3 ? mx_pos(hcol, p.h_tail0) : hcol);
+                const bool h8gap = WF == 3 && hcol >= p.h_tail0;
                 if (WF == 2) {
                     // the sum of code products times weight scale x row scale
 #pragma unroll
@@ -719,10 +755,12 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     // rows past 2I exist only in the last 256-row block of
                     // CTA pairs (gate and up rows share their validity)
                     if (c < t.z && row_ok) {
-                        if (WF == 2)
-                            h8row0[static_cast<size_t>(c) * hcols] = static_cast<uint8_t>(
+                        if (WF >= 2) {
+                            uint8_t* dst = h8row0 + static_cast<size_t>(c) * h8stride;
+                            *dst = static_cast<uint8_t>(
                                 cvt_e4m3x2(clamped_glu(gate, up) * (1.f / kFp8HScale), 0.f));
-                        else
+                            if (h8gap) dst[-64] = 0;
+                        } else
                             hrow0[static_cast<size_t>(c) * hstride] =
                                 __float2bfloat16_rn(clamped_glu(gate, up));
                     }
@@ -811,6 +849,72 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 if (ep == 0) mbar_arrive_cluster(mapa_shared(smem_u32(sm.tempty + buf), 0));
             } else {
                 mbar_arrive(smem_u32(sm.tempty + buf));
+            }
+        }
+    } else if (WF == 3) {
+        // ------------------------------------------------ MX scale writers
+        // Warps 6..9 (one per TMEM lane quadrant) copy each ring slot's
+        // UE8M0 scales into the slot's 8 TMEM columns once the MMAs are done
+        // with the slot's previous use (the same barrier the producer waits
+        // for), then arrive on the slot's "full" barrier beside the TMA
+        // bytes.  A: weight row r (this quadrant's lanes) at column r / 32 =
+        // quad, the 4 bytes of K blocks 2c..2c+3 (c the slot's code chunk).
+        // B: token row n at lane n % 32 of every quadrant (each quadrant of
+        // the MMA reads the token scales from its own lanes), column
+        // 4 + n / 32, the 4 bytes of the slot's K blocks 4 st..4 st+3 of the
+        // padded operand, or 2^-3 for every block of the h operand.
+        const int quad = warp & 3;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = cta0; u < num_units && ok; u += ncta) {
+            const Unit un = unit_of(u, p, n_st);
+            const int4 t = p.tiles[un.tile];
+            if (!tile_ok(t, p)) continue;
+            const int wrow = un.mb * kWeightTileRows + quad * 32 + lane;
+            const bool row_ok = wrow < p.w_rows;
+            // rows past the matrix are TMA zero-fill: scale 1 keeps them zero
+            const uint8_t* srow =
+                p.scales + (static_cast<size_t>(t.x) * p.w_rows + (row_ok ? wrow : 0)) * p.kscale;
+            for (int st = un.st_lo; st < un.st_hi; ++st) {
+                if (!warp_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
+                    if (lane == 0) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = sf_col0 + 8u * static_cast<uint32_t>(stage);
+                uint32_t va = 0x7F7F7F7Fu;
+                if (row_ok) {
+                    // kscale = K / 32 is even and so is 2c: two aligned halves
+                    const uint16_t* s16 =
+                        reinterpret_cast<const uint16_t*>(srow + 2 * min(2 * st, p.mx_cmax));
+                    va = static_cast<uint32_t>(__ldg(s16)) |
+                         (static_cast<uint32_t>(__ldg(s16 + 1)) << 16);
+                }
+                tmem_st1(lane_base + col + static_cast<uint32_t>(quad), va);
+                uint32_t vb[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int n = 32 * j + lane;
+                    vb[j] = 0x7C7C7C7Cu;                      // h operand: 2^-3
+                    if (p.xs_mx != nullptr)
+                        vb[j] = n < t.z ? __ldg(reinterpret_cast<const uint32_t*>(
+                                              p.xs_mx +
+                                              static_cast<size_t>(t.y + n) * p.xs_row_bytes +
+                                              4 * st))
+                                        : 0x7F7F7F7Fu;
+                }
+                tmem_st4(lane_base + col + 4u, vb[0], vb[1], vb[2], vb[3]);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(sm.full + stage));
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
     } else if (WF == 1) {
@@ -1020,7 +1124,7 @@ cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUte
                         bool pdl) {
     if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
     if (cg == 2) {
-        if (wf == 1) return cudaErrorInvalidValue;
+        if (wf == 1 || wf == 3) return cudaErrorInvalidValue;
         if (wf == 2)
             return epi == kEpiGlu
                        ? launch_gemm_t<kEpiGlu, 2, 2>(p, tmap_w, tmap_x, grid, smem, s, pdl)
@@ -1033,6 +1137,10 @@ cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUte
         return epi == kEpiGlu
                    ? launch_gemm_t<kEpiGlu, 2, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
                    : launch_gemm_t<kEpiCombine, 2, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl);
+    if (wf == 3)
+        return epi == kEpiGlu
+                   ? launch_gemm_t<kEpiGlu, 3, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
+                   : launch_gemm_t<kEpiCombine, 3, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl);
     if (epi == kEpiGlu)
         return wf == 1 ? launch_gemm_t<kEpiGlu, 1, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl)
                        : launch_gemm_t<kEpiGlu, 0, 1>(p, tmap_w, tmap_x, grid, smem, s, pdl);

@@ -69,18 +69,38 @@ moe_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 
 // Every map uses the 128-byte swizzle: box inner extent 128 B (64 bf16
 // elements, or 128 MXFP4 code bytes = 4 k-blocks of one row).
-moe_status make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-                     const cuuint64_t* strides, const cuuint32_t* box, bool bytes = false) {
+moe_status make_tmap_dt(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank,
+                        const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     moe_status st = encode_fn(&enc);
     if (st != MOE_OK) return st;
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                     static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box,
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box,
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides, const cuuint32_t* box, bool bytes = false) {
+    return make_tmap_dt(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        base, rank, dims, strides, box);
+}
+
+// MXFP4 codes [E, rows, K/2] for the block-scaled MMA: a 4-D view (element
+// in chunk, chunk, row, expert) whose chunks of 128 E2M1 codes start every
+// 64 elements (stride 32 B, overlapping), so that the K range's last 128
+// codes form a chunk even when K = 128 m + 64.  The 4-bit type with 16-byte
+// alignment makes TMA spread every 8 bytes of codes over 16 bytes of shared
+// memory, the form the MMA reads; box 128 codes x 1 chunk x 128 rows.
+moe_status mx_weight_tmap(CUtensorMap* m, const void* w, int E, int rows, int K) {
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(K) / 2;
+    const cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(K / 64 - 1),
+                                static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(E)};
+    const cuuint64_t str[3] = {32, row_bytes, row_bytes * static_cast<cuuint64_t>(rows)};
+    const cuuint32_t boxd[4] = {128u, 1u, 128u, 1u};
+    return make_tmap_dt(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, 4, dims, str, boxd);
 }
 
 // 3-D map over one expert weight bank [E, rows, K]: bf16 values (box 64 K
@@ -169,12 +189,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 moe_status check_shape(const moe_shape* s) {
     if (!s) return MOE_ERR_ARG;
-    if (s->wfmt != MOE_W_BF16 && s->wfmt != MOE_W_MXFP4 && s->wfmt != MOE_W_FP8) return MOE_ERR_ARG;
+    if (s->wfmt != MOE_W_BF16 && s->wfmt != MOE_W_MXFP4 && s->wfmt != MOE_W_FP8 &&
+        s->wfmt != MOE_W_MXFP4_MXFP8)
+        return MOE_ERR_ARG;
     if (s->T < 0 || s->T > (1 << 20)) return MOE_ERR_SHAPE;
     if (s->H <= 0 || s->H % 64 || s->H > 32768) return MOE_ERR_SHAPE;
     if (s->I <= 0 || s->I % 64 || s->I > 32768) return MOE_ERR_SHAPE;
     if (s->E < 1 || s->E > kMaxExperts) return MOE_ERR_SHAPE;
     if (s->top_k < 1 || s->top_k > kMaxTopK || s->top_k > s->E) return MOE_ERR_SHAPE;
+    // MXFP8 activations: the weights' chunk view needs K >= 128
+    if (s->wfmt == MOE_W_MXFP4_MXFP8 && (s->H < 128 || s->I < 128)) return MOE_ERR_SHAPE;
     return MOE_OK;
 }
 
@@ -217,7 +241,10 @@ int auto_token_tile(const moe_shape& s) {
     }
     if (t < 16) t = 16;
     if (t > kMaxTokenTile) t = kMaxTokenTile;
-    if (s.wfmt == MOE_W_MXFP4 && t > kMxfp4MaxTokenTile) t = kMxfp4MaxTokenTile;
+    // MXFP4 (TMEM A slots) and MXFP4 x MXFP8 (TMEM scale slots) share 512
+    // TMEM columns with the two accumulators
+    if ((s.wfmt == MOE_W_MXFP4 || s.wfmt == MOE_W_MXFP4_MXFP8) && t > kMxfp4MaxTokenTile)
+        t = kMxfp4MaxTokenTile;
     return static_cast<int>(t);
 }
 
@@ -318,6 +345,7 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     pp.x_perm = x_perm;
     pp.mx_layout = s.wfmt == MOE_W_MXFP4 ? 1 : 0;
     pp.fp8 = s.wfmt == MOE_W_FP8 ? 1 : 0;
+    pp.mx8 = s.wfmt == MOE_W_MXFP4_MXFP8 ? 1 : 0;
     pp.x_scale = reinterpret_cast<float*>(ws + L.x_scale);
     pp.status = status;
     MOE_CUDA(launch_permute(pp, stream, g_pdl.load() != 0));
@@ -389,10 +417,14 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     MOE_TRY(check_ptr(workspace));
     const bool mxfp4 = s.wfmt == MOE_W_MXFP4;
     const bool fp8 = s.wfmt == MOE_W_FP8;
-    if (mxfp4 || fp8) {
+    const bool mx = s.wfmt == MOE_W_MXFP4_MXFP8;
+    if (mxfp4 || fp8 || mx) {
         MOE_TRY(check_ptr(gate_up.scale));
         MOE_TRY(check_ptr(down.scale));
     }
+    // the 4-bit tensor maps of the block-scaled path want 32-byte alignment
+    if (mx && ((reinterpret_cast<uintptr_t>(gate_up.w) | reinterpret_cast<uintptr_t>(down.w)) & 31))
+        return MOE_ERR_ALIGN;
     if ((topk_ids_out && !aligned16(topk_ids_out)) || (topk_w_out && !aligned16(topk_w_out)))
         return MOE_ERR_ALIGN;
     const WsLayout L = ws_layout(s.T, s.H, s.I, s.E, s.top_k);
@@ -413,10 +445,10 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     const bool pair_auto =
         box >= kPairMinBox &&
         (!fp8 || static_cast<long long>(R) < kFp8PairMaxMeanRows * s.E);
-    const bool pair = !mxfp4 && (pair_mode == 2 || (pair_mode == 0 && pair_auto));
+    const bool pair = !mxfp4 && !mx && (pair_mode == 2 || (pair_mode == 0 && pair_auto));
     const int bbox = pair ? box / 2 : box;     // token rows of one CTA's B tile
     // Pipeline depth: as many stages as the shared memory allows (2..12).
-    const int wf = mxfp4 ? 1 : fp8 ? 2 : 0;
+    const int wf = mxfp4 ? 1 : fp8 ? 2 : mx ? 3 : 0;
     const int kscale_max = (s.H > s.I ? s.H : s.I) / 32;
     const size_t stage_bytes = gemm_stage_bytes(bbox, wf);
     const size_t budget = static_cast<size_t>(dev.max_smem) - 1024;
@@ -442,10 +474,15 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     if (stages < 2 || (mxfp4 && 2 * stages < astages + 2)) return MOE_ERR_UNSUPPORTED;
     const int max_stages = mxfp4 ? 24 : 12;   // MXFP4 slots carry 4 KB of HBM bytes
     if (stages > max_stages) stages = max_stages;
+    // MXFP4 x MXFP8: 8 TMEM scale columns per ring slot after the two
+    // accumulators of round_up(box, 32) columns
+    const int mx_acc = (box + 31) & ~31;
+    if (mx && stages > (512 - 2 * mx_acc) / 8) stages = (512 - 2 * mx_acc) / 8;
+    if (stages < 2) return MOE_ERR_UNSUPPORTED;
     const size_t smem = fixed + stages * stage_bytes + 1024;
     // two accumulators (+ MXFP4: A tiles of 32 columns after them)
     const int tmem_cols =
-        mxfp4 ? 512 : next_pow2(2 * box < 32 ? 32 : 2 * box);
+        mxfp4 ? 512 : mx ? next_pow2(2 * mx_acc + 8 * stages) : next_pow2(2 * box < 32 ? 32 : 2 * box);
     if (tmem_cols > 512) return MOE_ERR_UNSUPPORTED;
 
     __nv_bfloat16* x_perm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm);
@@ -454,8 +491,13 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
 
     // Tensor maps (host-side descriptors; cheap to build per call).
     CUtensorMap tm_wgu, tm_x, tm_wd, tm_h;
-    MOE_TRY(weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H, mxfp4, fp8));
-    MOE_TRY(weight_tmap(&tm_wd, down.w, s.E, s.H, s.I, mxfp4, fp8));
+    if (mx) {
+        MOE_TRY(mx_weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H));
+        MOE_TRY(mx_weight_tmap(&tm_wd, down.w, s.E, s.H, s.I));
+    } else {
+        MOE_TRY(weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H, mxfp4, fp8));
+        MOE_TRY(weight_tmap(&tm_wd, down.w, s.E, s.H, s.I, mxfp4, fp8));
+    }
     // Token operands: bf16 layers read [R, K] row-major, one 64-wide K chunk
     // per box; MXFP4 layers read the chunk-major [K/64, R, 64] layout the
     // gather and the GLU epilogue write, kMxfp4KbPerStage chunks per box.
@@ -466,6 +508,15 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
             const cuuint64_t str[2] = {128, static_cast<cuuint64_t>(R) * 128};
             const cuuint32_t boxd[3] = {64, static_cast<cuuint32_t>(box), kMxfp4KbPerStage};
             return make_tmap(m, base, 3, dims, str, boxd);
+        }
+        if (mx) {
+            // E4M3 codes [R, mx_padded_k(K)], one byte each: box 128 K x box rows
+            const cuuint64_t kp = static_cast<cuuint64_t>(mx_padded_k(K));
+            const cuuint64_t dims[2] = {kp, static_cast<cuuint64_t>(R)};
+            const cuuint64_t str[1] = {kp};
+            const cuuint32_t boxd[2] = {static_cast<cuuint32_t>(kBlockKFp8),
+                                        static_cast<cuuint32_t>(bbox)};
+            return make_tmap(m, base, 2, dims, str, boxd, true);
         }
         if (fp8) {
             // E4M3 codes [R, K], one byte each: box 128 K x box rows
@@ -513,7 +564,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.n_wblocks = (2 * s.I + unit_rows - 1) / unit_rows;
     // k-blocks of 64 bf16 / E4M3: 128 (a K tail past the last full block is
     // zero-filled by TMA)
-    g.k_blocks = fp8 ? (s.H + kBlockKFp8 - 1) / kBlockKFp8 : s.H / kBlockK;
+    g.k_blocks = (fp8 || mx) ? (s.H + kBlockKFp8 - 1) / kBlockKFp8 : s.H / kBlockK;
     g.w_rows = 2 * s.I;
     g.bias = static_cast<const __nv_bfloat16*>(gate_up.bias);
     g.h = h;
@@ -523,6 +574,11 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.h8 = reinterpret_cast<uint8_t*>(h);
     g.hscale = kFp8HScale;
     g.kscale = s.H / 32;
+    g.mx_cmax = s.H / 64 - 2;
+    g.xs_mx = mx ? reinterpret_cast<const uint8_t*>(ws + L.x_scale) : nullptr;
+    g.xs_row_bytes = mx_padded_k(s.H) / 32;
+    g.h_pad = mx_padded_k(s.I);
+    g.h_tail0 = mx_tail0(s.I);
     // K split when the units cannot fill two waves (small batches)
     const int kb_per_slot = mxfp4 ? kMxfp4KbPerStage : 1;
     const long long tiles_max = max_token_tiles(R, L.max_tiles);
@@ -566,7 +622,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
 
     // down + bias + weighted combine -> out (fp32 accumulation)
     g.n_wblocks = (s.H + unit_rows - 1) / unit_rows;
-    g.k_blocks = fp8 ? (s.I + kBlockKFp8 - 1) / kBlockKFp8 : s.I / kBlockK;
+    g.k_blocks = (fp8 || mx) ? (s.I + kBlockKFp8 - 1) / kBlockKFp8 : s.I / kBlockK;
     g.w_rows = s.H;
     g.bias = static_cast<const __nv_bfloat16*>(down.bias);
     g.h = nullptr;
@@ -577,6 +633,8 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.scales = static_cast<const uint8_t*>(down.scale);
     g.wscale = fp8 ? static_cast<const float*>(down.scale) : nullptr;
     g.kscale = s.I / 32;
+    g.mx_cmax = s.I / 64 - 2;
+    g.xs_mx = nullptr;                      // h codes: every block scale 2^-3
     // the down projection adds its K parts through the output's atomics
     g.ksplit = pair ? 1 : parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, kMaxKSplit);
     g.partial = nullptr;

@@ -97,6 +97,17 @@ inline int router_ksplit(int pairs, int nchunks) {
     return (nchunks + per - 1) / per;              // no empty slice
 }
 
+// MXFP4 weights x MXFP8 activations: token operands hold K padded to a
+// multiple of 128.  When K = 128 m + 64, the last 128-wide k-block holds 64
+// zero codes, then the last 64 elements: the weights' last k-block is read
+// through an overlapping chunk view that starts 64 elements early, so its
+// first half (already counted) meets the zeros.
+__host__ __device__ inline int mx_padded_k(int K) { return (K + 127) / 128 * 128; }
+// position of element k of a row in that padded layout (tail0 = K rounded
+// down to 128 when K % 128 == 64, else K)
+__host__ __device__ inline int mx_tail0(int K) { return K % 128 ? K / 128 * 128 : K; }
+__host__ __device__ inline int mx_pos(int k, int tail0) { return k < tail0 ? k : k + 64; }
+
 struct WsLayout {
     size_t status, topk_ids, topk_w, blk_cnt, logits, partials, counters, offsets, gemm_partial;
     size_t sorted_assign, assign_row, tiles, x_perm, x_scale, h, out_acc, total;
@@ -131,7 +142,9 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
     L.assign_row = take(R * 4);
     L.tiles = take(static_cast<size_t>(L.max_tiles) * 16);
     L.x_perm = take(R * H * 2);            // bf16, or E4M3 codes (FP8)
-    L.x_scale = take(R * 4);               // FP8: scale of each routed row
+    // FP8: fp32 scale of each routed row; MXFP4 x MXFP8: UE8M0 block scales
+    // [T*k][mx_padded_k(H) / 32]
+    L.x_scale = take(R * (mx_padded_k(H) / 32 > 4 ? mx_padded_k(H) / 32 : 4));
     L.h = take(R * I * 2);
     L.out_acc = take(static_cast<size_t>(T) * H * 4);
     // gate_up K-split partial tiles, fp32 [part][weight block][routed row][128].
@@ -199,6 +212,9 @@ struct PermuteParams {
                                  // in the order 0,4,1,5,2,6,3,7
     int fp8;                     // FP8 W8A8: x_perm holds E4M3 codes [T*k, H]
     float* x_scale;              // FP8: [T*k] scale of each routed row's codes
+    int mx8;                     // MXFP8 activations: x_perm holds E4M3 codes
+                                 // [T*k, mx_padded_k(H)] and x_scale UE8M0
+                                 // bytes [T*k, mx_padded_k(H) / 32]
     int32_t* status;
 };
 
@@ -231,6 +247,15 @@ struct GemmParams {
     const float* xscale;
     uint8_t* h8;
     float hscale;
+    // MXFP4 x MXFP8 (WF = 3): weights through the chunk view (the last
+    // chunk index is mx_cmax = K/64 - 2); token operand scales UE8M0
+    // [rows_total, xs_row_bytes] (null: every block scale 2^-3, the h
+    // operand); gate_up stores h codes [T*k, h_pad] (positions mx_pos)
+    int mx_cmax;
+    const uint8_t* xs_mx;
+    int xs_row_bytes;
+    int h_pad;
+    int h_tail0;
     // kEpiCombine: out[t, w_rows] += w * y
     float* out;
     const int32_t* sorted_assign;
@@ -260,6 +285,7 @@ inline size_t gemm_stage_bytes(int token_box, int wf) {
     size_t a = static_cast<size_t>(kWeightTileRows) * kBlockK * 2;
     size_t b = static_cast<size_t>(token_box) * kBlockK * 2;
     size_t codes = static_cast<size_t>(kWeightTileRows) * kBlockK / 2;
+    // FP8 and MXFP4 x MXFP8: 128-wide k-blocks of byte codes, the same bytes
     return wf == 1 ? kMxfp4KbPerStage * (codes + b) : a + b;
 }
 inline size_t gemm_fixed_bytes(int token_box, int wf, int kscale) {

@@ -20,6 +20,9 @@
 //      order in which the GEMM expands E2M1 codes).  With FP8 W8A8 weights
 //      the row is quantised on the way: E4M3 codes of x * (448 / max|x|)
 //      with the token's own max|x|, and the row's scale max|x| / 448.
+//      With MXFP8 activations every block of 32 elements is quantised by the
+//      OCP MX rule (scale 2^(floor(log2 max|x|) - 8) as a UE8M0 byte, codes
+//      E4M3 of x / scale) into the padded layout of mx_pos.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "../../include/moe.h"
@@ -162,6 +165,36 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
             const int row = rows_s[la];
             if (row < 0) continue;
             const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>((a0 + la) / k) * p.H);
+            if (p.mx8) {
+                // MXFP8: a block of 32 elements is the 4 vectors of 4
+                // adjacent lanes (the loop stays warp-uniform for the shuffles)
+                const int kp = mx_padded_k(p.H), tail0 = mx_tail0(p.H);
+                uint8_t* dst8 = reinterpret_cast<uint8_t*>(p.x_perm) + static_cast<size_t>(row) * kp;
+                uint8_t* dsts =
+                    reinterpret_cast<uint8_t*>(p.x_scale) + static_cast<size_t>(row) * (kp / 32);
+                for (int v0 = 0; v0 < vec_per_row; v0 += 32) {
+                    const int v = v0 + lane;
+                    const bool valid = v < vec_per_row;
+                    const uint4 x8 = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+                    float m = absmax8(x8);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    if (!valid) continue;
+                    // floor(log2 m) = biased exponent - 127 (0 for zero and
+                    // subnormal m: the scale then clamps at 2^-127, byte 0)
+                    const int ex = static_cast<int>(__float_as_uint(m) >> 23);
+                    const int sbyte = ex > 8 ? ex - 8 : 0;
+                    const float inv = __uint_as_float(static_cast<uint32_t>(254 - sbyte) << 23);
+                    const int k0 = 8 * v;
+                    *reinterpret_cast<uint2*>(dst8 + mx_pos(k0, tail0)) = e4m3x8(x8, inv);
+                    if (k0 >= tail0) *reinterpret_cast<uint2*>(dst8 + k0) = make_uint2(0u, 0u);
+                    if ((lane & 3) == 0) {
+                        dsts[mx_pos(k0, tail0) / 32] = static_cast<uint8_t>(sbyte);
+                        if (k0 >= tail0) dsts[k0 / 32] = 127;     // the gap's blocks: scale 1
+                    }
+                }
+                continue;
+            }
             if (p.fp8) {
                 // FP8 W8A8: the token's own scale, max|x| / 448, then the row
                 // as E4M3 codes of x * (448 / max|x|) (1 for an all-zero row)

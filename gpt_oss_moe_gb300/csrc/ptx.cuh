@@ -212,6 +212,17 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // ---------------------------------------------------------------- tcgen05
 
 // Warp-wide: allocates `ncols` TMEM columns, writes the base address to smem.
+// 4-D tile load (MXFP4 codes through an overlapping 64-element chunk view).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* desc, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1),
+          "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+
 // CG = 2: one warp of each CTA of a pair allocates, together, the same
 // columns in both CTAs.  A kernel uses one CTA group for all its tcgen05
 // allocation, MMA and commit instructions.
@@ -268,6 +279,28 @@ __device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t adesc, uin
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= (A[smem] x scale_A) * (B[smem] x scale_B)^T with MX block
+// scaling (kind::mxf8f6f4, scale_vec::1X: one UE8M0 byte per 32 K elements of
+// every A row and B row, K = 32 per instruction), fp32 accumulator.  A holds
+// E2M1 codes in the 16-byte-padded shared-memory form (16 codes in the first
+// 8 bytes of every 16, as TMA writes them for CU_TENSOR_MAP_DATA_TYPE_
+// 16U4_ALIGN16B), addressed like one byte per element; B holds E4M3 codes.
+// Scales in TMEM (measured on sm_103a): A row m at lane m, column
+// sfa + m / 32; B row n at lane 32 q + n % 32, column sfb + n / 32, in every
+// lane quadrant q (the rows of A in quadrant q read B's scales from q); the
+// byte of the 32-bit cell is the instruction descriptor's scale id.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
         : "memory");
 }
 
@@ -358,6 +391,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
           "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+// 32 lanes x 32 bit, one / four consecutive columns per thread.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                         uint32_t r3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(taddr), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -391,6 +434,20 @@ __host__ __device__ __forceinline__ uint32_t idesc_e4m3_f32(uint32_t M, uint32_t
     return (1u << 4)            // D = f32
          | ((N >> 3) << 17)
          | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: E2M1 A
+// (format 5), E4M3 B (format 0), both K-major, UE8M0 scales (bit 23), scale
+// byte `sf` of the A and B cells (bits 29-30 and 4-5).
+__host__ __device__ __forceinline__ uint32_t idesc_mx_e2m1_e4m3(uint32_t M, uint32_t N,
+                                                                uint32_t sf) {
+    return (sf << 4)            // B scale byte
+         | (5u << 7)            // A = E2M1
+         | (0u << 10)           // B = E4M3
+         | ((N >> 3) << 17)
+         | (1u << 23)           // UE8M0 scales
+         | ((M >> 4) << 24)
+         | (sf << 29);          // A scale byte
 }
 
 // Two fp32 values to two E4M3 codes (round to nearest even, magnitudes past

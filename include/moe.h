@@ -64,7 +64,7 @@ typedef enum {
                          the low nibble of byte i), plus one E8M0 scale byte
                          (value 2^(s-127)) per 32 consecutive input elements
                          of each output row (§5 "量化") */
-    MOE_W_FP8 = 2     /* FP8 W8A8 (§5 "量化"): E4M3 codes ("fn": max 448),
+    MOE_W_FP8 = 2,    /* FP8 W8A8 (§5 "量化"): E4M3 codes ("fn": max 448),
                          one byte per weight, [E, N, K] like bf16, and
                          moe_weight.scale = fp32 [E], one scale per expert,
                          applied to the finished products.  The layer
@@ -72,6 +72,16 @@ typedef enum {
                          its own scale max|x| / 448 (round to nearest even,
                          saturating), h with the fixed scale 1/8 (the GLU
                          clamps keep |h| * 8 <= 448) */
+    MOE_W_MXFP4_MXFP8 = 3 /* MXFP4 weights exactly as MOE_W_MXFP4 (codes
+                         32-byte aligned), with the activations quantised
+                         by the layer to MXFP8 (OCP MX): every block of 32
+                         consecutive elements of a token gets the scale
+                         2^(floor(log2 max|x|) - 8) (a UE8M0 byte, at least
+                         2^-127) and E4M3 codes of x / scale (round to
+                         nearest even, saturating); h likewise with every
+                         block scale 1/8.  The GEMMs run on the tensor cores'
+                         block-scaled MMA, with no software dequantisation.
+                         Needs H, I >= 128 */
 } moe_wfmt;
 
 /* Layer shape.  T tokens, hidden size H, expert intermediate size I,
@@ -89,7 +99,7 @@ typedef struct {
  *   down:    w bf16 [E, H, I] or codes u8 [E, H, I/2], scale u8 [E, H, I/32],
  *            or FP8 codes u8 [E, H, I] with scale fp32 [E];
  *            bias bf16 [E, H].
- * scale is NULL for bf16 weights. */
+ * MOE_W_MXFP4_MXFP8 takes the MXFP4 bank.  scale is NULL for bf16 weights. */
 typedef struct {
     const void* w;
     const void* scale;
@@ -187,8 +197,8 @@ moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
 
 /* Process-wide tuning switches for tests and benchmarks:
  *   "token_tile": rows of tokens per GEMM tile, 0 = automatic, else a
- *                 multiple of 16 in [16, 256] (MXFP4 layers use at most
- *                 128);
+ *                 multiple of 16 in [16, 256] (MXFP4 and MXFP4 x MXFP8
+ *                 layers use at most 128);
  *   "pdl":        1 = launch dependent kernels with programmatic dependent
  *                 launch (default), 0 = plain stream order;
  *   "ksplit":     0 = split the GEMMs' K range when a small batch leaves

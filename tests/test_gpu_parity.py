@@ -489,6 +489,70 @@ def test_forward_20b_mxfp4(moe, oracle_lib, layer_20b_mxfp4, T):
     _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample, tol=TOL_MXFP4)
 
 
+# ------------------------------------------- MXFP4 weights, MXFP8 activations
+
+MX_CASES = [
+    # E, k, H, I, T, token_tile
+    (8, 2, 128, 128, 1, 0),
+    (8, 4, 320, 192, 37, 0),        # K = 128 m + 64 on both GEMMs: the chunk view's tail
+    (4, 2, 192, 128, 700, 0),       # several token tiles per expert
+    (8, 4, 256, 256, 200, 48),
+    (8, 4, 256, 256, 200, 16),
+    (8, 4, 448, 320, 130, 128),     # widest MX token box
+    (32, 4, 2880, 2880, 5, 0),      # 2880 = 22.5 k-blocks of 128
+]
+
+
+@pytest.mark.parametrize("case", MX_CASES, ids=lambda c: "E{}k{}H{}I{}T{}tile{}".format(*c))
+def test_forward_mxfp8_small_shapes(moe, oracle_lib, synth_lib, case):
+    E, k, H, I, T, tile = case
+    L = synth_lib.make_layer(E=E, T=T, H=H, I=I, top_k=k, seed=600 + T, wfmt="mxfp4_mxfp8",
+                             router_w_std=0.05)
+    moe.moe_set_tuning("token_tile", tile)
+    try:
+        _check(moe, oracle_lib, L)
+    finally:
+        moe.moe_set_tuning("token_tile", 0)
+
+
+@pytest.mark.parametrize("parts", [3, 8])
+def test_mxfp8_fixed_ksplit(moe, oracle_lib, synth_lib, parts):
+    L = synth_lib.make_layer(E=8, T=9, H=1024, I=768, top_k=2, seed=640 + parts,
+                             wfmt="mxfp4_mxfp8", router_w_std=0.05)
+    moe.moe_set_tuning("ksplit", parts)
+    try:
+        _check(moe, oracle_lib, L)
+    finally:
+        moe.moe_set_tuning("ksplit", 0)
+
+
+def test_mxfp8_outliers_and_zero_rows(moe, oracle_lib, synth_lib):
+    """Per-block scales: 20x outliers, an all-zero token and a token whose
+    blocks span many binades."""
+    L = synth_lib.make_layer(E=8, T=20, H=256, I=192, top_k=2, seed=611, wfmt="mxfp4_mxfp8",
+                             router_w_std=0.05, p_outlier=0.05)
+    L.x = L.x.clone()
+    L.x[3] = 0
+    L.x[5] = (L.x[5].float() * torch.exp2(torch.arange(256).float() / 16 - 8)).to(torch.bfloat16)
+    _check(moe, oracle_lib, L)
+
+
+@pytest.fixture(scope="module")
+def layer_20b_mxfp8(synth_lib):
+    L = synth_lib.make_workload("20b_mxfp4_mxfp8", 512)
+    return L, to_device(L)
+
+
+@pytest.mark.parametrize("T", [1, 64, 512])
+def test_forward_20b_mxfp4_mxfp8(moe, oracle_lib, layer_20b_mxfp8, T):
+    L, dev = layer_20b_mxfp8
+    sample = None
+    if T > 64:
+        g = torch.Generator().manual_seed(T)
+        sample = [0, T - 1] + torch.randint(0, T, (30,), generator=g).tolist()
+    _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample)
+
+
 def test_one_workspace_serves_successive_shapes(moe, synth_lib):
     """A workspace sized for the largest call is reused for smaller ones
     (other token counts shift every region but the status word and the
