@@ -53,6 +53,8 @@ DESCRIPTIONS = {
                   "near-uniform routing, seed 3",
     "20b_mxfp4": "gpt-oss-20b MoE layer, MXFP4 expert weights, T={T}, seed 4",
     "20b_fp8": "gpt-oss-20b MoE layer, FP8 W8A8 (E4M3 weights, per-expert scales; per-token E4M3 activations), T={T}, seed 5",
+    "20b_mxfp4_mxfp8": "gpt-oss-20b MoE layer, MXFP4 expert weights (those of 20b_mxfp4) with "
+                       "MXFP8 activations on the block-scaled MMA, T={T}, seed 4",
 }
 
 
@@ -208,7 +210,8 @@ def base_record(args, n_gpus, workload_desc, layer):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": {"bf16": "bf16", "mxfp4": "mxfp4-weights/bf16-activations",
-                  "fp8": "e4m3-weights/e4m3-activations"}[layer.wfmt],
+                  "fp8": "e4m3-weights/e4m3-activations",
+                  "mxfp4_mxfp8": "mxfp4-weights/mxfp8-activations"}[layer.wfmt],
         "data": "synthetic: seeded gpt-oss-shaped layer, random-init weights (no checkpoint)",
         "config": {"workload": workload_desc, "T": layer.T, "H": layer.H, "I": layer.I,
                    "E": layer.E, "top_k": layer.top_k, "weights": layer.wfmt,
@@ -376,10 +379,13 @@ def main():
         gu_b, d_b = GU_BYTES_FP8(H, I), D_BYTES_FP8(H, I)
     else:
         gu_b, d_b = GU_BYTES_MXFP4(H, I), D_BYTES_MXFP4(H, I)
-    # activation and h bytes per element: E4M3 codes for FP8 W8A8, else bf16
-    ab = 1 if layer.wfmt == "fp8" else 2
+    # activation and h bytes per element: E4M3 codes for FP8 W8A8 and MXFP8
+    # (plus one scale byte per 32 for MXFP8 activations), else bf16
+    ab = 1 if layer.wfmt in ("fp8", "mxfp4_mxfp8") else 2
     gu_alg = U * gu_b + R * H * ab + R * I * ab
-    if layer.wfmt == "fp8":
+    if layer.wfmt == "mxfp4_mxfp8":
+        gu_alg += R * H // 32
+    if layer.wfmt in ("fp8", "mxfp4_mxfp8"):
         # an E4M3 contraction's peak: the measured bf16 rate x the nominal
         # dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
         tf_burst, tf_sust = 2.0 * tf_burst, 2.0 * tf_sust

@@ -877,28 +877,20 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             // rows past the matrix are TMA zero-fill: scale 1 keeps them zero
             const uint8_t* srow =
                 p.scales + (static_cast<size_t>(t.x) * p.w_rows + (row_ok ? wrow : 0)) * p.kscale;
-            for (int st = un.st_lo; st < un.st_hi; ++st) {
-                if (!warp_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
-                    if (lane == 0) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t col = sf_col0 + 8u * static_cast<uint32_t>(stage);
-                uint32_t va = 0x7F7F7F7Fu;
+            // the scale values of slot st (weight rows: two aligned halves, as
+            // kscale = K / 32 and 2c are even; token rows, or 2^-3 for h)
+            const auto load_vals = [&](int st, uint32_t& va, uint32_t (&vb)[4]) {
+                va = 0x7F7F7F7Fu;
                 if (row_ok) {
-                    // kscale = K / 32 is even and so is 2c: two aligned halves
                     const uint16_t* s16 =
                         reinterpret_cast<const uint16_t*>(srow + 2 * min(2 * st, p.mx_cmax));
                     va = static_cast<uint32_t>(__ldg(s16)) |
                          (static_cast<uint32_t>(__ldg(s16 + 1)) << 16);
                 }
-                tmem_st1(lane_base + col + static_cast<uint32_t>(quad), va);
-                uint32_t vb[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int n = 32 * j + lane;
-                    vb[j] = 0x7C7C7C7Cu;                      // h operand: 2^-3
+                    vb[j] = 0x7C7C7C7Cu;
                     if (p.xs_mx != nullptr)
                         vb[j] = n < t.z ? __ldg(reinterpret_cast<const uint32_t*>(
                                               p.xs_mx +
@@ -906,6 +898,20 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                                               4 * st))
                                         : 0x7F7F7F7Fu;
                 }
+            };
+            for (int st = un.st_lo; st < un.st_hi; ++st) {
+                // the slot's values first: their loads overlap the wait (loading
+                // one slot further ahead measured slower)
+                uint32_t va, vb[4];
+                load_vals(st, va, vb);
+                if (!warp_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
+                    if (lane == 0) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = sf_col0 + 8u * static_cast<uint32_t>(stage);
+                tmem_st1(lane_base + col + static_cast<uint32_t>(quad), va);
                 tmem_st4(lane_base + col + 4u, vb[0], vb[1], vb[2], vb[3]);
                 tmem_wait_st();
                 tc_fence_before();

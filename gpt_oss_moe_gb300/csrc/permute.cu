@@ -167,45 +167,79 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
             const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>((a0 + la) / k) * p.H);
             if (p.mx8) {
                 // MXFP8: a block of 32 elements is the 4 vectors of 4
-                // adjacent lanes (the loop stays warp-uniform for the shuffles)
+                // adjacent lanes; kRowVecUnroll vectors per lane are loaded
+                // before any is used (loads in flight), and the shuffles run
+                // in every lane (the batch's bounds are warp-uniform)
                 const int kp = mx_padded_k(p.H), tail0 = mx_tail0(p.H);
                 uint8_t* dst8 = reinterpret_cast<uint8_t*>(p.x_perm) + static_cast<size_t>(row) * kp;
                 uint8_t* dsts =
                     reinterpret_cast<uint8_t*>(p.x_scale) + static_cast<size_t>(row) * (kp / 32);
-                for (int v0 = 0; v0 < vec_per_row; v0 += 32) {
-                    const int v = v0 + lane;
-                    const bool valid = v < vec_per_row;
-                    const uint4 x8 = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
-                    float m = absmax8(x8);
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    if (!valid) continue;
-                    // floor(log2 m) = biased exponent - 127 (0 for zero and
-                    // subnormal m: the scale then clamps at 2^-127, byte 0)
-                    const int ex = static_cast<int>(__float_as_uint(m) >> 23);
-                    const int sbyte = ex > 8 ? ex - 8 : 0;
-                    const float inv = __uint_as_float(static_cast<uint32_t>(254 - sbyte) << 23);
-                    const int k0 = 8 * v;
-                    *reinterpret_cast<uint2*>(dst8 + mx_pos(k0, tail0)) = e4m3x8(x8, inv);
-                    if (k0 >= tail0) *reinterpret_cast<uint2*>(dst8 + k0) = make_uint2(0u, 0u);
-                    if ((lane & 3) == 0) {
-                        dsts[mx_pos(k0, tail0) / 32] = static_cast<uint8_t>(sbyte);
-                        if (k0 >= tail0) dsts[k0 / 32] = 127;     // the gap's blocks: scale 1
+                for (int v0 = 0; v0 < vec_per_row; v0 += 32 * kRowVecUnroll) {
+                    uint4 buf[kRowVecUnroll];
+#pragma unroll
+                    for (int u = 0; u < kRowVecUnroll; ++u) {
+                        const int v = v0 + u * 32 + lane;
+                        buf[u] = v < vec_per_row ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kRowVecUnroll; ++u) {
+                        if (v0 + u * 32 >= vec_per_row) break;        // warp-uniform
+                        const int v = v0 + u * 32 + lane;
+                        float m = absmax8(buf[u]);
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                        if (v >= vec_per_row) continue;
+                        // floor(log2 m) = biased exponent - 127 (0 for zero and
+                        // subnormal m: the scale then clamps at 2^-127, byte 0)
+                        const int ex = static_cast<int>(__float_as_uint(m) >> 23);
+                        const int sbyte = ex > 8 ? ex - 8 : 0;
+                        const float inv = __uint_as_float(static_cast<uint32_t>(254 - sbyte) << 23);
+                        const int k0 = 8 * v;
+                        *reinterpret_cast<uint2*>(dst8 + mx_pos(k0, tail0)) = e4m3x8(buf[u], inv);
+                        if (k0 >= tail0) *reinterpret_cast<uint2*>(dst8 + k0) = make_uint2(0u, 0u);
+                        if ((lane & 3) == 0) {
+                            dsts[mx_pos(k0, tail0) / 32] = static_cast<uint8_t>(sbyte);
+                            if (k0 >= tail0) dsts[k0 / 32] = 127;   // the gap's blocks: scale 1
+                        }
                     }
                 }
                 continue;
             }
             if (p.fp8) {
                 // FP8 W8A8: the token's own scale, max|x| / 448, then the row
-                // as E4M3 codes of x * (448 / max|x|) (1 for an all-zero row)
+                // as E4M3 codes of x * (448 / max|x|) (1 for an all-zero row).
+                // Rows of up to 32 x kRowVecUnroll vectors stay in registers
+                // (one pass over memory, loads in flight); longer rows are
+                // read twice.
+                uint2* dst8 = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.x_perm) +
+                                                       static_cast<size_t>(row) * p.H);
+                if (vec_per_row <= 32 * kRowVecUnroll) {
+                    uint4 buf[kRowVecUnroll];
+                    float m = 0.f;
+#pragma unroll
+                    for (int u = 0; u < kRowVecUnroll; ++u) {
+                        const int v = u * 32 + lane;
+                        buf[u] = v < vec_per_row ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kRowVecUnroll; ++u) m = fmaxf(m, absmax8(buf[u]));
+#pragma unroll
+                    for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+                    const float inv = m > 0.f ? 448.0f / m : 1.0f;
+                    if (lane == 0) p.x_scale[row] = m > 0.f ? m / 448.0f : 1.0f;
+#pragma unroll
+                    for (int u = 0; u < kRowVecUnroll; ++u) {
+                        const int v = u * 32 + lane;
+                        if (v < vec_per_row) dst8[v] = e4m3x8(buf[u], inv);
+                    }
+                    continue;
+                }
                 float m = 0.f;
                 for (int v = lane; v < vec_per_row; v += 32) m = fmaxf(m, absmax8(src[v]));
 #pragma unroll
                 for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
                 const float inv = m > 0.f ? 448.0f / m : 1.0f;
                 if (lane == 0) p.x_scale[row] = m > 0.f ? m / 448.0f : 1.0f;
-                uint2* dst8 = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.x_perm) +
-                                                       static_cast<size_t>(row) * p.H);
                 for (int v = lane; v < vec_per_row; v += 32) dst8[v] = e4m3x8(src[v], inv);
                 continue;
             }
