@@ -394,9 +394,11 @@ def main():
     flops_tok = 2 * (2 * I) * H + 2 * H * I
     gu_flops = R * 2 * (2 * I) * H
     wl_key = f"{args.workload}_T{T}"
+    # bound: the kernel's algorithmic flops per byte against the ridge of
+    # its own tensor peak (bytes per weight differ between formats)
     ridge = tf_burst * 1e12 / (bw * 1e9)
-    m_per_expert = R / max(U, 1)
-    if m_per_expert < ridge:
+    intensity = gu_flops / max(gu_alg, 1)
+    if intensity < ridge:
         roof = {"bound": "hbm", "achieved": gu_alg / (gu_ms * 1e-3) / 1e9, "peak": bw,
                 "unit": "GB/s"}
     else:
