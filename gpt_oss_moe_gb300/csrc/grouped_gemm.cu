@@ -72,7 +72,7 @@ constexpr uint32_t kATileBytes = kWeightTileRows * kBlockK * 2;      // 16 KB bf
 // two TMA operations of 16 KB codes + 4 token chunks (an SM keeps only about
 // ten TMA operations in flight, so bytes per operation set the bandwidth).
 template <int WF>
-constexpr int kKbPerStage = WF == 1 ? kMxfp4KbPerStage : 1;
+constexpr int kKbPerStage = WF == 1 ? kMxfp4KbPerStage : WF == 3 ? kMxKbPerStage : 1;
 constexpr uint32_t kCodeStageBytes = kWeightTileRows * kMxfp4KbPerStage * kBlockK / 2;  // 16 KB
 constexpr uint32_t kASlotCols = 32u * kMxfp4KbPerStage;    // TMEM columns of one MXFP4 A slot
 constexpr int kMaxStages = 24;
@@ -118,9 +118,10 @@ __device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int asta
     const uint32_t base = smem_u32(raw);
     uint8_t* p = raw + ((1024u - (base & 1023u)) & 1023u);
     s.a = p;
-    p += static_cast<size_t>(wf == 1 ? 0 : stages) * kATileBytes;
+    p += static_cast<size_t>(wf == 1 ? 0 : stages) * (wf == 3 ? kMxKbPerStage : 1) * kATileBytes;
     s.b = p;
-    p += static_cast<size_t>(stages) * (wf == 1 ? kMxfp4KbPerStage : 1) * bbox * 128;
+    p += static_cast<size_t>(stages) * (wf == 1 ? kMxfp4KbPerStage : wf == 3 ? kMxKbPerStage : 1) *
+         bbox * 128;
     s.codes = p;
     s.scales = p;
     if (wf == 1) {
@@ -272,9 +273,9 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     const uint32_t acc_stride = (WF == 1 || WF == 3) ? static_cast<uint32_t>((box + 31) & ~31)
                                                      : static_cast<uint32_t>(p.tmem_cols) / 2u;
     const uint32_t a_col0 = 2u * static_cast<uint32_t>(n_iss) * acc_stride;
-    // MXFP4 x MXFP8: after the two accumulators, 8 scale columns per ring
-    // slot: A (weight rows, column sf + row / 32) at +0..3, B (token rows,
-    // column sf + 4 + row / 32, lanes row % 32) at +4..7
+    // MXFP4 x MXFP8: after the two accumulators, 8 scale columns per
+    // k-block of a ring slot: A (weight rows, column sf + row / 32) at
+    // +0..3, B (token rows, column sf + 4 + row / 32, lanes row % 32) at +4..7
     const uint32_t sf_col0 = 2u * acc_stride;
     // ring sizes the converter teams rely on and the TMEM plan (uniform
     // exit, nothing started)
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         (EPI == kEpiGlu && p.ksplit > 1 && (p.partial == nullptr || p.tickets == nullptr)) ||
         (kPair && (WF == 1 || WF == 3 || p.ksplit != 1 || (gridDim.x & 1u) || (box & 15))) ||
         (WF == 3 && (box > 128 || p.mx_cmax < 0 ||
-                     sf_col0 + 8u * static_cast<uint32_t>(stages) >
+                     sf_col0 + 8u * KPS * static_cast<uint32_t>(stages) >
                          static_cast<uint32_t>(p.tmem_cols))) ||
         (WF == 1 && (astages < 2 || astages > kMxfp4AStages || 2 * stages < astages + 2 ||
                      (n_iss == 2 && (astages & 1)) ||
@@ -392,8 +393,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     const uint32_t fb = smem_u32(sm.full + stage);
                     // full boxes are counted, zero-filled past K included;
                     // pair: the even CTA's barrier counts both CTAs' bytes
+                    // MXFP4 x MXFP8: nk k-blocks (the K range's last slot may
+                    // hold one), 8 KB of codes + the token tile each
+                    const int nk = min(KPS, p.k_blocks - st * KPS);
                     if (rank == 0)
-                        mbar_arrive_expect_tx(fb, (kPair ? 2u : 1u) * (w_bytes + b_stage_bytes));
+                        mbar_arrive_expect_tx(
+                            fb, WF == 3 ? static_cast<uint32_t>(nk) * (kMxCodeTxBytes + b_bytes)
+                                        : (kPair ? 2u : 1u) * (w_bytes + b_stage_bytes));
                     const uint32_t b_dst = smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
                     if (WF == 1) {
                         // codes of k-blocks 4st..4st+3 (128 B per row), and the
@@ -405,10 +411,15 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     } else if (WF == 3) {
                         // E2M1 codes of K 64c..64c+127 (c = 2 st, or the last
                         // chunk starting 64 early), padded by TMA to 128 B rows
-                        tma_load_4d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
-                                    &tmap_w, fb, 0, min(2 * st, p.mx_cmax),
-                                    mb * kWeightTileRows, t.x, pol_w);
-                        tma_load_2d(b_dst, &tmap_x, fb, st * kKB, t.y, pol_x);
+                        for (int jj = 0; jj < nk; ++jj) {
+                            const int kb = st * KPS + jj;
+                            tma_load_4d(smem_u32(sm.a + (static_cast<size_t>(stage) * KPS + jj) *
+                                                            kATileBytes),
+                                        &tmap_w, fb, 0, min(2 * kb, p.mx_cmax),
+                                        mb * kWeightTileRows, t.x, pol_w);
+                            tma_load_2d(b_dst + static_cast<uint32_t>(jj) * b_bytes, &tmap_x, fb,
+                                        kb * kKB, t.y, pol_x);
+                        }
                     } else if (kPair) {
                         // rows 128 * rank.. of the 256-row block; token rows
                         // n/2 * rank.. of the tile (each CTA holds N/2 of B)
@@ -498,8 +509,27 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     const uint64_t bd =
                         smem_desc_sw128(smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes));
                     const uint32_t acc0 = st != un.st_lo ? 1u : 0u;   // the part's first k-block
-                    const uint32_t sfa = tmem_base + sf_col0 + 8u * static_cast<uint32_t>(stage);
-                    if (leader) {
+                    if (WF == 3 && leader) {
+                        // nk k-blocks, each 4 MMAs with scale byte kk of the
+                        // k-block's 8 scale columns
+                        const int nk = min(KPS, p.k_blocks - st * KPS);
+                        for (int jj = 0; jj < nk; ++jj) {
+                            const uint64_t adj = smem_desc_sw128(smem_u32(
+                                sm.a + (static_cast<size_t>(stage) * KPS + jj) * kATileBytes));
+                            const uint64_t bdj = smem_desc_sw128(smem_u32(
+                                sm.b + static_cast<size_t>(stage) * b_stage_bytes +
+                                static_cast<size_t>(jj) * b_bytes));
+                            const uint32_t sfa = tmem_base + sf_col0 +
+                                                 8u * static_cast<uint32_t>(stage * KPS + jj);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc_mma_mx(d_tmem, adj + 2 * kk, bdj + 2 * kk,
+                                          idesc | (static_cast<uint32_t>(kk) << 4) |
+                                              (static_cast<uint32_t>(kk) << 29),
+                                          sfa, sfa + 4u, (jj == 0 && kk == 0) ? acc0 : 1u);
+                        }
+                        tc_commit(smem_u32(sm.empty + stage));
+                    } else if (leader) {
 #pragma unroll
                         for (int kk = 0; kk < kBlockK / 16; ++kk) {
                             const uint32_t acc = kk == 0 ? acc0 : 1u;
@@ -510,11 +540,6 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                                 tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
                             else if constexpr (WF == 2)
                                 tc_mma_e4m3(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
-                            else if constexpr (WF == 3)   // scale byte kk of the slot's cells
-                                tc_mma_mx(d_tmem, ad + 2 * kk, bd + 2 * kk,
-                                          idesc | (static_cast<uint32_t>(kk) << 4) |
-                                              (static_cast<uint32_t>(kk) << 29),
-                                          sfa, sfa + 4u, acc);
                             else
                                 tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
                         }
@@ -877,13 +902,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             // rows past the matrix are TMA zero-fill: scale 1 keeps them zero
             const uint8_t* srow =
                 p.scales + (static_cast<size_t>(t.x) * p.w_rows + (row_ok ? wrow : 0)) * p.kscale;
-            // the scale values of slot st (weight rows: two aligned halves, as
-            // kscale = K / 32 and 2c are even; token rows, or 2^-3 for h)
-            const auto load_vals = [&](int st, uint32_t& va, uint32_t (&vb)[4]) {
+            // the scale values of k-block kb (weight rows: two aligned halves,
+            // as kscale = K / 32 and 2c are even; token rows, or 2^-3 for h)
+            const auto load_vals = [&](int kb, uint32_t& va, uint32_t (&vb)[4]) {
                 va = 0x7F7F7F7Fu;
                 if (row_ok) {
                     const uint16_t* s16 =
-                        reinterpret_cast<const uint16_t*>(srow + 2 * min(2 * st, p.mx_cmax));
+                        reinterpret_cast<const uint16_t*>(srow + 2 * min(2 * kb, p.mx_cmax));
                     va = static_cast<uint32_t>(__ldg(s16)) |
                          (static_cast<uint32_t>(__ldg(s16 + 1)) << 16);
                 }
@@ -895,24 +920,31 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                         vb[j] = n < t.z ? __ldg(reinterpret_cast<const uint32_t*>(
                                               p.xs_mx +
                                               static_cast<size_t>(t.y + n) * p.xs_row_bytes +
-                                              4 * st))
+                                              4 * kb))
                                         : 0x7F7F7F7Fu;
                 }
             };
             for (int st = un.st_lo; st < un.st_hi; ++st) {
                 // the slot's values first: their loads overlap the wait (loading
                 // one slot further ahead measured slower)
-                uint32_t va, vb[4];
-                load_vals(st, va, vb);
+                const int nk = min(KPS, p.k_blocks - st * KPS);
+                uint32_t va[KPS], vb[KPS][4];
+#pragma unroll
+                for (int jj = 0; jj < KPS; ++jj)
+                    if (jj < nk) load_vals(st * KPS + jj, va[jj], vb[jj]);
                 if (!warp_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
                     if (lane == 0) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t col = sf_col0 + 8u * static_cast<uint32_t>(stage);
-                tmem_st1(lane_base + col + static_cast<uint32_t>(quad), va);
-                tmem_st4(lane_base + col + 4u, vb[0], vb[1], vb[2], vb[3]);
+#pragma unroll
+                for (int jj = 0; jj < KPS; ++jj) {
+                    if (jj >= nk) break;
+                    const uint32_t col = sf_col0 + 8u * static_cast<uint32_t>(stage * KPS + jj);
+                    tmem_st1(lane_base + col + static_cast<uint32_t>(quad), va[jj]);
+                    tmem_st4(lane_base + col + 4u, vb[jj][0], vb[jj][1], vb[jj][2], vb[jj][3]);
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();

@@ -474,15 +474,16 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     if (stages < 2 || (mxfp4 && 2 * stages < astages + 2)) return MOE_ERR_UNSUPPORTED;
     const int max_stages = mxfp4 ? 24 : 12;   // MXFP4 slots carry 4 KB of HBM bytes
     if (stages > max_stages) stages = max_stages;
-    // MXFP4 x MXFP8: 8 TMEM scale columns per ring slot after the two
+    // MXFP4 x MXFP8: 8 TMEM scale columns per k-block of a ring slot after the two
     // accumulators of round_up(box, 32) columns
     const int mx_acc = (box + 31) & ~31;
-    if (mx && stages > (512 - 2 * mx_acc) / 8) stages = (512 - 2 * mx_acc) / 8;
+    if (mx && stages > (512 - 2 * mx_acc) / (8 * kMxKbPerStage))
+        stages = (512 - 2 * mx_acc) / (8 * kMxKbPerStage);
     if (stages < 2) return MOE_ERR_UNSUPPORTED;
     const size_t smem = fixed + stages * stage_bytes + 1024;
     // two accumulators (+ MXFP4: A tiles of 32 columns after them)
     const int tmem_cols =
-        mxfp4 ? 512 : mx ? next_pow2(2 * mx_acc + 8 * stages) : next_pow2(2 * box < 32 ? 32 : 2 * box);
+        mxfp4 ? 512 : mx ? next_pow2(2 * mx_acc + 8 * kMxKbPerStage * stages) : next_pow2(2 * box < 32 ? 32 : 2 * box);
     if (tmem_cols > 512) return MOE_ERR_UNSUPPORTED;
 
     __nv_bfloat16* x_perm = reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm);
@@ -580,7 +581,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.h_pad = mx_padded_k(s.I);
     g.h_tail0 = mx_tail0(s.I);
     // K split when the units cannot fill two waves (small batches)
-    const int kb_per_slot = mxfp4 ? kMxfp4KbPerStage : 1;
+    const int kb_per_slot = mxfp4 ? kMxfp4KbPerStage : mx ? kMxKbPerStage : 1;
     const long long tiles_max = max_token_tiles(R, L.max_tiles);
     const int split_mode = g_ksplit_mode.load();
     // parts for `slots` ring slots: the model's choice (at most auto_max), or

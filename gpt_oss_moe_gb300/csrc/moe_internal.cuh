@@ -281,12 +281,14 @@ struct GemmParams {
 constexpr int kMxfp4AStages = 3;
 constexpr int kMxfp4MaxTokenTile = 128;
 constexpr int kMxfp4KbPerStage = 4;     // k-blocks of 64 per MXFP4 ring slot
+constexpr int kMxKbPerStage = 2;        // k-blocks of 128 per MXFP4 x MXFP8 ring slot
 inline size_t gemm_stage_bytes(int token_box, int wf) {
     size_t a = static_cast<size_t>(kWeightTileRows) * kBlockK * 2;
     size_t b = static_cast<size_t>(token_box) * kBlockK * 2;
     size_t codes = static_cast<size_t>(kWeightTileRows) * kBlockK / 2;
-    // FP8 and MXFP4 x MXFP8: 128-wide k-blocks of byte codes, the same bytes
-    return wf == 1 ? kMxfp4KbPerStage * (codes + b) : a + b;
+    // FP8: one 128-wide k-block of byte codes, the same bytes; MXFP4 x
+    // MXFP8: kMxKbPerStage of them (the codes padded to a byte each)
+    return wf == 1 ? kMxfp4KbPerStage * (codes + b) : wf == 3 ? kMxKbPerStage * (a + b) : a + b;
 }
 inline size_t gemm_fixed_bytes(int token_box, int wf, int kscale) {
     size_t scales = wf == 1 ? 2 * align_up(static_cast<size_t>(kWeightTileRows) * kscale, 16) : 0;
