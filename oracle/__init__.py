@@ -78,6 +78,7 @@ def lib():
             L.oracle_forward_tokens.argtypes = [P, vp, i, vp, vp, vp, vp, i]
             L.oracle_moe_forward.argtypes = [P, vp, vp, vp, i]
             L.oracle_moe_forward_dense.argtypes = [P, vp, vp, vp, i]
+            L.oracle_moe_forward_ep.argtypes = [P, i, i, vp, i, vp, i]
             L.oracle_dequant_mxfp4.argtypes = [vp, vp, i, i, vp]
             _lib = L
     return _lib
@@ -211,6 +212,21 @@ def forward(layer, tokens=None, threads: int = 0, want_logits: bool = False):
     if want_logits:
         return ids, w, out, logits
     return ids, w, out
+
+
+def forward_ep(layer, ex_lo: int, ex_n: int, tokens=None, threads: int = 0) -> torch.Tensor:
+    """Partial output [n, H] fp32 of the experts [ex_lo, ex_lo + ex_n)."""
+    s = _layer_struct(layer)
+    if tokens is None:
+        n, tok_ptr = layer.T, None
+    else:
+        tokens = torch.as_tensor(tokens, dtype=torch.int32).contiguous()
+        n, tok_ptr = tokens.numel(), tokens.data_ptr()
+    out = torch.empty((n, layer.H), dtype=torch.float32)
+    rc = lib().oracle_moe_forward_ep(ctypes.byref(s), ex_lo, ex_n, tok_ptr, n,
+                                     out.data_ptr(), threads)
+    assert rc == 0
+    return out
 
 
 def forward_dense(layer, threads: int = 0):

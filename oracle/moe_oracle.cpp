@@ -494,6 +494,54 @@ int oracle_moe_forward(const oracle_layer* L, int32_t* ids, float* w,
                                  threads);
 }
 
+// Expert-parallel form of §2 (the page's multi-device path: a device holds
+// the experts [ex_lo, ex_lo + ex_n) and skips tokens' other experts): the
+// routing over all E experts as above, then out[p] = sum, in slot order, of
+// w * y over the slots whose expert is local.  The devices' partial outputs
+// of a partition of [0, E) add up to the full output.  L's weight banks hold
+// all E experts (the expert index stays global here).  tokens may be null
+// (all T tokens).
+int oracle_moe_forward_ep(const oracle_layer* L, int ex_lo, int ex_n, const int32_t* tokens,
+                          int n, float* out, int threads) {
+    const int H = L->H, E = L->E, k = L->top_k;
+    if (ex_lo < 0 || ex_n < 0 || ex_lo + ex_n > E) return -1;
+    if (!tokens) n = L->T;
+    std::vector<int32_t> ids(static_cast<size_t>(n) * k);
+    std::vector<float> w(static_cast<size_t>(n) * k);
+    set_threads(threads);
+    std::vector<float> lg(static_cast<size_t>(n) * E);
+    const long long nl = static_cast<long long>(n) * E;
+#pragma omp parallel for schedule(static)
+    for (long long i = 0; i < nl; ++i) {
+        const int p = static_cast<int>(i / E), e = static_cast<int>(i % E);
+        lg[i] = router_logit(L, tokens ? tokens[p] : p, e);
+    }
+    for (int p = 0; p < n; ++p)
+        topk_softmax_row(lg.data() + static_cast<size_t>(p) * E, E, k,
+                         ids.data() + static_cast<size_t>(p) * k,
+                         w.data() + static_cast<size_t>(p) * k);
+    std::vector<float> y(static_cast<size_t>(n) * k * H, 0.0f);
+    const long long np = static_cast<long long>(n) * k;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long long q = 0; q < np; ++q) {
+        const int e = ids[q];
+        if (e < ex_lo || e >= ex_lo + ex_n) continue;      // not this device's expert
+        const int p = static_cast<int>(q / k);
+        expert_ffn(L, e, tokens ? tokens[p] : p, nullptr, y.data() + static_cast<size_t>(q) * H);
+    }
+    for (int p = 0; p < n; ++p) {
+        for (int c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {    // other devices' slots hold y = 0
+                const size_t q = static_cast<size_t>(p) * k + j;
+                acc += w[q] * y[q * H + c];
+            }
+            out[static_cast<size_t>(p) * H + c] = acc;
+        }
+    }
+    return 0;
+}
+
 // Dense form of §2: every token goes through every expert, then the weighted
 // sum keeps the k selected ones only (a skip, never a multiply by zero).
 int oracle_moe_forward_dense(const oracle_layer* L, int32_t* ids, float* w,

@@ -46,6 +46,8 @@ int oracle_forward_tokens(const oracle_layer* L, const int32_t* tokens, int n,
                           int threads);
 int oracle_moe_forward(const oracle_layer* L, int32_t* ids, float* w,
                        float* out, int threads);
+int oracle_moe_forward_ep(const oracle_layer* L, int ex_lo, int ex_n, const int32_t* tokens,
+                          int n, float* out, int threads);
 int oracle_moe_forward_dense(const oracle_layer* L, int32_t* ids, float* w,
                              float* out, int threads);
 int oracle_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int rows,

@@ -47,6 +47,8 @@ MUTATIONS = {
                                "xv[32 * b + i] = e4m3_value(xq[32 * b + i]);"),
     "mx_h_scale_wrong": ("hv[j] = e4m3_value(e4m3_round(h[j] * 8.0f)) * 0.125f;",
                          "hv[j] = e4m3_value(e4m3_round(h[j] * 8.0f)) * 0.25f;"),
+    "ep_range_off_by_one": ("if (e < ex_lo || e >= ex_lo + ex_n) continue;",
+                            "if (e < ex_lo || e > ex_lo + ex_n) continue;"),
     "scale_bias_off_by_one": ("static_cast<int>(s) - 127", "static_cast<int>(s) - 128"),
     "softmax_over_all_experts": ("    for (int j = 0; j < k; ++j) w[j] = ex[j] / denom;",
                                  "    for (int e = 0; e < E; ++e) if (!taken[e]) denom += std::exp(logit[e] - m);\n"

@@ -601,3 +601,37 @@ def test_mx_layer_with_exact_activations_equals_mxfp4_layer(oracle_lib, synth_li
     L4.x = L.x
     h_4, _ = oracle_lib.expert_ffn(L4, 1, 0)
     assert torch.equal(h_mx, h_4)
+
+
+# ------------------------------------------------ expert-parallel partial form
+
+def test_ep_full_range_is_the_forward(oracle_lib, synth_lib):
+    L = _tiny(synth_lib, E=8, T=10, k=3, seed=41)
+    _, _, out = oracle_lib.forward(L)
+    assert torch.equal(oracle_lib.forward_ep(L, 0, 8), out)
+
+
+def test_ep_single_expert_is_weight_times_expert_output(oracle_lib, synth_lib):
+    """A device holding expert e alone outputs w[t, j] * y(e, t) for the
+    tokens that chose e (ids are distinct, so one slot at most) and zero rows
+    for the others."""
+    L = _tiny(synth_lib, E=6, T=12, k=2, seed=43)
+    ids, w, _ = oracle_lib.forward(L)
+    for e in range(6):
+        part = oracle_lib.forward_ep(L, e, 1)
+        for t in range(12):
+            hit = (ids[t] == e).nonzero()
+            if len(hit) == 0:
+                assert part[t].eq(0).all()
+            else:
+                _, y = oracle_lib.expert_ffn(L, e, t)
+                assert torch.equal(part[t], w[t, hit[0, 0]] * y)
+
+
+def test_ep_partition_sums_to_the_forward(oracle_lib, synth_lib):
+    L = _tiny(synth_lib, E=8, T=10, k=3, seed=45)
+    _, _, out = oracle_lib.forward(L)
+    parts = [oracle_lib.forward_ep(L, lo, n) for lo, n in ((0, 3), (3, 1), (4, 4))]
+    total = parts[0] + parts[1] + parts[2]
+    assert (total - out).abs().max() <= 1e-6 * out.abs().max()
+    assert oracle_lib.forward_ep(L, 2, 0).eq(0).all()
