@@ -25,7 +25,7 @@ MOE_W_BF16, MOE_W_MXFP4, MOE_W_FP8, MOE_W_MXFP4_MXFP8 = 0, 1, 2, 3
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_BAD_TILE = 0x1, 0x2, 0x4
 
 # Every function the C header declares, in order (checked by the tests).
-EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_forward",
+EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_ep",
            "moe_forward_noalloc", "moe_get_device_status",
            "moe_clear_device_status",
            "moe_set_tuning", "moe_profile_enable", "moe_profile_read",
@@ -72,6 +72,9 @@ def lib():
             L.moe_forward.argtypes = [S, vp, vp, vp, moe_weight, moe_weight, vp, i,
                                       vp, vp, vp, sz, vp]
             L.moe_forward.restype = i
+            L.moe_forward_ep.argtypes = [S, i, i, vp, vp, vp, moe_weight, moe_weight, vp, i,
+                                         vp, vp, vp, sz, vp]
+            L.moe_forward_ep.restype = i
             L.moe_forward_noalloc.argtypes = [S, vp, vp, vp, moe_weight, moe_weight,
                                               vp, i, vp, vp, vp, vp]
             L.moe_forward_noalloc.restype = i
@@ -162,6 +165,46 @@ def moe_forward(shape, hidden, router_w, router_b, w_gu, b_gu, w_d, b_d,
                              ws.numel(), _stream(stream))
     _check(code, "moe_forward")
     return ws
+
+
+def moe_forward_ep(shape, expert_start, local_experts, hidden, router_w, router_b,
+                   w_gu, b_gu, w_d, b_d, out, s_gu=None, s_d=None, topk_ids_out=None,
+                   topk_w_out=None, workspace=None, stream=None):
+    """Expert-parallel forward: this device's partial output over the experts
+    [expert_start, expert_start + local_experts), whose banks alone are given
+    (w_gu, b_gu, w_d, b_d, s_gu, s_d hold local_experts experts); routing uses
+    the router of all shape.E experts.  Sum the devices' partial outputs
+    (ep_all_reduce) for the layer's output."""
+    ws = workspace if workspace is not None else alloc_workspace(shape, hidden.device)
+    gu = moe_weight(_p(w_gu), _p(s_gu), _p(b_gu))
+    dn = moe_weight(_p(w_d), _p(s_d), _p(b_d))
+    out_f32 = 1 if out.dtype == torch.float32 else 0
+    if not out_f32 and out.dtype != torch.bfloat16:
+        raise ValueError("out must be float32 or bfloat16")
+    code = lib().moe_forward_ep(ctypes.byref(shape), int(expert_start), int(local_experts),
+                                _p(hidden), _p(router_w), _p(router_b), gu, dn, _p(out),
+                                out_f32, _p(topk_ids_out), _p(topk_w_out), _p(ws),
+                                ws.numel(), _stream(stream))
+    _check(code, "moe_forward_ep")
+    return ws
+
+
+def ep_expert_range(rank: int, world: int, num_experts: int):
+    """Contiguous expert range (start, count) of one rank: E / world each,
+    the first E % world ranks one more."""
+    if world < 1 or not 0 <= rank < world or num_experts < world:
+        raise ValueError("need 0 <= rank < world <= num_experts")
+    base, extra = divmod(num_experts, world)
+    start = rank * base + min(rank, extra)
+    return start, base + (1 if rank < extra else 0)
+
+
+def ep_all_reduce(partial: torch.Tensor, group=None) -> torch.Tensor:
+    """Sums the ranks' partial outputs in place (torch.distributed: NCCL
+    for device tensors, gloo for host tensors) and returns them."""
+    import torch.distributed as dist
+    dist.all_reduce(partial, op=dist.ReduceOp.SUM, group=group)
+    return partial
 
 
 def moe_forward_noalloc(shape, hidden, router_w, router_b, w_gu, b_gu, w_d, b_d,

@@ -265,7 +265,7 @@ struct Routing {
 moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, const void* hidden,
                           const void* router_w, const void* router_b, const Routing& r,
                           float* zero_out, __nv_bfloat16* x_perm, int token_tile,
-                          const DevInfo& dev, cudaStream_t stream) {
+                          const DevInfo& dev, cudaStream_t stream, int ex_lo, int ex_n) {
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     const int nb = (s.T + kRouterTokens - 1) / kRouterTokens;
 
@@ -317,6 +317,8 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     rp.tiles = reinterpret_cast<int4*>(ws + L.tiles);
     rp.max_tiles = L.max_tiles;
     rp.token_tile = token_tile;
+    rp.ex_lo = ex_lo;
+    rp.ex_n = ex_n;
     rp.status = status;
     MOE_CUDA(launch_router(rp, &tm_x, &tm_wr, router_smem_bytes(stages), stream));
     prof_mark("router_topk", stream);
@@ -347,6 +349,8 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     pp.fp8 = s.wfmt == MOE_W_FP8 ? 1 : 0;
     pp.mx8 = s.wfmt == MOE_W_MXFP4_MXFP8 ? 1 : 0;
     pp.x_scale = reinterpret_cast<float*>(ws + L.x_scale);
+    pp.ex_lo = ex_lo;
+    pp.ex_hi = ex_lo + ex_n;
     pp.status = status;
     MOE_CUDA(launch_permute(pp, stream, g_pdl.load() != 0));
     prof_mark(x_perm ? "permute_gather" : "permute", stream);
@@ -394,16 +398,23 @@ moe_status moe_route(const moe_shape* shape, const void* hidden, const void* rou
     std::lock_guard<std::mutex> lock(g_prof_mu);
     prof_reset(stream);
     const moe_status st = launch_routing(s, L, ws, hidden, router_w, router_b, r, nullptr,
-                                         nullptr, auto_token_tile(s), dev, stream);
+                                         nullptr, auto_token_tile(s), dev, stream, 0, s.E);
     prof_finish();
     return st;
 }
 
-moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* router_w,
-                       const void* router_b, moe_weight gate_up, moe_weight down, void* out,
-                       int out_is_fp32, int32_t* topk_ids_out, float* topk_w_out,
-                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+namespace moe {
+namespace {
+
+// moe_forward for the local experts [ex_lo, ex_lo + ex_n) of the layer's E
+// (all of them for moe_forward); the weight banks hold those ex_n experts.
+moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void* hidden,
+                        const void* router_w, const void* router_b, moe_weight gate_up,
+                        moe_weight down, void* out, int out_is_fp32, int32_t* topk_ids_out,
+                        float* topk_w_out, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
     MOE_TRY(check_shape(shape));
+    if (ex_lo < 0 || ex_n < 1 || ex_lo + ex_n > shape->E) return MOE_ERR_ARG;
     const moe_shape s = *shape;
     if (s.T == 0) return MOE_OK;
     MOE_TRY(check_ptr(hidden));
@@ -418,9 +429,15 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     const bool mxfp4 = s.wfmt == MOE_W_MXFP4;
     const bool fp8 = s.wfmt == MOE_W_FP8;
     const bool mx = s.wfmt == MOE_W_MXFP4_MXFP8;
-    if (mxfp4 || fp8 || mx) {
+    if (mxfp4 || mx) {
         MOE_TRY(check_ptr(gate_up.scale));
         MOE_TRY(check_ptr(down.scale));
+    } else if (fp8) {
+        // per-expert fp32 scales, read one float at a time: 4-byte alignment
+        // (a slice of an expert-parallel rank is 4-byte aligned)
+        if (!gate_up.scale || !down.scale) return MOE_ERR_ARG;
+        if ((reinterpret_cast<uintptr_t>(gate_up.scale) | reinterpret_cast<uintptr_t>(down.scale)) & 3)
+            return MOE_ERR_ALIGN;
     }
     // the 4-bit tensor maps of the block-scaled path want 32-byte alignment
     if (mx && ((reinterpret_cast<uintptr_t>(gate_up.w) | reinterpret_cast<uintptr_t>(down.w)) & 31))
@@ -493,11 +510,11 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     // Tensor maps (host-side descriptors; cheap to build per call).
     CUtensorMap tm_wgu, tm_x, tm_wd, tm_h;
     if (mx) {
-        MOE_TRY(mx_weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H));
-        MOE_TRY(mx_weight_tmap(&tm_wd, down.w, s.E, s.H, s.I));
+        MOE_TRY(mx_weight_tmap(&tm_wgu, gate_up.w, ex_n, 2 * s.I, s.H));
+        MOE_TRY(mx_weight_tmap(&tm_wd, down.w, ex_n, s.H, s.I));
     } else {
-        MOE_TRY(weight_tmap(&tm_wgu, gate_up.w, s.E, 2 * s.I, s.H, mxfp4, fp8));
-        MOE_TRY(weight_tmap(&tm_wd, down.w, s.E, s.H, s.I, mxfp4, fp8));
+        MOE_TRY(weight_tmap(&tm_wgu, gate_up.w, ex_n, 2 * s.I, s.H, mxfp4, fp8));
+        MOE_TRY(weight_tmap(&tm_wd, down.w, ex_n, s.H, s.I, mxfp4, fp8));
     }
     // Token operands: bf16 layers read [R, K] row-major, one 64-wide K chunk
     // per box; MXFP4 layers read the chunk-major [K/64, R, 64] layout the
@@ -544,7 +561,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     r.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
     r.sorted_assign = reinterpret_cast<int32_t*>(ws + L.sorted_assign);
     MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r, out32, x_perm, box, dev,
-                           stream));
+                           stream, ex_lo, ex_n));
 
     GemmParams g{};
     g.tiles = reinterpret_cast<const int4*>(ws + L.tiles);
@@ -554,7 +571,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     g.astages = astages;
     g.n_iss = n_iss;
     g.tmem_cols = tmem_cols;
-    g.num_experts = s.E;
+    g.num_experts = ex_n;            // tiles number the local experts from 0
     g.rows_total = R;
     g.status = status;
 
@@ -653,6 +670,30 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
     }
     prof_finish();
     return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* router_w,
+                       const void* router_b, moe_weight gate_up, moe_weight down, void* out,
+                       int out_is_fp32, int32_t* topk_ids_out, float* topk_w_out,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!shape) return MOE_ERR_ARG;
+    return forward_impl(shape, 0, shape->E, hidden, router_w, router_b, gate_up, down, out,
+                        out_is_fp32, topk_ids_out, topk_w_out, workspace, workspace_bytes,
+                        stream);
+}
+
+moe_status moe_forward_ep(const moe_shape* shape, int expert_start, int local_experts,
+                          const void* hidden, const void* router_w, const void* router_b,
+                          moe_weight gate_up, moe_weight down, void* out, int out_is_fp32,
+                          int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+    if (!shape) return MOE_ERR_ARG;
+    return forward_impl(shape, expert_start, local_experts, hidden, router_w, router_b,
+                        gate_up, down, out, out_is_fp32, topk_ids_out, topk_w_out, workspace,
+                        workspace_bytes, stream);
 }
 
 moe_status moe_get_device_status(const void* workspace, int32_t* host_status) {

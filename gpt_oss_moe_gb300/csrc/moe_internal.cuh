@@ -191,6 +191,9 @@ struct RouterParams {
     int4* tiles;                 // GEMM token tiles (expert, first row, rows, 0)
     int max_tiles;
     int token_tile;              // rows of tokens per GEMM tile
+    // expert-parallel form: GEMM tiles only for experts [ex_lo, ex_lo + ex_n),
+    // numbered from 0 (the local weight banks); 0, E for the whole layer
+    int ex_lo, ex_n;
     int32_t* status;             // status region (status word, tile count, counter)
 };
 
@@ -212,6 +215,7 @@ struct PermuteParams {
                                  // in the order 0,4,1,5,2,6,3,7
     int fp8;                     // FP8 W8A8: x_perm holds E4M3 codes [T*k, H]
     float* x_scale;              // FP8: [T*k] scale of each routed row's codes
+    int ex_lo, ex_hi;            // gather only the rows of experts [ex_lo, ex_hi)
     int mx8;                     // MXFP8 activations: x_perm holds E4M3 codes
                                  // [T*k, mx_padded_k(H)] and x_scale UE8M0
                                  // bytes [T*k, mx_padded_k(H) / 32]

@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
                     if (good) p.sorted_assign[row] = a;
                     p.assign_row[a] = row;
                 }
-                rows_s[a - a0] = row;
+                // the gather copies only the rows of this device's experts
+                rows_s[a - a0] = good && e >= p.ex_lo && e < p.ex_hi ? row : -1;
             }
         }
     }

@@ -224,20 +224,23 @@ __device__ void finish_routing(const RouterParams& p, int* total_s, int* offs_s,
     if (warp == 0) warp_exclusive_scan256(total_s, offs_s, E);
     __syncthreads();
     for (int e = tid; e <= E; e += kThreads) p.offsets[e] = offs_s[e];
+    // token tiles of the local experts only (expert-parallel form)
     for (int e = tid; e < E; e += kThreads)
-        tcnt_s[e] = (total_s[e] + p.token_tile - 1) / p.token_tile;
+        tcnt_s[e] = e >= p.ex_lo && e < p.ex_lo + p.ex_n
+                        ? (total_s[e] + p.token_tile - 1) / p.token_tile : 0;
     __syncthreads();
     if (warp == 0) warp_exclusive_scan256(tcnt_s, toff_s, E);
     __syncthreads();
     for (int e = tid; e < E; e += kThreads) {
         const int m = total_s[e];
-        if (m == 0) continue;
         const int nt = tcnt_s[e];
+        if (m == 0 || nt == 0) continue;
         const int per = ((m + nt - 1) / nt + 15) / 16 * 16;
         for (int i = 0; i < nt; ++i) {
             const int slot = toff_s[e] + i;
             if (slot < p.max_tiles)
-                p.tiles[slot] = make_int4(e, offs_s[e] + i * per, min(per, m - i * per), 0);
+                p.tiles[slot] =
+                    make_int4(e - p.ex_lo, offs_s[e] + i * per, min(per, m - i * per), 0);
             else
                 atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
         }

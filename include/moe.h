@@ -19,7 +19,7 @@
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers, row-major, densely packed,
- *     16-byte aligned.  The caller owns every buffer; the library allocates
+ *     16-byte aligned (FP8 per-expert scale arrays: 4-byte aligned).  The caller owns every buffer; the library allocates
  *     no device memory and keeps no state beyond a per-device cache of device
  *     attributes and the optional profiling events below.
  *   - bf16 is IEEE-754 binary16-brain (uint16 storage).
@@ -155,6 +155,29 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden,
                        int32_t* topk_ids_out, float* topk_w_out,
                        void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
+
+/* Expert-parallel form of moe_forward (§2 "MoE 前向", the multi-device
+ * path: a device holds a contiguous range of experts and skips tokens'
+ * other experts, never multiplying them by zero).
+ *   expert_start, local_experts: this device's experts [expert_start,
+ *        expert_start + local_experts), 0 <= expert_start, local_experts >= 1,
+ *        expert_start + local_experts <= shape->E;
+ *   router_w, router_b: for all shape->E experts (routing is global);
+ *   gate_up, down: banks holding only the local experts (local_experts
+ *        experts in the layouts of moe_weight, local expert 0 first);
+ *   out: this device's partial output, out[t] = sum over the slots j whose
+ *        expert is local of w[t,j] * y (zero rows for tokens with none).
+ * The partial outputs of devices whose ranges partition [0, E) add up to
+ * moe_forward's output (in another order: last-bit differences); the caller
+ * sums them (an all-reduce).  Other arguments and errors as for moe_forward;
+ * MOE_ERR_ARG for a bad expert range. */
+moe_status moe_forward_ep(const moe_shape* shape, int expert_start, int local_experts,
+                          const void* hidden, const void* router_w, const void* router_b,
+                          moe_weight gate_up, moe_weight down,
+                          void* out, int out_is_fp32,
+                          int32_t* topk_ids_out, float* topk_w_out,
+                          void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
 
 /* Size of the library-owned scratch array used by moe_forward_noalloc
  * (8 MiB per device that loads the library, held until the process exits). */

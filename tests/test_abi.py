@@ -95,6 +95,39 @@ def test_forward_rejects_bad_arguments_on_the_host(moe):
     assert _fwd(moe, _shape(moe, T=0), {"x": 0, "out": 0}) == 0
 
 
+def test_forward_ep_rejects_bad_expert_ranges_on_the_host(moe):
+    L = moe.lib()
+    s = _shape(moe, E=32)
+
+    def ep(start, n, wfmt=None):
+        sh = s if wfmt is None else _shape(moe, E=32, wfmt=wfmt)
+        gu = moe.moe_weight(256, 1024 if wfmt else None, 512)
+        dn = moe.moe_weight(768, 1024 if wfmt else None, 1024)
+        return L.moe_forward_ep(ctypes.byref(sh), start, n, 16, 32, 48, gu, dn, 64, 1,
+                                None, None, 4096, 1 << 30, None)
+    for start, n in [(-1, 4), (0, 0), (30, 3), (32, 1), (0, 33)]:
+        assert ep(start, n) == -1, (start, n)                 # MOE_ERR_ARG
+    # MXFP4 x MXFP8 codes must be 32-byte aligned: 16 + 256 is not
+    gu = moe.moe_weight(272, 1024, 512)
+    dn = moe.moe_weight(768, 1024, 1024)
+    sh = _shape(moe, E=32, wfmt=moe.MOE_W_MXFP4_MXFP8)
+    assert L.moe_forward_ep(ctypes.byref(sh), 0, 32, 16, 32, 48, gu, dn, 64, 1,
+                            None, None, 4096, 1 << 30, None) == -3
+    assert L.moe_forward_ep(None, 0, 1, 16, 32, 48, gu, dn, 64, 1, None, None, 4096,
+                            1 << 30, None) == -1
+
+
+def test_ep_expert_ranges_partition_the_experts(moe):
+    for E in (1, 7, 32, 128):
+        for world in range(1, min(E, 9) + 1):
+            got = [moe.ep_expert_range(r, world, E) for r in range(world)]
+            assert got[0][0] == 0 and sum(n for _, n in got) == E
+            assert all(a + n == b for (a, n), (b, _) in zip(got, got[1:]))
+            assert max(n for _, n in got) - min(n for _, n in got) <= 1
+    with pytest.raises(ValueError):
+        moe.ep_expert_range(0, 5, 4)
+
+
 def test_route_rejects_bad_arguments_on_the_host(moe):
     L = moe.lib()
     s = _shape(moe)

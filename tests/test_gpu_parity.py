@@ -553,6 +553,56 @@ def test_forward_20b_mxfp4_mxfp8(moe, oracle_lib, layer_20b_mxfp8, T):
     _check(moe, oracle_lib, L, dev=dev, T=T, sample=sample)
 
 
+# ------------------------------------------------ expert-parallel partial form
+
+def _ep_partials(moe, L, dev, world, tokens=None):
+    """Partial outputs of `world` devices (run one after another on this
+    GPU) that partition the experts, each given its slice of the banks."""
+    shape = moe.layer_shape(L)
+    parts = []
+    for r in range(world):
+        lo, n = moe.ep_expert_range(r, world, L.E)
+        sl = lambda t: None if t is None else t[lo:lo + n]
+        out = torch.empty((L.T, L.H), dtype=torch.float32, device="cuda")
+        ws = moe.moe_forward_ep(shape, lo, n, dev["x"], dev["wr"], dev["br"], sl(dev["w_gu"]),
+                                sl(dev["b_gu"]), sl(dev["w_d"]), sl(dev["b_d"]), out,
+                                s_gu=sl(dev["s_gu"]), s_d=sl(dev["s_d"]))
+        assert moe.moe_get_device_status(ws) == 0
+        parts.append((lo, n, out.cpu()))
+    return parts
+
+
+@pytest.mark.parametrize("wfmt", ["bf16", "fp8", "mxfp4", "mxfp4_mxfp8"])
+def test_forward_ep_partials_match_and_sum_to_the_layer(moe, oracle_lib, synth_lib, wfmt):
+    from parity_util import TOL_MXFP4
+    L = synth_lib.make_layer(E=8, T=40, H=256, I=192, top_k=3, seed=900, wfmt=wfmt,
+                             router_w_std=0.05)
+    tol = TOL_MXFP4 if wfmt == "mxfp4" else TOL_BF16
+    _, _, full = oracle_lib.forward(L)
+    ref = full.abs().max().item()
+    total = torch.zeros_like(full)
+    for lo, n, part in _ep_partials(moe, L, to_device(L), 3):
+        o_part = oracle_lib.forward_ep(L, lo, n)
+        assert (part - o_part).abs().max().item() <= tol * ref, (lo, n)
+        total += part
+    assert (total - full).abs().max().item() <= tol * ref
+
+
+def test_forward_ep_20b_four_ranks(moe, oracle_lib, layer_20b_decode):
+    """gpt-oss-20b widths, T = 64, four ranks of 8 experts."""
+    L64, dev64 = layer_20b_decode
+    assert L64.T == 64
+    parts = _ep_partials(moe, L64, dev64, 4)
+    sample = list(range(0, 64, 4))
+    _, _, full = oracle_lib.forward(L64, tokens=sample)
+    ref = full.abs().max().item()
+    total = sum(p for _, _, p in parts)[sample]
+    assert (total - full).abs().max().item() <= TOL_BF16 * ref
+    lo, n, part = parts[1]
+    o_part = oracle_lib.forward_ep(L64, lo, n, tokens=sample)
+    assert (part[sample] - o_part).abs().max().item() <= TOL_BF16 * ref
+
+
 def test_one_workspace_serves_successive_shapes(moe, synth_lib):
     """A workspace sized for the largest call is reused for smaller ones
     (other token counts shift every region but the status word and the
