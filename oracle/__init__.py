@@ -79,6 +79,7 @@ def lib():
             L.oracle_moe_forward.argtypes = [P, vp, vp, vp, i]
             L.oracle_moe_forward_dense.argtypes = [P, vp, vp, vp, i]
             L.oracle_moe_forward_ep.argtypes = [P, i, i, vp, i, vp, i]
+            L.oracle_attention_sinks.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, i]
             L.oracle_dequant_mxfp4.argtypes = [vp, vp, i, i, vp]
             _lib = L
     return _lib
@@ -225,6 +226,24 @@ def forward_ep(layer, ex_lo: int, ex_n: int, tokens=None, threads: int = 0) -> t
     out = torch.empty((n, layer.H), dtype=torch.float32)
     rc = lib().oracle_moe_forward_ep(ctypes.byref(s), ex_lo, ex_n, tok_ptr, n,
                                      out.data_ptr(), threads)
+    assert rc == 0
+    return out
+
+
+def attention_sinks(q, k, v, sinks, window: int = 0, q_start=None, threads: int = 0):
+    """q [Tq, Hq, D], k / v [Tkv, Hkv, D] bf16, sinks [Hq] fp32 -> out
+    [Tq, Hq, D] fp32 (fp64 inside).  q_start defaults to Tkv - Tq."""
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    sinks = sinks.to(torch.float32).contiguous()
+    assert q.dtype == k.dtype == v.dtype == torch.bfloat16
+    Tq, Hq, D = q.shape
+    Tkv, Hkv, _ = k.shape
+    if q_start is None:
+        q_start = Tkv - Tq
+    out = torch.empty((Tq, Hq, D), dtype=torch.float32)
+    rc = lib().oracle_attention_sinks(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                      sinks.data_ptr(), Tq, Tkv, Hq, Hkv, D, window,
+                                      q_start, out.data_ptr(), threads)
     assert rc == 0
     return out
 

@@ -69,6 +69,7 @@
 // the whole layer on E=4/top-2/H=I=64, routed == dense bit-exactly, and the
 // exact E2M1/E8M0 table.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -567,6 +568,57 @@ int oracle_moe_forward_dense(const oracle_layer* L, int32_t* ids, float* w,
                        y[(static_cast<size_t>(t) * E + e) * H + c];
             }
             out[static_cast<size_t>(t) * H + c] = acc;
+        }
+    }
+    return 0;
+}
+
+// Attention with sinks (§1 model-architecture table, "attention" row:
+// alternating sliding-window (128) / full layers, one learnable sink scalar
+// per head; §3 on the empty-tile case).  Readings: GQA head h reads KV head
+// h / (Hq / Hkv); scores are q.k / sqrt(D); query i sits at position
+// q_start + i and sees key j when j <= q_start + i and, with a window W > 0,
+// j > q_start + i - W (W keys including its own); the sink is one more logit
+// in the softmax's denominator that carries no value:
+//   out = sum_j exp(s_j - m) v_j / (exp(sink - m) + sum_j exp(s_j - m)),
+// m = max(sink, s_j).  fp64 throughout (the page fixes no precision).
+// q [Tq, Hq, D], k and v [Tkv, Hkv, D] bf16; sinks [Hq] fp32 (-inf: none);
+// out [Tq, Hq, D] fp32.
+int oracle_attention_sinks(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const float* sinks, int Tq, int Tkv, int Hq, int Hkv, int D,
+                           int window, int q_start, float* out, int threads) {
+    if (Hkv < 1 || Hq % Hkv || Tq < 0 || q_start < 0 || q_start + Tq > Tkv || window < 0)
+        return -1;
+    set_threads(threads);
+    const int rep = Hq / Hkv;
+    const double scale = 1.0 / std::sqrt(static_cast<double>(D));
+    const long long n = static_cast<long long>(Tq) * Hq;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long long r = 0; r < n; ++r) {
+        const int i = static_cast<int>(r / Hq), h = static_cast<int>(r % Hq);
+        const int hk = h / rep;
+        const int pos = q_start + i;
+        const int j0 = window > 0 ? std::max(0, pos - window + 1) : 0;
+        const uint16_t* qr = q + (static_cast<size_t>(i) * Hq + h) * D;
+        std::vector<double> sc(static_cast<size_t>(pos - j0 + 1));
+        double m = sinks[h];
+        for (int j = j0; j <= pos; ++j) {
+            const uint16_t* kr = k + (static_cast<size_t>(j) * Hkv + hk) * D;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += static_cast<double>(bf16_value(qr[d])) * bf16_value(kr[d]);
+            sc[j - j0] = acc * scale;
+            m = std::max(m, sc[j - j0]);
+        }
+        double denom = std::isinf(sinks[h]) && sinks[h] < 0 ? 0.0 : std::exp(sinks[h] - m);
+        for (int j = j0; j <= pos; ++j) denom += std::exp(sc[j - j0] - m);
+        float* o = out + (static_cast<size_t>(i) * Hq + h) * D;
+        for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int j = j0; j <= pos; ++j)
+                acc += std::exp(sc[j - j0] - m) *
+                       bf16_value(v[(static_cast<size_t>(j) * Hkv + hk) * D + d]);
+            o[d] = static_cast<float>(acc / denom);
         }
     }
     return 0;

@@ -50,6 +50,9 @@ int oracle_moe_forward_ep(const oracle_layer* L, int ex_lo, int ex_n, const int3
                           int n, float* out, int threads);
 int oracle_moe_forward_dense(const oracle_layer* L, int32_t* ids, float* w,
                              float* out, int threads);
+int oracle_attention_sinks(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const float* sinks, int Tq, int Tkv, int Hq, int Hkv, int D,
+                           int window, int q_start, float* out, int threads);
 int oracle_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int rows,
                          int K, float* out);
 

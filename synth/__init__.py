@@ -46,6 +46,7 @@ S_GU_CODES, S_GU_SCALES, S_D_CODES, S_D_SCALES = 8, 9, 10, 11
 # FP8 code fields (sign, exponent, mantissa) and per-expert scales
 S_F8_GU_SIGN, S_F8_GU_EXP, S_F8_GU_MAN, S_F8_GU_SCALE = 12, 13, 14, 15
 S_F8_D_SIGN, S_F8_D_EXP, S_F8_D_MAN, S_F8_D_SCALE = 16, 17, 18, 19
+S_ATT_Q, S_ATT_K, S_ATT_V, S_ATT_SINK = 20, 21, 22, 23
 
 
 def build(force: bool = False) -> str:
@@ -233,3 +234,14 @@ def make_workload(name: str, T: int, pin: bool = False, **over) -> Layer:
     w.pop("Ts")
     w.update(over)
     return make_layer(T=T, pin=pin, **w)
+
+
+def make_attention(Tq: int, Tkv: int, Hq: int = 64, Hkv: int = 8, D: int = 64, seed: int = 0,
+                   qk_std: float = 1.0, sink_std: float = 1.0, pin: bool = False) -> dict:
+    """Attention inputs of the gpt-oss block's shape (64 query heads, 8 KV
+    heads, head_dim 64): q [Tq, Hq, D], k / v [Tkv, Hkv, D] bf16 ~ N(0, std)
+    (q and k post-rotary stand-ins), sinks [Hq] fp32 ~ N(0, sink_std)."""
+    return dict(q=normal_bf16((Tq, Hq, D), seed, S_ATT_Q, 0.0, qk_std, pin=pin),
+                k=normal_bf16((Tkv, Hkv, D), seed, S_ATT_K, 0.0, qk_std, pin=pin),
+                v=normal_bf16((Tkv, Hkv, D), seed, S_ATT_V, 0.0, 1.0, pin=pin),
+                sinks=normal_f32((Hq,), seed, S_ATT_SINK, 0.0, sink_std))

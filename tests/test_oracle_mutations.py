@@ -49,6 +49,11 @@ MUTATIONS = {
                          "hv[j] = e4m3_value(e4m3_round(h[j] * 8.0f)) * 0.25f;"),
     "ep_range_off_by_one": ("if (e < ex_lo || e >= ex_lo + ex_n) continue;",
                             "if (e < ex_lo || e > ex_lo + ex_n) continue;"),
+    "att_sink_not_in_denominator": (
+        "double denom = std::isinf(sinks[h]) && sinks[h] < 0 ? 0.0 : std::exp(sinks[h] - m);",
+        "double denom = 0.0;"),
+    "att_window_off_by_one": ("std::max(0, pos - window + 1)", "std::max(0, pos - window)"),
+    "att_gqa_mapping_wrong": ("const int hk = h / rep;", "const int hk = h % Hkv;"),
     "scale_bias_off_by_one": ("static_cast<int>(s) - 127", "static_cast<int>(s) - 128"),
     "softmax_over_all_experts": ("    for (int j = 0; j < k; ++j) w[j] = ex[j] / denom;",
                                  "    for (int e = 0; e < E; ++e) if (!taken[e]) denom += std::exp(logit[e] - m);\n"

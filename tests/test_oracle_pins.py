@@ -635,3 +635,69 @@ def test_ep_partition_sums_to_the_forward(oracle_lib, synth_lib):
     total = parts[0] + parts[1] + parts[2]
     assert (total - out).abs().max() <= 1e-6 * out.abs().max()
     assert oracle_lib.forward_ep(L, 2, 0).eq(0).all()
+
+
+# ------------------------------------------------ attention with sinks (f4)
+
+def _att(synth_lib, Tq, Tkv, Hq=4, Hkv=2, D=16, seed=0, **kw):
+    return synth_lib.make_attention(Tq, Tkv, Hq=Hq, Hkv=Hkv, D=D, seed=seed, **kw)
+
+
+def test_attention_without_sink_is_library_causal_attention(oracle_lib, synth_lib):
+    a = _att(synth_lib, 9, 9, seed=1)
+    out = oracle_lib.attention_sinks(a["q"], a["k"], a["v"],
+                                     torch.full((4,), float("-inf")))
+    q = a["q"].double().permute(1, 0, 2)
+    k = a["k"].double().repeat_interleave(2, dim=1).permute(1, 0, 2)
+    v = a["v"].double().repeat_interleave(2, dim=1).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    assert torch.allclose(out.double(), ref.permute(1, 0, 2), rtol=0, atol=1e-6)
+
+
+def test_attention_window_of_one_closed_form(oracle_lib, synth_lib):
+    """W = 1: each query sees its own key only, against the sink:
+    out_i = v_i / (1 + exp(sink - s_ii))."""
+    a = _att(synth_lib, 6, 6, seed=2)
+    out = oracle_lib.attention_sinks(a["q"], a["k"], a["v"], a["sinks"], window=1)
+    for i in range(6):
+        for h in range(4):
+            s = float((a["q"][i, h].double() * a["k"][i, h // 2].double()).sum()) / 4.0
+            w = 1.0 / (1.0 + math.exp(float(a["sinks"][h]) - s))
+            assert torch.allclose(out[i, h].double(), w * a["v"][i, h // 2].double(),
+                                  rtol=1e-6, atol=1e-7)
+
+
+def test_attention_large_sink_takes_all_mass(oracle_lib, synth_lib):
+    a = _att(synth_lib, 5, 5, seed=3, qk_std=0.1)
+    out = oracle_lib.attention_sinks(a["q"], a["k"], a["v"], torch.full((4,), 60.0))
+    assert out.abs().max() < 1e-20
+
+
+def test_attention_window_covering_everything_is_full(oracle_lib, synth_lib):
+    a = _att(synth_lib, 12, 12, seed=4)
+    full = oracle_lib.attention_sinks(a["q"], a["k"], a["v"], a["sinks"])
+    assert torch.equal(oracle_lib.attention_sinks(a["q"], a["k"], a["v"], a["sinks"],
+                                                  window=12), full)
+    w3 = oracle_lib.attention_sinks(a["q"], a["k"], a["v"], a["sinks"], window=3)
+    assert torch.equal(w3[:3], full[:3]) and not torch.equal(w3[3:], full[3:])
+
+
+def test_attention_decode_rows_equal_prefill_rows(oracle_lib, synth_lib):
+    """A query at position p over the cache [0, p] (decode) equals row p of
+    the prefill over the same keys."""
+    a = _att(synth_lib, 10, 10, seed=5)
+    full = oracle_lib.attention_sinks(a["q"], a["k"], a["v"], a["sinks"], window=4)
+    for p in (0, 3, 9):
+        one = oracle_lib.attention_sinks(a["q"][p:p + 1], a["k"][:p + 1], a["v"][:p + 1],
+                                         a["sinks"], window=4)
+        assert torch.equal(one[0], full[p])
+
+
+def test_attention_gqa_heads_share_their_kv_head(oracle_lib, synth_lib):
+    a = _att(synth_lib, 7, 7, Hq=6, Hkv=3, seed=6)
+    q = a["q"].clone()
+    q[:, 1] = q[:, 0]                       # heads 0 and 1 read KV head 0
+    q[:, 2] = q[:, 0]                       # head 2 reads KV head 1
+    sinks = torch.zeros(6)
+    out = oracle_lib.attention_sinks(q, a["k"], a["v"], sinks)
+    assert torch.equal(out[:, 0], out[:, 1]) and not torch.equal(out[:, 0], out[:, 2])
