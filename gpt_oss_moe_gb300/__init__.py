@@ -29,7 +29,7 @@ EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_ep",
            "moe_forward_noalloc", "moe_get_device_status",
            "moe_clear_device_status",
            "moe_set_tuning", "moe_profile_enable", "moe_profile_read",
-           "moe_status_str")
+           "moe_status_str", "moe_attention_sinks")
 
 
 class MoEError(RuntimeError):
@@ -42,6 +42,11 @@ class moe_shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
                 ("E", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("wfmt", ctypes.c_int)]
+
+
+class moe_attn_shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("Tq", "Tkv", "Hq", "Hkv", "D", "window",
+                                            "q_start")]
 
 
 class moe_weight(ctypes.Structure):
@@ -75,6 +80,9 @@ def lib():
             L.moe_forward_ep.argtypes = [S, i, i, vp, vp, vp, moe_weight, moe_weight, vp, i,
                                          vp, vp, vp, sz, vp]
             L.moe_forward_ep.restype = i
+            L.moe_attention_sinks.argtypes = [ctypes.POINTER(moe_attn_shape), vp, vp, vp, vp,
+                                              vp, vp]
+            L.moe_attention_sinks.restype = i
             L.moe_forward_noalloc.argtypes = [S, vp, vp, vp, moe_weight, moe_weight,
                                               vp, i, vp, vp, vp, vp]
             L.moe_forward_noalloc.restype = i
@@ -187,6 +195,21 @@ def moe_forward_ep(shape, expert_start, local_experts, hidden, router_w, router_
                                 ws.numel(), _stream(stream))
     _check(code, "moe_forward_ep")
     return ws
+
+
+def attention_sinks(q, k, v, sinks, out=None, window: int = 0, q_start=None, stream=None):
+    """Attention with sinks on the GPU: q [Tq, Hq, 64], k / v [Tkv, Hkv, 64]
+    bf16, sinks [Hq] fp32 -> out [Tq, Hq, 64] fp32 (see moe_attention_sinks)."""
+    Tq, Hq, D = q.shape
+    Tkv, Hkv, _ = k.shape
+    if out is None:
+        out = torch.empty((Tq, Hq, D), dtype=torch.float32, device=q.device)
+    shape = moe_attn_shape(int(Tq), int(Tkv), int(Hq), int(Hkv), int(D), int(window),
+                           int(Tkv - Tq if q_start is None else q_start))
+    code = lib().moe_attention_sinks(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(sinks),
+                                     _p(out), _stream(stream))
+    _check(code, "moe_attention_sinks")
+    return out
 
 
 def ep_expert_range(rank: int, world: int, num_experts: int):

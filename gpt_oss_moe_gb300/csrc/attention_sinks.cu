@@ -1,0 +1,249 @@
+// Attention with sinks and an optional sliding window, the other half of a
+// gpt-oss block (xserv docs/19-gpt-oss-moe.md, "Phase 19: gpt-oss-20b": §1
+// model-architecture table, "attention" row -- sliding (128) / full layers
+// alternate, one learnable sink logit per head, 64 query / 8 KV heads of
+// dim 64; §3 on the fully masked tile of a sliding window).
+//
+// One CTA per (64 query rows, query head), four warps of 16 rows.  Per KV
+// tile of 64 keys: S = Q K^T on the tensor cores (mma.sync m16n8k16, bf16 in,
+// fp32 out), scale and mask, online softmax in the exp2 domain, O += P V
+// (P rounded to bf16).  The sink enters as the running max's starting value
+// with one unit in the denominator (exp2(sink - m) after rescaling), so it
+// weighs in the softmax and carries no value.  A row whose tile is fully
+// masked (its tile max is -inf: all keys in the future or slid out of the
+// window) leaves the row's state untouched -- the guard whose absence, with
+// a running max of -inf, turns exp(-inf - -inf) into NaN.
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+#include "../../include/moe.h"
+
+namespace moe {
+namespace {
+
+constexpr int kD = 64;          // head dim
+constexpr int kBq = 64;         // query rows per CTA
+constexpr int kBk = 64;         // keys per tile
+constexpr int kLd = kD + 8;     // shared-memory row stride (bf16): 144 B
+constexpr int kThreadsAttn = 128;
+
+struct AttnParams {
+    const __nv_bfloat16* q;     // [Tq, Hq, D]
+    const __nv_bfloat16* k;     // [Tkv, Hkv, D]
+    const __nv_bfloat16* v;     // [Tkv, Hkv, D]
+    const float* sinks;         // [Hq]
+    float* out;                 // [Tq, Hq, D]
+    int Tq, Tkv, Hq, Hkv, window, q_start;
+    float scale_log2;           // log2(e) / sqrt(D)
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// rows [r0, r0 + 64) of a [T, H, D] tensor's head h into smem (zero past T)
+__device__ __forceinline__ void load_tile(__nv_bfloat16* dst, const __nv_bfloat16* src, int r0,
+                                          int T, int H, int h) {
+    for (int i = threadIdx.x; i < 64 * (kD / 8); i += kThreadsAttn) {
+        const int r = i / (kD / 8), c = (i % (kD / 8)) * 8;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r0 + r < T)
+            val = *reinterpret_cast<const uint4*>(src + (static_cast<size_t>(r0 + r) * H + h) * kD + c);
+        *reinterpret_cast<uint4*>(dst + r * kLd + c) = val;
+    }
+}
+
+__global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const AttnParams p) {
+    __shared__ __align__(16) __nv_bfloat16 qs[kBq * kLd];
+    __shared__ __align__(16) __nv_bfloat16 ks[kBk * kLd];
+    __shared__ __align__(16) __nv_bfloat16 vs[kBk * kLd];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int q0 = blockIdx.x * kBq;
+    const int h = blockIdx.y;
+    const int hk = h / (p.Hq / p.Hkv);
+
+    load_tile(qs, p.q, q0, p.Tq, p.Hq, h);
+    __syncthreads();
+
+    // this warp's Q fragments (16 rows x 64), kept in registers
+    uint32_t qa[4][4];
+    {
+        const __nv_bfloat16* base = qs + (warp * 16) * kLd;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int c = kk * 16 + 2 * t;
+            qa[kk][0] = *reinterpret_cast<const uint32_t*>(base + g * kLd + c);
+            qa[kk][1] = *reinterpret_cast<const uint32_t*>(base + (g + 8) * kLd + c);
+            qa[kk][2] = *reinterpret_cast<const uint32_t*>(base + g * kLd + c + 8);
+            qa[kk][3] = *reinterpret_cast<const uint32_t*>(base + (g + 8) * kLd + c + 8);
+        }
+    }
+
+    // rows g and g + 8 of this warp: positions, running max (log2 domain),
+    // denominator, output accumulators
+    const int row_a = q0 + warp * 16 + g, row_b = row_a + 8;
+    const int pos_a = p.q_start + row_a, pos_b = p.q_start + row_b;
+    const float sink2 = p.sinks[h] * 1.4426950408889634f;
+    float m_a = sink2, m_b = sink2;
+    const float l0 = isinf(sink2) && sink2 < 0.f ? 0.f : 1.f;
+    float l_a = l0, l_b = l0;
+    float o[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+    // key tiles that any row of this CTA can see
+    const int last_row = min(q0 + kBq, p.Tq) - 1;
+    const int kv_hi = min(p.Tkv, p.q_start + last_row + 1);
+    int kv_lo = p.window > 0 ? max(0, p.q_start + q0 - p.window + 1) : 0;
+    kv_lo = kv_lo / kBk * kBk;
+
+    for (int kv0 = kv_lo; kv0 < kv_hi; kv0 += kBk) {
+        __syncthreads();                      // previous tile's readers are done
+        load_tile(ks, p.k, kv0, p.Tkv, p.Hkv, hk);
+        load_tile(vs, p.v, kv0, p.Tkv, p.Hkv, hk);
+        __syncthreads();
+
+        // S = Q K^T: 16 x 64 per warp, 8 n-tiles of 8 keys
+        float s[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+            const __nv_bfloat16* kr = ks + (j * 8 + g) * kLd;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int c = kk * 16 + 2 * t;
+                mma_bf16_16816(s[j], qa[kk], *reinterpret_cast<const uint32_t*>(kr + c),
+                               *reinterpret_cast<const uint32_t*>(kr + c + 8));
+            }
+        }
+        // scale, mask (future keys, keys that slid out of the window, keys
+        // past Tkv), tile row maxima
+        float tm_a = -INFINITY, tm_b = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kv = kv0 + j * 8 + 2 * t + (e & 1);
+                const int pos = e < 2 ? pos_a : pos_b;
+                const bool ok = kv <= pos && kv < p.Tkv && (p.window <= 0 || kv > pos - p.window);
+                const float v = ok ? s[j][e] * p.scale_log2 : -INFINITY;
+                s[j][e] = v;
+                if (e < 2) tm_a = fmaxf(tm_a, v); else tm_b = fmaxf(tm_b, v);
+            }
+        }
+        tm_a = fmaxf(tm_a, __shfl_xor_sync(0xffffffffu, tm_a, 1));
+        tm_a = fmaxf(tm_a, __shfl_xor_sync(0xffffffffu, tm_a, 2));
+        tm_b = fmaxf(tm_b, __shfl_xor_sync(0xffffffffu, tm_b, 1));
+        tm_b = fmaxf(tm_b, __shfl_xor_sync(0xffffffffu, tm_b, 2));
+        // empty-tile guard: a fully masked row keeps its state (its p = 0)
+        const bool live_a = tm_a != -INFINITY, live_b = tm_b != -INFINITY;
+        const float mn_a = live_a ? fmaxf(m_a, tm_a) : m_a;
+        const float mn_b = live_b ? fmaxf(m_b, tm_b) : m_b;
+        const float al_a = live_a && m_a != -INFINITY ? exp2f(m_a - mn_a) : (live_a ? 0.f : 1.f);
+        const float al_b = live_b && m_b != -INFINITY ? exp2f(m_b - mn_b) : (live_b ? 0.f : 1.f);
+        m_a = mn_a;
+        m_b = mn_b;
+        float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            s[j][0] = live_a ? exp2f(s[j][0] - m_a) : 0.f;
+            s[j][1] = live_a ? exp2f(s[j][1] - m_a) : 0.f;
+            s[j][2] = live_b ? exp2f(s[j][2] - m_b) : 0.f;
+            s[j][3] = live_b ? exp2f(s[j][3] - m_b) : 0.f;
+            ps_a += s[j][0] + s[j][1];
+            ps_b += s[j][2] + s[j][3];
+            o[j][0] *= al_a;
+            o[j][1] *= al_a;
+            o[j][2] *= al_b;
+            o[j][3] *= al_b;
+        }
+        ps_a += __shfl_xor_sync(0xffffffffu, ps_a, 1);
+        ps_a += __shfl_xor_sync(0xffffffffu, ps_a, 2);
+        ps_b += __shfl_xor_sync(0xffffffffu, ps_b, 1);
+        ps_b += __shfl_xor_sync(0xffffffffu, ps_b, 2);
+        l_a = l_a * al_a + ps_a;
+        l_b = l_b * al_b + ps_b;
+
+        // O += P V: P from the S accumulators (bf16), V columns as B
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            uint32_t pa[4];
+            pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+            pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+            pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+            pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+            const __nv_bfloat16* v0 = vs + (kk * 16 + 2 * t) * kLd;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = j * 8 + g;
+                const uint32_t b0 = static_cast<uint32_t>(__bfloat16_as_ushort(v0[c])) |
+                                    (static_cast<uint32_t>(__bfloat16_as_ushort(v0[kLd + c])) << 16);
+                const uint32_t b1 =
+                    static_cast<uint32_t>(__bfloat16_as_ushort(v0[8 * kLd + c])) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(v0[9 * kLd + c])) << 16);
+                mma_bf16_16816(o[j], pa, b0, b1);
+            }
+        }
+    }
+
+    // out = O / l (l includes the sink's share)
+    const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f, inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int c = j * 8 + 2 * t;
+        if (row_a < p.Tq) {
+            float* dst = p.out + (static_cast<size_t>(row_a) * p.Hq + h) * kD + c;
+            *reinterpret_cast<float2*>(dst) = make_float2(o[j][0] * inv_a, o[j][1] * inv_a);
+        }
+        if (row_b < p.Tq) {
+            float* dst = p.out + (static_cast<size_t>(row_b) * p.Hq + h) * kD + c;
+            *reinterpret_cast<float2*>(dst) = make_float2(o[j][2] * inv_b, o[j][3] * inv_b);
+        }
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_attention_sinks(const moe_attn_shape* shape, const void* q,
+                                          const void* k, const void* v, const float* sinks,
+                                          float* out, cudaStream_t stream) {
+    if (!shape || !q || !k || !v || !sinks || !out) return MOE_ERR_ARG;
+    const moe_attn_shape s = *shape;
+    if (s.D != kD || s.Hkv < 1 || s.Hq < s.Hkv || s.Hq % s.Hkv || s.Hq > 65535 || s.Tq < 0 ||
+        s.Tkv < 1 || s.q_start < 0 || s.q_start + s.Tq > s.Tkv || s.window < 0)
+        return MOE_ERR_SHAPE;
+    for (const void* ptr : {q, k, v, static_cast<const void*>(out)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15) return MOE_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(sinks) & 3) return MOE_ERR_ALIGN;
+    if (s.Tq == 0) return MOE_OK;
+    AttnParams p;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.sinks = sinks;
+    p.out = out;
+    p.Tq = s.Tq;
+    p.Tkv = s.Tkv;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.window = s.window;
+    p.q_start = s.q_start;
+    p.scale_log2 = 1.4426950408889634f / 8.0f;     // log2(e) / sqrt(64)
+    const dim3 grid((s.Tq + kBq - 1) / kBq, s.Hq);
+    attention_sinks_kernel<<<grid, kThreadsAttn, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

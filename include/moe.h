@@ -249,6 +249,31 @@ moe_status moe_profile_enable(int calls);
 moe_status moe_profile_read(const char** names, float* ms, int cap,
                             int* count);
 
+/* Attention with sinks, the other half of a gpt-oss block (§1 model-
+ * architecture table, "attention" row: sliding-window (128) and full layers
+ * alternate; one learnable sink logit per head; GQA).
+ *   Query i (position q_start + i) of head h attends to the keys j of KV
+ *   head h / (Hq / Hkv) with j <= q_start + i and, when window > 0,
+ *   j > q_start + i - window; scores s_j = q.k_j / sqrt(D); the sink is one
+ *   more logit in the softmax's denominator that carries no value:
+ *     out = sum_j exp(s_j) v_j / (exp(sink_h) + sum_j exp(s_j))
+ *   (sink = -inf: plain causal / windowed softmax attention).
+ * A prefill passes Tq = Tkv, q_start = 0; a decode step Tq new queries at
+ * the end of a cache of Tkv keys, q_start = Tkv - Tq.
+ *   q bf16 [Tq, Hq, D]; k, v bf16 [Tkv, Hkv, D] (post-rotary q and k);
+ *   sinks fp32 [Hq] (4-byte aligned); out fp32 [Tq, Hq, D].
+ * Supported: D == 64, Hq a multiple of Hkv, 0 <= q_start, q_start + Tq <=
+ * Tkv, window >= 0 (0 = full).  Enqueued on `stream`; no workspace. */
+typedef struct {
+    int Tq, Tkv, Hq, Hkv, D;
+    int window;                /* keys per query's window, 0 = full */
+    int q_start;               /* position of query 0 */
+} moe_attn_shape;
+
+moe_status moe_attention_sinks(const moe_attn_shape* shape, const void* q, const void* k,
+                               const void* v, const float* sinks, float* out,
+                               cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* moe_status_str(moe_status status);
 

@@ -1,0 +1,63 @@
+"""Attention with sinks on the GPU against the fp64 CPU oracle (the other
+half of a gpt-oss block: sliding-window / full layers, per-head sinks, GQA)."""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2      # P is rounded to bf16 for the second MMA
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from gpt_oss_moe_gb300 import _build
+    _build.build()
+    import gpt_oss_moe_gb300 as m
+    return m
+
+
+CASES = [
+    # Tq, Tkv, Hq, Hkv, window, sinks ("n": N(0,1), "none": -inf, "big": +20)
+    (1, 1, 8, 1, 0, "n"),
+    (70, 70, 8, 2, 0, "n"),              # ragged query and key tails
+    (300, 300, 8, 1, 128, "n"),          # tiles that slid out of the window
+    (300, 300, 8, 1, 128, "none"),       # ... with no sink: the running max starts at -inf
+    (200, 200, 4, 4, 1, "n"),            # window of one key
+    (512, 512, 64, 8, 128, "n"),         # gpt-oss sliding layer
+    (512, 512, 64, 8, 0, "n"),           # gpt-oss full layer
+    (130, 130, 8, 2, 0, "big"),          # the sink takes almost all the mass
+    (1, 1000, 64, 8, 128, "n"),          # decode step, sliding
+    (1, 1000, 64, 8, 0, "n"),            # decode step, full
+    (5, 700, 16, 2, 128, "none"),        # several new queries at the end of a cache
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "Tq{}Tkv{}Hq{}Hkv{}W{}{}".format(*c))
+def test_attention_sinks_matches_oracle(moe, oracle_lib, synth_lib, case):
+    Tq, Tkv, Hq, Hkv, W, sk = case
+    a = synth_lib.make_attention(Tkv, Tkv, Hq=Hq, Hkv=Hkv, D=64, seed=Tq + Tkv + W)
+    q = a["q"][Tkv - Tq:]
+    sinks = a["sinks"]
+    if sk == "none":
+        sinks = torch.full_like(sinks, float("-inf"))
+    elif sk == "big":
+        sinks = torch.full_like(sinks, 20.0)
+    ref = oracle_lib.attention_sinks(q, a["k"], a["v"], sinks, window=W)
+    out = moe.attention_sinks(q.cuda(), a["k"].cuda(), a["v"].cuda(), sinks.cuda(), window=W)
+    torch.cuda.synchronize()
+    got = out.cpu()
+    assert torch.isfinite(got).all()
+    err = (got - ref).abs().max().item()
+    assert err <= TOL * max(ref.abs().max().item(), 1e-30), err
+
+
+def test_attention_rejects_bad_shapes(moe):
+    q = torch.zeros((4, 8, 32), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((4, 2, 32), dtype=torch.bfloat16, device="cuda")
+    s = torch.zeros(8, device="cuda")
+    with pytest.raises(Exception):
+        moe.attention_sinks(q, k, k, s)                     # D = 32
+    q = torch.zeros((4, 6, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((4, 4, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(Exception):
+        moe.attention_sinks(q, k, k, torch.zeros(6, device="cuda"))   # 6 % 4 != 0
