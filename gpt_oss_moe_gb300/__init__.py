@@ -29,7 +29,7 @@ EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_ep",
            "moe_forward_noalloc", "moe_get_device_status",
            "moe_clear_device_status",
            "moe_set_tuning", "moe_profile_enable", "moe_profile_read",
-           "moe_status_str", "moe_attention_sinks")
+           "moe_status_str", "moe_attention_sinks", "moe_attention_workspace_bytes")
 
 
 class MoEError(RuntimeError):
@@ -81,8 +81,10 @@ def lib():
                                          vp, vp, vp, sz, vp]
             L.moe_forward_ep.restype = i
             L.moe_attention_sinks.argtypes = [ctypes.POINTER(moe_attn_shape), vp, vp, vp, vp,
-                                              vp, vp]
+                                              vp, vp, sz, vp]
             L.moe_attention_sinks.restype = i
+            L.moe_attention_workspace_bytes.argtypes = [ctypes.POINTER(moe_attn_shape)]
+            L.moe_attention_workspace_bytes.restype = sz
             L.moe_forward_noalloc.argtypes = [S, vp, vp, vp, moe_weight, moe_weight,
                                               vp, i, vp, vp, vp, vp]
             L.moe_forward_noalloc.restype = i
@@ -197,7 +199,8 @@ def moe_forward_ep(shape, expert_start, local_experts, hidden, router_w, router_
     return ws
 
 
-def attention_sinks(q, k, v, sinks, out=None, window: int = 0, q_start=None, stream=None):
+def attention_sinks(q, k, v, sinks, out=None, window: int = 0, q_start=None, workspace=None,
+                    stream=None):
     """Attention with sinks on the GPU: q [Tq, Hq, 64], k / v [Tkv, Hkv, 64]
     bf16, sinks [Hq] fp32 -> out [Tq, Hq, 64] fp32 (see moe_attention_sinks)."""
     Tq, Hq, D = q.shape
@@ -206,8 +209,12 @@ def attention_sinks(q, k, v, sinks, out=None, window: int = 0, q_start=None, str
         out = torch.empty((Tq, Hq, D), dtype=torch.float32, device=q.device)
     shape = moe_attn_shape(int(Tq), int(Tkv), int(Hq), int(Hkv), int(D), int(window),
                            int(Tkv - Tq if q_start is None else q_start))
+    need = lib().moe_attention_workspace_bytes(ctypes.byref(shape))
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     code = lib().moe_attention_sinks(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(sinks),
-                                     _p(out), _stream(stream))
+                                     _p(out), _p(workspace) if need else None,
+                                     workspace.numel() if need else 0, _stream(stream))
     _check(code, "moe_attention_sinks")
     return out
 

@@ -4,7 +4,11 @@
 // alternate, one learnable sink logit per head, 64 query / 8 KV heads of
 // dim 64; §3 on the fully masked tile of a sliding window).
 //
-// One CTA per (64 query rows, query head), four warps of 16 rows.  Per KV
+// One CTA per (64 query rows, query head, key split), four warps of 16
+// rows.  Small grids (decode: one query block per head) split each block's
+// key tiles over several CTAs (flash-decoding); each writes its unnormalised
+// output with its running max and sum, and a second kernel merges the splits
+// and adds the sink's share once.  Per KV
 // tile of 64 keys: S = Q K^T on the tensor cores (mma.sync m16n8k16, bf16 in,
 // fp32 out), scale and mask, online softmax in the exp2 domain, O += P V
 // (P rounded to bf16).  The sink enters as the running max's starting value
@@ -34,6 +38,9 @@ struct AttnParams {
     float* out;                 // [Tq, Hq, D]
     int Tq, Tkv, Hq, Hkv, window, q_start;
     float scale_log2;           // log2(e) / sqrt(D)
+    int nsplit;                 // key splits per query block (grid.z)
+    float* part_o;              // [nsplit, Tq, Hq, D] unnormalised (nsplit > 1)
+    float2* part_ml;            // [nsplit, Tq, Hq] (running max log2, sum)
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
@@ -95,8 +102,10 @@ __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const Att
     const int row_a = q0 + warp * 16 + g, row_b = row_a + 8;
     const int pos_a = p.q_start + row_a, pos_b = p.q_start + row_b;
     const float sink2 = p.sinks[h] * 1.4426950408889634f;
-    float m_a = sink2, m_b = sink2;
-    const float l0 = isinf(sink2) && sink2 < 0.f ? 0.f : 1.f;
+    // split runs start without the sink (the merge adds it once)
+    const bool whole = p.nsplit == 1;
+    float m_a = whole ? sink2 : -INFINITY, m_b = m_a;
+    const float l0 = !whole || (isinf(sink2) && sink2 < 0.f) ? 0.f : 1.f;
     float l_a = l0, l_b = l0;
     float o[8][4];
 #pragma unroll
@@ -107,8 +116,12 @@ __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const Att
     const int kv_hi = min(p.Tkv, p.q_start + last_row + 1);
     int kv_lo = p.window > 0 ? max(0, p.q_start + q0 - p.window + 1) : 0;
     kv_lo = kv_lo / kBk * kBk;
+    // this split's share of the block's key tiles
+    const int ntile = kv_hi > kv_lo ? (kv_hi - kv_lo + kBk - 1) / kBk : 0;
+    const int per = (ntile + p.nsplit - 1) / p.nsplit;
+    const int t_lo = blockIdx.z * per, t_hi = min(ntile, t_lo + per);
 
-    for (int kv0 = kv_lo; kv0 < kv_hi; kv0 += kBk) {
+    for (int kv0 = kv_lo + t_lo * kBk; kv0 < kv_lo + t_hi * kBk; kv0 += kBk) {
         __syncthreads();                      // previous tile's readers are done
         load_tile(ks, p.k, kv0, p.Tkv, p.Hkv, hk);
         load_tile(vs, p.v, kv0, p.Tkv, p.Hkv, hk);
@@ -197,6 +210,25 @@ __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const Att
         }
     }
 
+    if (!whole) {
+        // this split's unnormalised output, running max and sum
+        const size_t plane = static_cast<size_t>(blockIdx.z) * p.Tq * p.Hq;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = j * 8 + 2 * t;
+            if (row_a < p.Tq)
+                *reinterpret_cast<float2*>(p.part_o + ((plane + static_cast<size_t>(row_a) * p.Hq + h) * kD + c)) =
+                    make_float2(o[j][0], o[j][1]);
+            if (row_b < p.Tq)
+                *reinterpret_cast<float2*>(p.part_o + ((plane + static_cast<size_t>(row_b) * p.Hq + h) * kD + c)) =
+                    make_float2(o[j][2], o[j][3]);
+        }
+        if (t == 0) {
+            if (row_a < p.Tq) p.part_ml[plane + static_cast<size_t>(row_a) * p.Hq + h] = make_float2(m_a, l_a);
+            if (row_b < p.Tq) p.part_ml[plane + static_cast<size_t>(row_b) * p.Hq + h] = make_float2(m_b, l_b);
+        }
+        return;
+    }
     // out = O / l (l includes the sink's share)
     const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f, inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
 #pragma unroll
@@ -213,23 +245,93 @@ __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const Att
     }
 }
 
+// Merge of the key splits: one CTA of 64 threads (one per output column) per
+// (query row, head).  M = max(sink, m_s), L = exp2(sink - M) + sum l_s
+// exp2(m_s - M), out = sum o_s exp2(m_s - M) / L; splits without live keys
+// (m_s = -inf) add nothing.
+__global__ void __launch_bounds__(kD) attention_merge_kernel(const AttnParams p) {
+    const int r = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+    const size_t rh = static_cast<size_t>(r) * p.Hq + h;
+    const size_t plane = static_cast<size_t>(p.Tq) * p.Hq;
+    const float sink2 = p.sinks[h] * 1.4426950408889634f;
+    float M = sink2;
+    for (int z = 0; z < p.nsplit; ++z) M = fmaxf(M, p.part_ml[z * plane + rh].x);
+    float L = M == -INFINITY || sink2 == -INFINITY ? 0.f : exp2f(sink2 - M);
+    float acc = 0.f;
+    for (int z = 0; z < p.nsplit; ++z) {
+        const float2 ml = p.part_ml[z * plane + rh];
+        if (ml.x == -INFINITY) continue;
+        const float f = exp2f(ml.x - M);
+        L += ml.y * f;
+        acc += p.part_o[(z * plane + rh) * kD + d] * f;
+    }
+    p.out[rh * kD + d] = L > 0.f ? acc / L : 0.f;
+}
+
+// Key splits: enough CTAs for about four waves, at least two key tiles per
+// split (counted for the last query block, the widest under causality), at
+// most kMaxSplit.  Grids of four waves or more need none.
+constexpr int kMaxSplit = 32;
+int attn_splits(const moe_attn_shape& s, int sms) {
+    const int qb = (s.Tq + kBq - 1) / kBq;
+    const long long ctas = static_cast<long long>(qb) * s.Hq;
+    const int kv_hi = min(s.Tkv, s.q_start + s.Tq);
+    int kv_lo = s.window > 0 ? max(0, s.q_start + (qb - 1) * kBq - s.window + 1) : 0;
+    kv_lo = kv_lo / kBk * kBk;
+    const int tiles = kv_hi > kv_lo ? (kv_hi - kv_lo + kBk - 1) / kBk : 0;
+    long long n = (4LL * sms + ctas - 1) / ctas;
+    if (n > tiles / 2) n = tiles / 2;
+    if (n > kMaxSplit) n = kMaxSplit;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 152;
+    }
+    return sms;
+}
+
+bool attn_shape_ok(const moe_attn_shape& s) {
+    return s.D == kD && s.Hkv >= 1 && s.Hq >= s.Hkv && s.Hq % s.Hkv == 0 && s.Hq <= 65535 &&
+           s.Tq >= 0 && s.Tkv >= 1 && s.q_start >= 0 && s.q_start + s.Tq <= s.Tkv &&
+           s.window >= 0;
+}
+
+size_t attn_ws_bytes(const moe_attn_shape& s, int nsplit) {
+    if (nsplit <= 1) return 0;
+    const size_t rows = static_cast<size_t>(nsplit) * s.Tq * s.Hq;
+    return rows * kD * sizeof(float) + 256 + rows * sizeof(float2);
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
 
+extern "C" size_t moe_attention_workspace_bytes(const moe_attn_shape* shape) {
+    if (!shape || !attn_shape_ok(*shape)) return 0;
+    return attn_ws_bytes(*shape, attn_splits(*shape, sm_count()));
+}
+
 extern "C" moe_status moe_attention_sinks(const moe_attn_shape* shape, const void* q,
                                           const void* k, const void* v, const float* sinks,
-                                          float* out, cudaStream_t stream) {
+                                          float* out, void* workspace, size_t workspace_bytes,
+                                          cudaStream_t stream) {
     if (!shape || !q || !k || !v || !sinks || !out) return MOE_ERR_ARG;
     const moe_attn_shape s = *shape;
-    if (s.D != kD || s.Hkv < 1 || s.Hq < s.Hkv || s.Hq % s.Hkv || s.Hq > 65535 || s.Tq < 0 ||
-        s.Tkv < 1 || s.q_start < 0 || s.q_start + s.Tq > s.Tkv || s.window < 0)
-        return MOE_ERR_SHAPE;
+    if (!attn_shape_ok(s)) return MOE_ERR_SHAPE;
     for (const void* ptr : {q, k, v, static_cast<const void*>(out)})
         if (reinterpret_cast<uintptr_t>(ptr) & 15) return MOE_ERR_ALIGN;
     if (reinterpret_cast<uintptr_t>(sinks) & 3) return MOE_ERR_ALIGN;
     if (s.Tq == 0) return MOE_OK;
+    const int nsplit = attn_splits(s, sm_count());
+    const size_t need = attn_ws_bytes(s, nsplit);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 15)) return MOE_ERR_ALIGN;
     AttnParams p;
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.k = static_cast<const __nv_bfloat16*>(k);
@@ -243,7 +345,15 @@ extern "C" moe_status moe_attention_sinks(const moe_attn_shape* shape, const voi
     p.window = s.window;
     p.q_start = s.q_start;
     p.scale_log2 = 1.4426950408889634f / 8.0f;     // log2(e) / sqrt(64)
-    const dim3 grid((s.Tq + kBq - 1) / kBq, s.Hq);
+    p.nsplit = nsplit;
+    const size_t rows = static_cast<size_t>(nsplit) * s.Tq * s.Hq;
+    p.part_o = static_cast<float*>(workspace);
+    p.part_ml = need > 0 ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
+                                                     (rows * kD * sizeof(float) + 255) / 256 * 256)
+                         : nullptr;
+    const dim3 grid((s.Tq + kBq - 1) / kBq, s.Hq, nsplit);
     attention_sinks_kernel<<<grid, kThreadsAttn, 0, stream>>>(p);
+    if (nsplit > 1)
+        attention_merge_kernel<<<dim3(s.Tq, s.Hq), kD, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -263,15 +263,26 @@ moe_status moe_profile_read(const char** names, float* ms, int cap,
  *   q bf16 [Tq, Hq, D]; k, v bf16 [Tkv, Hkv, D] (post-rotary q and k);
  *   sinks fp32 [Hq] (4-byte aligned); out fp32 [Tq, Hq, D].
  * Supported: D == 64, Hq a multiple of Hkv, 0 <= q_start, q_start + Tq <=
- * Tkv, window >= 0 (0 = full).  Enqueued on `stream`; no workspace. */
+ * Tkv, window >= 0 (0 = full).  Enqueued on `stream`. */
 typedef struct {
     int Tq, Tkv, Hq, Hkv, D;
     int window;                /* keys per query's window, 0 = full */
     int q_start;               /* position of query 0 */
 } moe_attn_shape;
 
+/* Bytes of scratch moe_attention_sinks needs for this shape on the current
+ * device (0: none; small grids -- decode -- split the keys over several
+ * CTAs and merge their partial results through it; 0 also for an invalid
+ * shape). */
+size_t moe_attention_workspace_bytes(const moe_attn_shape* shape);
+
+/* workspace: device scratch of at least moe_attention_workspace_bytes
+ * (NULL when that is 0), 16-byte aligned, owned by the caller; its contents
+ * between calls are unspecified.  MOE_ERR_WORKSPACE when it is missing or
+ * too small. */
 moe_status moe_attention_sinks(const moe_attn_shape* shape, const void* q, const void* k,
                                const void* v, const float* sinks, float* out,
+                               void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 
 /* Static description of a status code. */

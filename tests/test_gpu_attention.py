@@ -29,6 +29,8 @@ CASES = [
     (1, 1000, 64, 8, 128, "n"),          # decode step, sliding
     (1, 1000, 64, 8, 0, "n"),            # decode step, full
     (5, 700, 16, 2, 128, "none"),        # several new queries at the end of a cache
+    (64, 2048, 8, 1, 0, "n"),            # keys split over 16 CTAs, merged
+    (200, 3000, 8, 2, 0, "none"),        # split keys, no sink, four query blocks
 ]
 
 
