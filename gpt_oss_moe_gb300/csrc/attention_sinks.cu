@@ -69,10 +69,39 @@ __device__ __forceinline__ void load_tile(__nv_bfloat16* dst, const __nv_bfloat1
     }
 }
 
+// The same rows copied asynchronously (cp.async, 16 B per thread and step;
+// rows past T are zero-filled: source size 0).
+__device__ __forceinline__ void load_tile_async(__nv_bfloat16* dst, const __nv_bfloat16* src,
+                                                int r0, int T, int H, int h) {
+    for (int i = threadIdx.x; i < 64 * (kD / 8); i += kThreadsAttn) {
+        const int r = i / (kD / 8), c = (i % (kD / 8)) * 8;
+        const bool in = r0 + r < T;
+        const __nv_bfloat16* g = in ? src + (static_cast<size_t>(r0 + r) * H + h) * kD + c : src;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                     ::"r"(smem_u32(dst + r * kLd + c)), "l"(g), "r"(in ? 16 : 0) : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Four 8x8 bf16 matrices, transposed: lane L gives the address of row L % 8
+// of matrix L / 8; each register receives, for its matrix, the elements
+// (2t, g) and (2t + 1, g) -- a B fragment of m16n8k16 from a [k][n] tile.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
 __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const AttnParams p) {
     __shared__ __align__(16) __nv_bfloat16 qs[kBq * kLd];
-    __shared__ __align__(16) __nv_bfloat16 ks[kBk * kLd];
-    __shared__ __align__(16) __nv_bfloat16 vs[kBk * kLd];
+    __shared__ __align__(16) __nv_bfloat16 ks[2][kBk * kLd];   // double-buffered
+    __shared__ __align__(16) __nv_bfloat16 vs[2][kBk * kLd];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -121,10 +150,25 @@ __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const Att
     const int per = (ntile + p.nsplit - 1) / p.nsplit;
     const int t_lo = blockIdx.z * per, t_hi = min(ntile, t_lo + per);
 
-    for (int kv0 = kv_lo + t_lo * kBk; kv0 < kv_lo + t_hi * kBk; kv0 += kBk) {
-        __syncthreads();                      // previous tile's readers are done
-        load_tile(ks, p.k, kv0, p.Tkv, p.Hkv, hk);
-        load_tile(vs, p.v, kv0, p.Tkv, p.Hkv, hk);
+    // tile it + 1 loads while tile it computes
+    if (t_lo < t_hi) {
+        load_tile_async(ks[0], p.k, kv_lo + t_lo * kBk, p.Tkv, p.Hkv, hk);
+        load_tile_async(vs[0], p.v, kv_lo + t_lo * kBk, p.Tkv, p.Hkv, hk);
+        cp_async_commit();
+    }
+    for (int it = t_lo; it < t_hi; ++it) {
+        const int kv0 = kv_lo + it * kBk;
+        const int buf = (it - t_lo) & 1;
+        if (it + 1 < t_hi) {
+            // buffer buf ^ 1 was last read in the previous iteration, which
+            // ended with a barrier
+            load_tile_async(ks[buf ^ 1], p.k, kv0 + kBk, p.Tkv, p.Hkv, hk);
+            load_tile_async(vs[buf ^ 1], p.v, kv0 + kBk, p.Tkv, p.Hkv, hk);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
         __syncthreads();
 
         // S = Q K^T: 16 x 64 per warp, 8 n-tiles of 8 keys
@@ -132,7 +176,7 @@ __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const Att
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-            const __nv_bfloat16* kr = ks + (j * 8 + g) * kLd;
+            const __nv_bfloat16* kr = ks[buf] + (j * 8 + g) * kLd;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const int c = kk * 16 + 2 * t;
@@ -196,18 +240,19 @@ __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const Att
             pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
             pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
             pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-            const __nv_bfloat16* v0 = vs + (kk * 16 + 2 * t) * kLd;
+            // V rows kk*16 .. +15 (k) x columns 8j .. 8j+15 (two n-tiles)
+            const int mat = lane >> 3;
+            const uint32_t vrow = smem_u32(vs[buf] + (kk * 16 + (mat & 1) * 8 + (lane & 7)) * kLd +
+                                           (mat >> 1) * 8);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int c = j * 8 + g;
-                const uint32_t b0 = static_cast<uint32_t>(__bfloat16_as_ushort(v0[c])) |
-                                    (static_cast<uint32_t>(__bfloat16_as_ushort(v0[kLd + c])) << 16);
-                const uint32_t b1 =
-                    static_cast<uint32_t>(__bfloat16_as_ushort(v0[8 * kLd + c])) |
-                    (static_cast<uint32_t>(__bfloat16_as_ushort(v0[9 * kLd + c])) << 16);
+            for (int j = 0; j < 8; j += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(vrow + j * 16, b0, b1, b2, b3);
                 mma_bf16_16816(o[j], pa, b0, b1);
+                mma_bf16_16816(o[j + 1], pa, b2, b3);
             }
         }
+        __syncthreads();                      // both buffers' readers are done
     }
 
     if (!whole) {
