@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kThreadsAttn) attention_sinks_kernel(const Att
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int q0 = blockIdx.x * kBq;
+    // later query blocks see the most keys (causal): they start first
+    const int q0 = (gridDim.x - 1 - blockIdx.x) * kBq;
     const int h = blockIdx.y;
     const int hk = h / (p.Hq / p.Hkv);
 
