@@ -31,6 +31,8 @@ CASES = [
     (5, 700, 16, 2, 128, "none"),        # several new queries at the end of a cache
     (64, 2048, 8, 1, 0, "n"),            # keys split over 16 CTAs, merged
     (200, 3000, 8, 2, 0, "none"),        # split keys, no sink, four query blocks
+    (100, 100, 12, 4, 0, "n"),           # 3 heads per KV head: one head per CTA
+    (1, 500, 12, 4, 128, "n"),           # ... decode
 ]
 
 
