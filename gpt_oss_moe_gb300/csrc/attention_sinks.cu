@@ -345,6 +345,7 @@ int attn_splits(const moe_attn_shape& s, int sms) {
     const int qpb = attn_qpb(s);
     const int qb = (s.Tq + qpb - 1) / qpb;
     const long long ctas = static_cast<long long>(qb) * (attn_grouped(s) ? s.Hkv : s.Hq);
+    if (ctas == 0) return 1;                               // Tq == 0: nothing to split
     const int kv_hi = min(s.Tkv, s.q_start + s.Tq);
     int kv_lo = s.window > 0 ? max(0, s.q_start + (qb - 1) * qpb - s.window + 1) : 0;
     kv_lo = kv_lo / kBk * kBk;
@@ -391,13 +392,14 @@ extern "C" moe_status moe_attention_sinks(const moe_attn_shape* shape, const voi
                                           const void* k, const void* v, const float* sinks,
                                           float* out, void* workspace, size_t workspace_bytes,
                                           cudaStream_t stream) {
-    if (!shape || !q || !k || !v || !sinks || !out) return MOE_ERR_ARG;
+    if (!shape) return MOE_ERR_ARG;
     const moe_attn_shape s = *shape;
     if (!attn_shape_ok(s)) return MOE_ERR_SHAPE;
+    if (s.Tq == 0) return MOE_OK;            // nothing to do (pointers may be null)
+    if (!q || !k || !v || !sinks || !out) return MOE_ERR_ARG;
     for (const void* ptr : {q, k, v, static_cast<const void*>(out)})
         if (reinterpret_cast<uintptr_t>(ptr) & 15) return MOE_ERR_ALIGN;
     if (reinterpret_cast<uintptr_t>(sinks) & 3) return MOE_ERR_ALIGN;
-    if (s.Tq == 0) return MOE_OK;
     const int nsplit = attn_splits(s, sm_count());
     const size_t need = attn_ws_bytes(s, nsplit);
     if (need > 0 && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;

@@ -263,7 +263,8 @@ moe_status moe_profile_read(const char** names, float* ms, int cap,
  *   q bf16 [Tq, Hq, D]; k, v bf16 [Tkv, Hkv, D] (post-rotary q and k);
  *   sinks fp32 [Hq] (4-byte aligned); out fp32 [Tq, Hq, D].
  * Supported: D == 64, Hq a multiple of Hkv, 0 <= q_start, q_start + Tq <=
- * Tkv, window >= 0 (0 = full).  Enqueued on `stream`. */
+ * Tkv, window >= 0 (0 = full).  Enqueued on `stream`; Tq == 0 is valid and
+ * enqueues nothing (pointers may then be NULL). */
 typedef struct {
     int Tq, Tkv, Hq, Hkv, D;
     int window;                /* keys per query's window, 0 = full */

@@ -128,6 +128,30 @@ def test_ep_expert_ranges_partition_the_experts(moe):
         moe.ep_expert_range(0, 5, 4)
 
 
+def test_attention_workspace_and_argument_checks_on_the_host(moe):
+    L = moe.lib()
+
+    def shape(**kw):
+        d = dict(Tq=4, Tkv=4, Hq=8, Hkv=1, D=64, window=0, q_start=0)
+        d.update(kw)
+        return moe.moe_attn_shape(*[d[n] for n, _ in moe.moe_attn_shape._fields_])
+    ws = L.moe_attention_workspace_bytes
+    assert ws(ctypes.byref(shape(Tq=0, q_start=4))) == 0          # nothing to split
+    assert ws(ctypes.byref(shape(D=32))) == 0                     # invalid shape
+    assert ws(ctypes.byref(shape(Tq=1, Tkv=4096, q_start=4095))) > 0   # decode splits
+    call = lambda s, q=16, sinks=32: L.moe_attention_sinks(ctypes.byref(s), q, 48, 64, sinks,
+                                                           80, None, 0, None)
+    assert call(shape(D=32)) == -2
+    assert call(shape(Hq=6, Hkv=4)) == -2
+    assert call(shape(Tq=5)) == -2                                # q_start + Tq > Tkv
+    assert call(shape(), q=24) == -3                              # misaligned q
+    assert call(shape(), sinks=34) == -3                          # misaligned sinks
+    assert call(shape(), q=0) == -1
+    assert call(shape(Tq=0, q_start=4)) == 0                      # empty: enqueues nothing
+    assert call(shape(Tq=0, q_start=4), q=0) == 0                 # ... even with null pointers
+    assert call(shape(Tq=1, Tkv=4096, q_start=4095)) == -4        # decode needs a workspace
+
+
 def test_route_rejects_bad_arguments_on_the_host(moe):
     L = moe.lib()
     s = _shape(moe)

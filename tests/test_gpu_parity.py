@@ -588,6 +588,32 @@ def test_forward_ep_partials_match_and_sum_to_the_layer(moe, oracle_lib, synth_l
     assert (total - full).abs().max().item() <= tol * ref
 
 
+def test_forward_ep_rank_without_tokens_outputs_zero(moe, oracle_lib, synth_lib):
+    """+20 on the router bias of experts 0 and 1 with top-2 routes every
+    token there: the rank holding experts 4..7 has no tile at all and must
+    write an all-zero partial; the rank holding 0..3 carries the layer."""
+    L = synth_lib.make_layer(E=8, T=50, H=256, I=128, top_k=2, seed=905, hot=(0, 1),
+                             hot_bias=20.0, router_w_std=0.05)
+    parts = _ep_partials(moe, L, to_device(L), 2)
+    assert parts[1][2].eq(0).all()
+    _, _, full = oracle_lib.forward(L)
+    assert (parts[0][2] - full).abs().max().item() <= TOL_BF16 * full.abs().max().item()
+
+
+def test_empty_calls_enqueue_nothing(moe, synth_lib):
+    L = synth_lib.make_layer(E=8, T=4, H=128, I=128, top_k=2, seed=906)
+    dev = to_device(L)
+    shape = moe.make_shape(0, 128, 128, 8, 2)
+    out = torch.empty((1, 128), device="cuda")
+    moe.moe_forward_ep(shape, 2, 3, dev["x"], dev["wr"], dev["br"], dev["w_gu"][2:5],
+                       dev["b_gu"][2:5], dev["w_d"][2:5], dev["b_d"][2:5], out)
+    a = synth_lib.make_attention(4, 4, Hq=8, Hkv=1, D=64)
+    o = moe.attention_sinks(a["q"][:0].cuda(), a["k"].cuda(), a["v"].cuda(),
+                            a["sinks"].cuda())
+    torch.cuda.synchronize()
+    assert o.shape == (0, 8, 64)
+
+
 def test_forward_ep_20b_four_ranks(moe, oracle_lib, layer_20b_decode):
     """gpt-oss-20b widths, T = 64, four ranks of 8 experts."""
     L64, dev64 = layer_20b_decode
