@@ -92,7 +92,8 @@ struct SmemPlan {
     uint8_t* a;          // stages x 16 KB bf16 W tiles (1024-aligned)
     uint8_t* b;          // stages x kb_per_stage x box*128 B token tiles (1024-aligned)
     uint8_t* codes;      // stages x 16 KB E2M1 tiles [128 rows x 128 B], 128-byte swizzled (MXFP4)
-    uint8_t* scales;     // 2 x 128*kscale B (MXFP4)
+    uint8_t* scales;     // 2 x 128*kscale B (MXFP4, MXFP4 x MXFP8)
+    uint8_t* tscales;    // 2 x box*xs_row_bytes B: token tile scale rows (MXFP4 x MXFP8)
     int* meta_tok;       // [box] token of each tile row (combine)
     float* meta_w;       // [box] routing weight of each tile row (combine)
     uint64_t* full;      // [stages] TMA landed
@@ -113,7 +114,7 @@ struct SmemPlan {
 // MXFP4: one ring of `stages` slots, each a code tile + a token tile; the
 // converted bf16 W tiles live in TMEM, not here.
 __device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int astages, int box,
-                                              int bbox, int wf, int kscale) {
+                                              int bbox, int wf, int kscale, int xs_row_bytes) {
     SmemPlan s;
     const uint32_t base = smem_u32(raw);
     uint8_t* p = raw + ((1024u - (base & 1023u)) & 1023u);
@@ -124,10 +125,16 @@ __device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int asta
          bbox * 128;
     s.codes = p;
     s.scales = p;
+    s.tscales = p;
     if (wf == 1) {
         p += static_cast<size_t>(stages) * kCodeStageBytes;
         s.scales = p;
         p += 2 * ((kWeightTileRows * kscale + 15) / 16 * 16);
+    } else if (wf == 3) {
+        s.scales = p;
+        p += 2 * ((kWeightTileRows * kscale + 15) / 16 * 16);
+        s.tscales = p;
+        p += 2 * static_cast<size_t>(box) * xs_row_bytes;
     }
     s.meta_tok = reinterpret_cast<int*>(p);
     p += box * 4;
@@ -296,7 +303,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     const uint32_t b_bytes = static_cast<uint32_t>(bbox) * 128u;      // one 64-wide K chunk
     const uint32_t b_stage_bytes = b_bytes * KPS;
     const int n_st = (p.k_blocks + KPS - 1) / KPS;                     // ring slots per unit
-    SmemPlan sm = plan_smem(smem_raw, stages, astages, box, bbox, WF, p.kscale);
+    SmemPlan sm = plan_smem(smem_raw, stages, astages, box, bbox, WF, p.kscale, p.xs_row_bytes);
+    const uint32_t tscale_buf_bytes = static_cast<uint32_t>(box * p.xs_row_bytes);
     volatile int* flags = sm.flags;
     const uint32_t scale_buf_bytes =
         static_cast<uint32_t>((kWeightTileRows * p.kscale + 15) / 16 * 16);
@@ -318,7 +326,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             // pair: one arrival from each CTA's epilogue, on the even CTA's
             mbar_init(smem_u32(sm.tempty + b), kPair ? 2u : static_cast<uint32_t>(kEpiThreads));
             mbar_init(smem_u32(sm.sfull + b), 1);
-            mbar_init(smem_u32(sm.sempty + b), kConvTeams * kConvThreads);
+            mbar_init(smem_u32(sm.sempty + b), WF == 3 ? kMxScaleWarps : kConvTeams * kConvThreads);
         }
         mbar_init(smem_u32(sm.drain), 1);
         mbar_init(smem_u32(sm.drain + 1), 1);
@@ -365,8 +373,9 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
                 const int mb = un.mb;
-                if (WF == 1) {
+                if (WF == 1 || WF == 3) {
                     // this unit's scale rows, one bulk copy, double-buffered
+                    // (MXFP4 x MXFP8: and the token tile's scale rows)
                     const int sb = local & 1;
                     const uint32_t sph = static_cast<uint32_t>(local >> 1) & 1u;
                     if (!mbar_wait(smem_u32(sm.sempty + sb), sph ^ 1u, flags)) {
@@ -376,12 +385,17 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     }
                     const int rows = min(kWeightTileRows, p.w_rows - mb * kWeightTileRows);
                     const uint32_t bytes = static_cast<uint32_t>(rows * p.kscale);
+                    const bool tok = WF == 3 && p.xs_mx != nullptr;
+                    const uint32_t tbytes = tok ? static_cast<uint32_t>(t.z * p.xs_row_bytes) : 0u;
                     const uint32_t sf = smem_u32(sm.sfull + sb);
-                    mbar_arrive_expect_tx(sf, bytes);
+                    mbar_arrive_expect_tx(sf, bytes + tbytes);
                     bulk_load(smem_u32(sm.scales + sb * scale_buf_bytes),
                               p.scales + (static_cast<size_t>(t.x) * p.w_rows +
                                           static_cast<size_t>(mb) * kWeightTileRows) * p.kscale,
                               bytes, sf);
+                    if (tok)
+                        bulk_load(smem_u32(sm.tscales + sb * tscale_buf_bytes),
+                                  p.xs_mx + static_cast<size_t>(t.y) * p.xs_row_bytes, tbytes, sf);
                 }
                 ++local;
                 for (int st = un.st_lo; st < un.st_hi; ++st) {
@@ -457,7 +471,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     }
                     mbar_wait(smem_u32(sm.full + s), ph, nullptr);
                 }
-                if (WF == 1 && local > 0) {
+                if ((WF == 1 || WF == 3) && local > 0) {
                     const int sb = (local - 1) & 1;
                     mbar_wait(smem_u32(sm.sfull + sb), static_cast<uint32_t>((local - 1) >> 1) & 1u,
                               nullptr);
@@ -892,6 +906,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
         int stage = 0;
         uint32_t phase = 0;
+        int local = 0;
         bool ok = true;
         for (int u = cta0; u < num_units && ok; u += ncta) {
             const Unit un = unit_of(u, p, n_st);
@@ -899,9 +914,20 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             if (!tile_ok(t, p)) continue;
             const int wrow = un.mb * kWeightTileRows + quad * 32 + lane;
             const bool row_ok = wrow < p.w_rows;
+            // this unit's scale rows, staged in shared memory by the producer
+            // (one bulk copy per unit, double-buffered): a per-slot load from
+            // L2 kept the slot's MMAs waiting ~0.5 us for these warps
+            const int sb = local & 1;
+            const uint32_t sph = static_cast<uint32_t>(local >> 1) & 1u;
+            ++local;
+            if (!warp_wait(smem_u32(sm.sfull + sb), sph, flags)) {
+                if (lane == 0) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                ok = false;
+                break;
+            }
             // rows past the matrix are TMA zero-fill: scale 1 keeps them zero
-            const uint8_t* srow =
-                p.scales + (static_cast<size_t>(t.x) * p.w_rows + (row_ok ? wrow : 0)) * p.kscale;
+            const uint8_t* srow = sm.scales + sb * scale_buf_bytes + (quad * 32 + lane) * p.kscale;
+            const uint8_t* trow = sm.tscales + sb * tscale_buf_bytes;
             // the scale values of k-block kb (weight rows: two aligned halves,
             // as kscale = K / 32 and 2c are even; token rows, or 2^-3 for h)
             const auto load_vals = [&](int kb, uint32_t& va, uint32_t (&vb)[4]) {
@@ -909,18 +935,15 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 if (row_ok) {
                     const uint16_t* s16 =
                         reinterpret_cast<const uint16_t*>(srow + 2 * min(2 * kb, p.mx_cmax));
-                    va = static_cast<uint32_t>(__ldg(s16)) |
-                         (static_cast<uint32_t>(__ldg(s16 + 1)) << 16);
+                    va = static_cast<uint32_t>(s16[0]) | (static_cast<uint32_t>(s16[1]) << 16);
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int n = 32 * j + lane;
                     vb[j] = 0x7C7C7C7Cu;
                     if (p.xs_mx != nullptr)
-                        vb[j] = n < t.z ? __ldg(reinterpret_cast<const uint32_t*>(
-                                              p.xs_mx +
-                                              static_cast<size_t>(t.y + n) * p.xs_row_bytes +
-                                              4 * kb))
+                        vb[j] = n < t.z ? *reinterpret_cast<const uint32_t*>(
+                                              trow + n * p.xs_row_bytes + 4 * kb)
                                         : 0x7F7F7F7Fu;
                 }
             };
@@ -954,6 +977,11 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     phase ^= 1u;
                 }
             }
+            if (!ok) break;
+            // this unit's staged scales are consumed (their values are in
+            // TMEM): the producer may refill the buffer
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(sm.sempty + sb));
         }
     } else if (WF == 1) {
         // ------------------------------------------------ MXFP4 converters

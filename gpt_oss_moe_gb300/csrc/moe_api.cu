@@ -233,9 +233,14 @@ int auto_token_tile(const moe_shape& s) {
     long long t;
     if (tuned > 0) {
         t = tuned;
-    } else if (s.wfmt == MOE_W_MXFP4) {
+    } else if (s.wfmt == MOE_W_MXFP4 || s.wfmt == MOE_W_MXFP4_MXFP8) {
         const long long mean = (static_cast<long long>(s.T) * s.top_k + s.E - 1) / s.E;
         t = (2 * mean + 15) / 16 * 16;
+        // MXFP4 x MXFP8: at most 96 rows, so that the ring keeps three slots
+        // beside the staged scales; measured on gpt-oss-20b (layer, us):
+        // T=64 box 16/64: 104.2/117.4, T=512 box 96/128: 134.2/164.0,
+        // T=4096 box 96/128: 605.3/633.0
+        if (s.wfmt == MOE_W_MXFP4_MXFP8 && t > 96) t = 96;
     } else {
         t = (static_cast<long long>(s.T) + 15) / 16 * 16;
     }
@@ -485,7 +490,7 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
         if (n_iss == 2) astages &= ~1;
         if (astages < 2) return MOE_ERR_UNSUPPORTED;
     }
-    const size_t fixed = gemm_fixed_bytes(box, wf, kscale_max);
+    const size_t fixed = gemm_fixed_bytes(box, wf, kscale_max, mx ? mx_scale_row_bytes(s.H) : 0);
     int stages = budget < fixed ? 0 : static_cast<int>((budget - fixed) / stage_bytes);
     // MXFP4 converter teams need 2 x stages >= astages + 2
     if (stages < 2 || (mxfp4 && 2 * stages < astages + 2)) return MOE_ERR_UNSUPPORTED;
@@ -594,7 +599,7 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     g.kscale = s.H / 32;
     g.mx_cmax = s.H / 64 - 2;
     g.xs_mx = mx ? reinterpret_cast<const uint8_t*>(ws + L.x_scale) : nullptr;
-    g.xs_row_bytes = mx_padded_k(s.H) / 32;
+    g.xs_row_bytes = mx_scale_row_bytes(s.H);
     g.h_pad = mx_padded_k(s.I);
     g.h_tail0 = mx_tail0(s.I);
     // K split when the units cannot fill two waves (small batches)

@@ -107,6 +107,11 @@ __host__ __device__ inline int mx_padded_k(int K) { return (K + 127) / 128 * 128
 // down to 128 when K % 128 == 64, else K)
 __host__ __device__ inline int mx_tail0(int K) { return K % 128 ? K / 128 * 128 : K; }
 __host__ __device__ inline int mx_pos(int k, int tail0) { return k < tail0 ? k : k + 64; }
+// bytes of one token row's UE8M0 scales (mx_padded_k(K) / 32, padded to 16
+// so that a tile's rows are one 16-byte-aligned bulk copy)
+__host__ __device__ inline int mx_scale_row_bytes(int K) {
+    return (mx_padded_k(K) / 32 + 15) / 16 * 16;
+}
 
 struct WsLayout {
     size_t status, topk_ids, topk_w, blk_cnt, logits, partials, counters, offsets, gemm_partial;
@@ -144,7 +149,7 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
     L.x_perm = take(R * H * 2);            // bf16, or E4M3 codes (FP8)
     // FP8: fp32 scale of each routed row; MXFP4 x MXFP8: UE8M0 block scales
     // [T*k][mx_padded_k(H) / 32]
-    L.x_scale = take(R * (mx_padded_k(H) / 32 > 4 ? mx_padded_k(H) / 32 : 4));
+    L.x_scale = take(R * (mx_scale_row_bytes(H) > 4 ? mx_scale_row_bytes(H) : 4));
     L.h = take(R * I * 2);
     L.out_acc = take(static_cast<size_t>(T) * H * 4);
     // gate_up K-split partial tiles, fp32 [part][weight block][routed row][128].
@@ -294,8 +299,12 @@ inline size_t gemm_stage_bytes(int token_box, int wf) {
     // MXFP8: kMxKbPerStage of them (the codes padded to a byte each)
     return wf == 1 ? kMxfp4KbPerStage * (codes + b) : wf == 3 ? kMxKbPerStage * (a + b) : a + b;
 }
-inline size_t gemm_fixed_bytes(int token_box, int wf, int kscale) {
-    size_t scales = wf == 1 ? 2 * align_up(static_cast<size_t>(kWeightTileRows) * kscale, 16) : 0;
+inline size_t gemm_fixed_bytes(int token_box, int wf, int kscale, int xs_row_bytes = 0) {
+    // MXFP4 and MXFP4 x MXFP8: each unit's weight scale rows, double-buffered;
+    // MXFP4 x MXFP8 also the token tile's scale rows
+    size_t scales = (wf == 1 || wf == 3)
+                        ? 2 * align_up(static_cast<size_t>(kWeightTileRows) * kscale, 16) : 0;
+    if (wf == 3) scales += 2 * static_cast<size_t>(token_box) * xs_row_bytes;
     size_t meta = static_cast<size_t>(token_box) * 8;
     size_t bars = 768;
     return scales + meta + bars;

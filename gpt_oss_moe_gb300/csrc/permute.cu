@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
                 // in every lane (the batch's bounds are warp-uniform)
                 const int kp = mx_padded_k(p.H), tail0 = mx_tail0(p.H);
                 uint8_t* dst8 = reinterpret_cast<uint8_t*>(p.x_perm) + static_cast<size_t>(row) * kp;
-                uint8_t* dsts =
-                    reinterpret_cast<uint8_t*>(p.x_scale) + static_cast<size_t>(row) * (kp / 32);
+                uint8_t* dsts = reinterpret_cast<uint8_t*>(p.x_scale) +
+                                static_cast<size_t>(row) * mx_scale_row_bytes(p.H);
                 for (int v0 = 0; v0 < vec_per_row; v0 += 32 * kRowVecUnroll) {
                     uint4 buf[kRowVecUnroll];
 #pragma unroll
