@@ -59,9 +59,11 @@ extern "C" moe_status moe_forward_noalloc(const moe_shape* shape, const void* hi
                                           cudaStream_t stream) {
     if (!shape) return MOE_ERR_ARG;
     const size_t need = moe_workspace_bytes(shape);
-    if (need == 0) return shape->wfmt == MOE_W_BF16 || shape->wfmt == MOE_W_MXFP4
-                              ? MOE_ERR_SHAPE
-                              : MOE_ERR_ARG;
+    if (need == 0)
+        return shape->wfmt == MOE_W_BF16 || shape->wfmt == MOE_W_MXFP4 ||
+                       shape->wfmt == MOE_W_FP8 || shape->wfmt == MOE_W_MXFP4_MXFP8
+                   ? MOE_ERR_SHAPE
+                   : MOE_ERR_ARG;
     if (shape->T == 0) return MOE_OK;
     if (need > moe::kNoallocScratchBytes) return MOE_ERR_WORKSPACE;
     if (device_status_out && (reinterpret_cast<uintptr_t>(device_status_out) & 3u))

@@ -117,6 +117,20 @@ def test_forward_ep_rejects_bad_expert_ranges_on_the_host(moe):
                             1 << 30, None) == -1
 
 
+def test_noalloc_maps_bad_shapes_for_every_format(moe):
+    L = moe.lib()
+    for wfmt in (moe.MOE_W_BF16, moe.MOE_W_MXFP4, moe.MOE_W_FP8, moe.MOE_W_MXFP4_MXFP8):
+        bad = _shape(moe, H=100, wfmt=wfmt)
+        code = L.moe_forward_noalloc(ctypes.byref(bad), 16, 32, 48, moe.moe_weight(),
+                                     moe.moe_weight(), 64, 1, None, None, None, None)
+        assert code == -2, wfmt                                # MOE_ERR_SHAPE
+    # MXFP4 x MXFP8 needs H, I >= 128
+    assert moe.moe_workspace_bytes(_shape(moe, H=64, wfmt=moe.MOE_W_MXFP4_MXFP8)) == 0
+    bad = _shape(moe, wfmt=9)
+    assert L.moe_forward_noalloc(ctypes.byref(bad), 16, 32, 48, moe.moe_weight(),
+                                 moe.moe_weight(), 64, 1, None, None, None, None) == -1
+
+
 def test_ep_expert_ranges_partition_the_experts(moe):
     for E in (1, 7, 32, 128):
         for world in range(1, min(E, 9) + 1):
