@@ -458,11 +458,11 @@ def test_fp8_outliers_and_zero_rows(moe, oracle_lib, synth_lib):
 
 @pytest.fixture(scope="module")
 def layer_20b_fp8(synth_lib):
-    L = synth_lib.make_workload("20b_fp8", 512)
+    L = synth_lib.make_workload("20b_fp8", 4096)
     return L, to_device(L)
 
 
-@pytest.mark.parametrize("T", [1, 64, 512])
+@pytest.mark.parametrize("T", [1, 64, 512, 4096])
 def test_forward_20b_fp8(moe, oracle_lib, layer_20b_fp8, T):
     L, dev = layer_20b_fp8
     sample = None
@@ -474,11 +474,11 @@ def test_forward_20b_fp8(moe, oracle_lib, layer_20b_fp8, T):
 
 @pytest.fixture(scope="module")
 def layer_20b_mxfp4(synth_lib):
-    L = synth_lib.make_workload("20b_mxfp4", 512)
+    L = synth_lib.make_workload("20b_mxfp4", 4096)
     return L, to_device(L)
 
 
-@pytest.mark.parametrize("T", [1, 64, 512])
+@pytest.mark.parametrize("T", [1, 64, 512, 4096])
 def test_forward_20b_mxfp4(moe, oracle_lib, layer_20b_mxfp4, T):
     from parity_util import TOL_MXFP4
     L, dev = layer_20b_mxfp4
@@ -539,11 +539,11 @@ def test_mxfp8_outliers_and_zero_rows(moe, oracle_lib, synth_lib):
 
 @pytest.fixture(scope="module")
 def layer_20b_mxfp8(synth_lib):
-    L = synth_lib.make_workload("20b_mxfp4_mxfp8", 512)
+    L = synth_lib.make_workload("20b_mxfp4_mxfp8", 4096)
     return L, to_device(L)
 
 
-@pytest.mark.parametrize("T", [1, 64, 512])
+@pytest.mark.parametrize("T", [1, 64, 512, 4096])
 def test_forward_20b_mxfp4_mxfp8(moe, oracle_lib, layer_20b_mxfp8, T):
     L, dev = layer_20b_mxfp8
     sample = None
