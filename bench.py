@@ -221,21 +221,6 @@ def base_record(args, n_gpus, workload_desc, layer):
     }
 
 
-def cpu_oracle_rate(layer, budget_s, max_tokens=None):
-    """Oracle tokens/s on a bounded sample of the batch (first n tokens)."""
-    import oracle
-    oracle.build()
-    n = 1
-    max_tokens = max_tokens or layer.T
-    while True:
-        t0 = time.perf_counter()
-        oracle.forward(layer, tokens=list(range(n)))
-        dt = time.perf_counter() - t0
-        if dt >= budget_s / 3 or n >= max_tokens:
-            return n / dt, n, dt, oracle.max_threads()
-        n = min(max_tokens, n * 2)
-
-
 def run_reference(args, layer, desc):
     """CPU oracle arm: each step runs the oracle on one token of the batch."""
     import oracle
@@ -265,6 +250,191 @@ def run_reference(args, layer, desc):
     print(json.dumps(rec), flush=True)
 
 
+ALG_BYTES = {"bf16": (GU_BYTES, D_BYTES), "fp8": (GU_BYTES_FP8, D_BYTES_FP8),
+             "mxfp4": (GU_BYTES_MXFP4, D_BYTES_MXFP4),
+             "mxfp4_mxfp8": (GU_BYTES_MXFP4, D_BYTES_MXFP4)}
+
+
+def measure(moe, layer, args, dist, workload):
+    """Times K steps of one layer (inputs resident in HBM), then K more with
+    a CUDA event around every kernel; returns the measurement and the
+    routing and output of the last step."""
+    T, H, I, E, k = layer.T, layer.H, layer.I, layer.E, layer.top_k
+    dev = {}
+    for name in ("x", "wr", "br", "w_gu", "b_gu", "w_d", "b_d", "s_gu", "s_d"):
+        t = getattr(layer, name)
+        dev[name] = None if t is None else t.to("cuda", non_blocking=True)
+    torch.cuda.synchronize()
+    shape = moe.layer_shape(layer)
+    ws = moe.alloc_workspace(shape)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(x=None):
+        moe.moe_forward(shape, dev["x"] if x is None else x, dev["wr"], dev["br"],
+                        dev["w_gu"], dev["b_gu"], dev["w_d"], dev["b_d"], out,
+                        s_gu=dev["s_gu"], s_d=dev["s_d"], topk_ids_out=ids,
+                        workspace=ws, stream=stream)
+
+    clocks = ClockSampler(device_id_for_smi())
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = moe.moe_get_device_status(ws)
+    if status:
+        raise SystemExit(f"device status word {status:#x} after warm-up ({workload})")
+    U = int(torch.unique(ids).numel())
+
+    # Timed region 1: K steps, bracketed by CUDA events only (this gives
+    # `value`).  Timed region 2: K more steps with a CUDA event around every
+    # kernel (per-kernel durations for the roofline).  Events between kernels
+    # stop dependent launches from overlapping, so region 2 runs slightly
+    # slower; both step times are reported.
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    elapsed_ms = ev0.elapsed_time(ev1)
+
+    moe.moe_profile_enable(min(args.steps, 8192))
+    ev2 = torch.cuda.Event(enable_timing=True)
+    ev3 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev2.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev3.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    wall2 = time.time()
+    profiled_ms = ev2.elapsed_time(ev3)
+    kernels = moe.moe_profile_read()
+    moe.moe_profile_enable(0)
+    clocks.stop()
+    status = moe.moe_get_device_status(ws)
+    if status:
+        raise SystemExit(f"device status word {status:#x} after the timed region ({workload})")
+
+    max_ms = max_over_ranks(dist, elapsed_ms)
+    tokens_all = sum_over_ranks(dist, float(T * args.steps))
+
+    # Roofline of the dominant kernel (the gate_up GEMM: 2/3 of the bytes).
+    bw, tf_burst, tf_sust, peak_kind = peaks()
+    kmap = dict(kernels)
+    R = T * k
+    gu_b, d_b = (f(H, I) for f in ALG_BYTES[layer.wfmt])
+    # activation and h bytes per element: E4M3 codes for FP8 W8A8 and MXFP8
+    # (plus one scale byte per 32 for MXFP8 activations), else bf16
+    ab = 1 if layer.wfmt in ("fp8", "mxfp4_mxfp8") else 2
+    gu_alg = U * gu_b + R * H * ab + R * I * ab
+    if layer.wfmt == "mxfp4_mxfp8":
+        gu_alg += R * H // 32
+    tkind = "bf16"
+    if layer.wfmt in ("fp8", "mxfp4_mxfp8"):
+        # an E4M3 contraction's peak: the measured bf16 rate x the nominal
+        # dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+        tf_burst, tf_sust = 2.0 * tf_burst, 2.0 * tf_sust
+        peak_kind += ", x2 nominal fp8/bf16 ratio"
+        tkind = "e4m3"
+    gu_ms = kmap.get("gate_up_glu")
+    flops_tok = 2 * (2 * I) * H + 2 * H * I
+    gu_flops = R * 2 * (2 * I) * H
+    wl_key = f"{workload}_T{T}"
+    # bound: the kernel's algorithmic flops per byte against the ridge of
+    # its own tensor peak (bytes per weight differ between formats)
+    ridge = tf_burst * 1e12 / (bw * 1e9)
+    intensity = gu_flops / max(gu_alg, 1)
+    if intensity < ridge:
+        roof = {"bound": "hbm", "achieved": gu_alg / (gu_ms * 1e-3) / 1e9, "peak": bw,
+                "unit": "GB/s"}
+        peak_kind += ", HBM copy"
+    else:
+        # the step lasts about a millisecond, far from the seconds-long loop
+        # the sustained GEMM rate was measured on: the burst rate is the
+        # denominator, the sustained one a secondary figure
+        roof = {"bound": "tensor", "achieved": gu_flops / (gu_ms * 1e-3) / 1e12,
+                "peak": tf_burst, "unit": "TFLOP/s"}
+        roof["frac_of_sustained"] = roof["achieved"] / tf_sust
+        peak_kind += f", burst {tkind} GEMM rate"
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic("gate_up_glu", wl_key)
+    roof["kernel"] = "gate_up_glu (tcgen05 grouped GEMM + fused bias/GLU)"
+    roof["algorithmic_bytes_per_launch"] = gu_alg
+    roof["algorithmic_flops_per_launch"] = gu_flops
+    roof["peak_source"] = f"MEASURED_PEAKS.json ({peak_kind})"
+
+    layer_bytes = U * (gu_b + d_b) + E * H * 2 + E * 2 + T * H * (2 + 4)
+    layer_flops = T * (k * flops_tok + 2 * H * E)
+    step_s = max_ms / 1e3 / args.steps
+    m = {
+        "value": tokens_all / (max_ms / 1e3),
+        "ms_per_step": max_ms / args.steps,
+        "roofline": roof,
+        "layer": {"experts_touched": U, "bytes_per_step": layer_bytes,
+                  "flops_per_step": layer_flops,
+                  "hbm_gbs": layer_bytes / step_s / 1e9,
+                  "hbm_frac": layer_bytes / step_s / 1e9 / bw,
+                  "tflops": layer_flops / step_s / 1e12,
+                  "tensor_frac": layer_flops / step_s / 1e12 / tf_burst,
+                  "tensor_frac_of_sustained": layer_flops / step_s / 1e12 / tf_sust},
+        "kernels_ms": {n: round(v, 5) for n, v in kernels},
+        "kernel_timing": {"method": "CUDA events around every kernel, second timed region "
+                                    "of the same K steps",
+                          "ms_per_step_with_events": profiled_ms / args.steps},
+        "gpu_launches": len(kernels) * args.steps,
+        "clocks": clocks.summary(wall0, wall2),
+    }
+    return m, dev, step, out, ids
+
+
+def oracle_parity(layer, out, ids, n_tokens, threads=0):
+    """The oracle on the first n tokens (timed) and its agreement with the
+    GPU's last step on those tokens; near ties counted over all tokens."""
+    import oracle
+    oracle.build()
+    toks = list(range(n_tokens))
+    t0 = time.perf_counter()
+    o_ids, _, o_out = oracle.forward(layer, tokens=toks, threads=threads)
+    dt = time.perf_counter() - t0
+    logits = oracle.router_logits(layer)
+    srt = torch.sort(logits.double(), dim=1, descending=True).values
+    k = layer.top_k
+    near = (srt[:, k - 1] - srt[:, k]) < 1e-5 if k < layer.E else torch.zeros(layer.T, dtype=torch.bool)
+    keep = [t for t in toks if not near[t]]
+    g = out.cpu()[keep].double()
+    o = o_out[[toks.index(t) for t in keep]].double()
+    err = (g - o).abs().max().item() if keep else 0.0
+    ref = o.abs().max().item() if keep else 0.0
+    ids_equal = bool(torch.equal(ids.cpu()[keep], o_ids[[toks.index(t) for t in keep]]))
+    return dt, {"tokens_compared": len(keep), "near_ties": int(near.sum()),
+                "ids_bit_exact": ids_equal, "max_abs_err": err,
+                "max_abs_oracle": ref, "rel_err": err / ref if ref else 0.0}
+
+
+def cpu_oracle_rate(layer, budget_s, max_tokens=None, threads=0):
+    """Oracle tokens/s on a bounded sample of the batch (first n tokens)."""
+    import oracle
+    oracle.build()
+    n = 1
+    max_tokens = max_tokens or layer.T
+    while True:
+        t0 = time.perf_counter()
+        oracle.forward(layer, tokens=list(range(n)), threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 3 or n >= max_tokens:
+            return n / dt, n, dt, (threads or oracle.max_threads())
+        n = min(max_tokens, n * 2)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -273,6 +443,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="20b_decode")
     ap.add_argument("--T", type=int, default=64)
+    ap.add_argument("--prefill-workload", default="20b_prefill_skewed",
+                    help="second workload timed in the same run ('none' to skip)")
+    ap.add_argument("--prefill-T", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -299,145 +472,11 @@ def main():
     moe.lib()
 
     layer = synth.make_workload(args.workload, args.T, pin=True)
-    dev = {}
-    for name in ("x", "wr", "br", "w_gu", "b_gu", "w_d", "b_d", "s_gu", "s_d"):
-        t = getattr(layer, name)
-        dev[name] = None if t is None else t.to("cuda", non_blocking=True)
-    torch.cuda.synchronize()
-    T, H, I, E, k = layer.T, layer.H, layer.I, layer.E, layer.top_k
-    shape = moe.layer_shape(layer)
-    ws = moe.alloc_workspace(shape)
-    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
-    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
-    stream = torch.cuda.current_stream()
-
-    def step(x=None):
-        moe.moe_forward(shape, dev["x"] if x is None else x, dev["wr"], dev["br"],
-                        dev["w_gu"], dev["b_gu"], dev["w_d"], dev["b_d"], out,
-                        s_gu=dev["s_gu"], s_d=dev["s_d"], topk_ids_out=ids,
-                        workspace=ws, stream=stream)
-
-    clocks = ClockSampler(device_id_for_smi())
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    status = moe.moe_get_device_status(ws)
-    if status:
-        raise SystemExit(f"device status word {status:#x} after warm-up")
-    U = int(torch.unique(ids).numel())
-
-    # Timed region 1: K steps, bracketed by CUDA events only (this gives
-    # `value`).  Timed region 2: K more steps with a CUDA event around every
-    # kernel (per-kernel durations for the roofline).  Events between kernels
-    # stop dependent launches from overlapping, so region 2 runs slightly
-    # slower; both step times are reported.
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize()
-    wall0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    wall1 = time.time()
-    elapsed_ms = ev0.elapsed_time(ev1)
-
-    moe.moe_profile_enable(min(args.steps, 8192))
-    ev2 = torch.cuda.Event(enable_timing=True)
-    ev3 = torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize()
-    ev2.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev3.record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    wall2 = time.time()
-    profiled_ms = ev2.elapsed_time(ev3)
-    kernels = moe.moe_profile_read()
-    moe.moe_profile_enable(0)
-    clocks.stop()
-    status = moe.moe_get_device_status(ws)
-    if status:
-        raise SystemExit(f"device status word {status:#x} after the timed region")
-
-    max_ms = max_over_ranks(dist, elapsed_ms)
-    tokens_all = sum_over_ranks(dist, float(T * args.steps))
-    value = tokens_all / (max_ms / 1e3)
-
-    # Roofline of the dominant kernel (the gate_up GEMM: 2/3 of the bytes).
-    bw, tf_burst, tf_sust, peak_kind = peaks()
-    kmap = dict(kernels)
-    R = T * k
-    if layer.wfmt == "bf16":
-        gu_b, d_b = GU_BYTES(H, I), D_BYTES(H, I)
-    elif layer.wfmt == "fp8":
-        gu_b, d_b = GU_BYTES_FP8(H, I), D_BYTES_FP8(H, I)
-    else:
-        gu_b, d_b = GU_BYTES_MXFP4(H, I), D_BYTES_MXFP4(H, I)
-    # activation and h bytes per element: E4M3 codes for FP8 W8A8 and MXFP8
-    # (plus one scale byte per 32 for MXFP8 activations), else bf16
-    ab = 1 if layer.wfmt in ("fp8", "mxfp4_mxfp8") else 2
-    gu_alg = U * gu_b + R * H * ab + R * I * ab
-    if layer.wfmt == "mxfp4_mxfp8":
-        gu_alg += R * H // 32
-    if layer.wfmt in ("fp8", "mxfp4_mxfp8"):
-        # an E4M3 contraction's peak: the measured bf16 rate x the nominal
-        # dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
-        tf_burst, tf_sust = 2.0 * tf_burst, 2.0 * tf_sust
-        peak_kind += ", x2 nominal fp8/bf16 ratio"
-    gu_ms = kmap.get("gate_up_glu")
-    flops_tok = 2 * (2 * I) * H + 2 * H * I
-    gu_flops = R * 2 * (2 * I) * H
-    wl_key = f"{args.workload}_T{T}"
-    # bound: the kernel's algorithmic flops per byte against the ridge of
-    # its own tensor peak (bytes per weight differ between formats)
-    ridge = tf_burst * 1e12 / (bw * 1e9)
-    intensity = gu_flops / max(gu_alg, 1)
-    if intensity < ridge:
-        roof = {"bound": "hbm", "achieved": gu_alg / (gu_ms * 1e-3) / 1e9, "peak": bw,
-                "unit": "GB/s"}
-    else:
-        # a kernel timed inside a long run of steps runs under the power
-        # cap: its peak is the sustained GEMM rate, a short run's the burst
-        long_run = elapsed_ms >= 100.0
-        roof = {"bound": "tensor", "achieved": gu_flops / (gu_ms * 1e-3) / 1e12,
-                "peak": tf_sust if long_run else tf_burst, "unit": "TFLOP/s"}
-        roof["frac_of_burst"] = roof["achieved"] / tf_burst
-        peak_kind += ", sustained bf16 GEMM rate" if long_run else ", burst bf16 GEMM rate"
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic("gate_up_glu", wl_key)
-    roof["kernel"] = "gate_up_glu (tcgen05 grouped GEMM + fused bias/GLU)"
-    roof["algorithmic_bytes_per_launch"] = gu_alg
-    roof["peak_source"] = f"MEASURED_PEAKS.json ({peak_kind})"
-
-    layer_bytes = U * (gu_b + d_b) + E * H * 2 + E * 2 + T * H * (2 + 4)
-    layer_flops = T * (k * flops_tok + 2 * H * E)
-    step_s = elapsed_ms / 1e3 / args.steps
+    m, dev, step, out, ids = measure(moe, layer, args, dist, args.workload)
+    T, H = layer.T, layer.H
 
     rec = base_record(args, world, desc, layer)
-    rec.update({
-        "value": value,
-        "ms_per_step": max_ms / args.steps,
-        "roofline": roof,
-        "layer": {"experts_touched": U, "bytes_per_step": layer_bytes,
-                  "hbm_gbs": layer_bytes / step_s / 1e9,
-                  "hbm_frac": layer_bytes / step_s / 1e9 / bw,
-                  "tflops": layer_flops / step_s / 1e12,
-                  "tensor_frac": layer_flops / step_s / 1e12 /
-                                 (tf_sust if elapsed_ms >= 100.0 else tf_burst),
-                  "tensor_frac_of_burst": layer_flops / step_s / 1e12 / tf_burst},
-        "kernels_ms": {n: round(v, 5) for n, v in kernels},
-        "kernel_timing": {"method": "CUDA events around every kernel, second timed region "
-                                    "of the same K steps",
-                          "ms_per_step_with_events": profiled_ms / args.steps},
-        "gpu_launches": len(kernels) * args.steps,
-        "clocks": clocks.summary(wall0, wall2),
-    })
+    rec.update(m)
 
     # End to end through the public API with host buffers.
     if not args.no_e2e:
@@ -462,13 +501,42 @@ def main():
                       "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                       "d2h_bytes_per_step": T * H * 4, "steps": n_e2e,
                       "timing": "host wall clock, synchronised on both sides"}
+    # the last step's routing and output, for the parity figures below
+    step()
+    torch.cuda.synchronize()
+    out_last, ids_last = out.clone(), ids.clone()
+    del dev
+
+    # The prefill half of the metric: the same measurement on the prefill
+    # workload, in the same process.
+    if args.prefill_workload != "none":
+        pl = synth.make_workload(args.prefill_workload, args.prefill_T, pin=True)
+        pm, pdev, _, pout, pids = measure(moe, pl, args, dist, args.prefill_workload)
+        pm["workload"] = DESCRIPTIONS.get(args.prefill_workload,
+                                          args.prefill_workload).format(T=pl.T)
+        pm["T"] = pl.T
+        rec["prefill"] = pm
+        rec["gpu_launches"] += pm["gpu_launches"]
+        prefill_out, prefill_ids = pout.cpu(), pids.cpu()
+        del pdev
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, dt, cores = cpu_oracle_rate(layer, args.cpu_budget)
+        # one thread on a small sample (a few seconds at most)
+        rate1, n1, dt1, _ = cpu_oracle_rate(layer, min(3.0, args.cpu_budget / 4),
+                                            max_tokens=8, threads=1)
         rec["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores,
-                               "kind": "oracle",
+                               "nproc": os.cpu_count(), "kind": "oracle",
                                "sample": f"first {n} of the {T} tokens, one oracle call "
-                                         f"({dt:.1f} s)"}
+                                         f"({dt:.1f} s)",
+                               "one_thread": {"value": rate1, "unit": "tokens/s",
+                                              "sample": f"first {n1} tokens ({dt1:.1f} s)"}}
+        # parity of the timed runs: the headline batch in full, the prefill
+        # batch on its first 64 tokens (near ties counted over all tokens)
+        _, rec["parity"] = oracle_parity(layer, out_last, ids_last, T)
+        if "prefill" in rec:
+            _, rec["prefill"]["parity"] = oracle_parity(pl, prefill_out, prefill_ids,
+                                                        min(64, pl.T))
     if rank == 0:
         print(json.dumps(rec), flush=True)
     if dist is not None:

@@ -19,15 +19,18 @@ from typing import Optional
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libgpt_oss_moe.so")
+# GPT_OSS_MOE_LIB selects another build of the same library (the
+# MOE_DEBUG_BOUNDS variant, libgpt_oss_moe_debug_bounds.so)
+LIB_PATH = os.environ.get("GPT_OSS_MOE_LIB") or os.path.join(_PKG, "libgpt_oss_moe.so")
 
 MOE_W_BF16, MOE_W_MXFP4, MOE_W_FP8, MOE_W_MXFP4_MXFP8 = 0, 1, 2, 3
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_BAD_TILE = 0x1, 0x2, 0x4
+MOE_DEV_NONFINITE, MOE_DEV_BOUNDS = 0x8, 0x10
 
 # Every function the C header declares, in order (checked by the tests).
 EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_ep",
            "moe_forward_noalloc", "moe_get_device_status",
-           "moe_clear_device_status",
+           "moe_clear_device_status", "moe_stage_stats", "moe_trace_read",
            "moe_set_tuning", "moe_profile_enable", "moe_profile_read",
            "moe_status_str", "moe_attention_sinks", "moe_attention_workspace_bytes")
 
@@ -92,6 +95,12 @@ def lib():
             L.moe_get_device_status.restype = i
             L.moe_clear_device_status.argtypes = [vp, vp]
             L.moe_clear_device_status.restype = i
+            L.moe_stage_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_float)]
+            L.moe_stage_stats.restype = i
+            L.moe_trace_read.argtypes = [ctypes.POINTER(ctypes.c_uint64), sz,
+                                         ctypes.POINTER(sz)]
+            L.moe_trace_read.restype = i
             L.moe_set_tuning.argtypes = [ctypes.c_char_p, i]
             L.moe_set_tuning.restype = i
             L.moe_profile_enable.argtypes = [i]
@@ -263,6 +272,28 @@ def moe_get_device_status(workspace: torch.Tensor) -> int:
     if code not in (0, -7):
         _check(code, "moe_get_device_status")
     return v.value
+
+
+def moe_stage_stats(workspace: torch.Tensor):
+    """Synchronising read of the stage checks (MOE_CHECK_STAGES=1):
+    [(non-finite count, largest finite magnitude)] for the gathered
+    activations, h and the output of the last checked call."""
+    nf = (ctypes.c_int32 * 3)()
+    mx = (ctypes.c_float * 3)()
+    _check(lib().moe_stage_stats(_p(workspace), nf, mx), "moe_stage_stats")
+    return [(int(nf[i]), float(mx[i])) for i in range(3)]
+
+
+def moe_trace_read():
+    """Phase timestamps of the last call (trace build only): a dict of
+    int64 tensors router [512, 8], permute [512, 8], gemm [2, 512, 8]."""
+    cap = 4 * 512 * 8
+    buf = (ctypes.c_uint64 * cap)()
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_trace_read(buf, cap, ctypes.byref(n)), "moe_trace_read")
+    t = torch.tensor(list(buf[:n.value]), dtype=torch.int64)
+    return {"router": t[:4096].view(512, 8), "permute": t[4096:8192].view(512, 8),
+            "gemm": t[8192:].view(2, 512, 8)}
 
 
 def moe_clear_device_status(workspace: torch.Tensor, stream=None):

@@ -40,17 +40,31 @@ def _deps_mtime():
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+# Build variants: name -> (library, object folder, extra nvcc flags).
+# "debug_bounds" checks the index of every store of the layer's kernels and
+# skips (and reports, MOE_DEV_BOUNDS) one that falls outside its buffer.
+VARIANTS = {
+    "": (LIB, BUILD, []),
+    "debug_bounds": (os.path.join(PKG, "libgpt_oss_moe_debug_bounds.so"),
+                     os.path.join(BUILD, "debug_bounds"), ["-DMOE_DEBUG_BOUNDS"]),
+    # "trace" records per-CTA phase timestamps (moe_trace_read)
+    "trace": (os.path.join(PKG, "libgpt_oss_moe_trace.so"),
+              os.path.join(BUILD, "trace"), ["-DMOE_TRACE"]),
+}
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
     """Compile and link; returns the library path.  Rebuilds when a source,
     a header or this script is newer than the library."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    lib, build_dir, vflags = VARIANTS[variant]
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    flags = _flags() + list(extra_flags)
+    flags = _flags() + vflags + list(extra_flags)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -62,13 +76,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lrt", "-ldl", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

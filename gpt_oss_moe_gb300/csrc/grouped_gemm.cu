@@ -59,12 +59,17 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "trace.cuh"
 #include "../../include/moe.h"
 
 namespace moe {
 namespace {
 
-constexpr int kEpiThreads = 128;
+// gate_up (kernel 0) and down (kernel 1): 0 entry, 1 set-up done, 2 weight
+// loads issued before the wait, 3 producer past the wait, 4 first MMA slot
+// full, 5 last MMA commit, 6 epilogue done, 7 exit
+MOE_TRACE_ARRAY(g_trace_gemm, 2);
+
 constexpr int kConvThreads = 256;   // per team: two threads per weight row (half a row each)
 constexpr int kConvTeams = 2;
 constexpr uint32_t kATileBytes = kWeightTileRows * kBlockK * 2;      // 16 KB bf16
@@ -83,9 +88,16 @@ constexpr int kBarBytes = 768;
 constexpr uint32_t kMxCodeTxBytes = kWeightTileRows * 64;
 constexpr int kMxScaleWarps = 4;        // MXFP4 x MXFP8: warps 6..9 write the scales
 
+// Epilogue warps (from warp 2): bf16 and FP8 kernels run two warps per TMEM
+// lane quadrant, each taking alternate 16-column chunks of the accumulator,
+// so that a prefill unit's epilogue (GLU, or the output reductions) ends
+// within the next unit's main loop; the MXFP4 kernels keep one per quadrant
+// (their other warps convert or write scales).
+template <int WF>
+constexpr int kEpiWarps = (WF == 0 || WF == 2) ? 8 : 4;
 template <int WF>
 constexpr int kThreadsOf = WF == 1 ? 192 + kConvTeams * kConvThreads + 32
-                         : WF == 3 ? 192 + kMxScaleWarps * 32 : 192;
+                         : WF == 3 ? 192 + kMxScaleWarps * 32 : 64 + kEpiWarps<WF> * 32;
 constexpr int kSecondIssuerWarp = 6 + kConvTeams * kConvThreads / 32;    // MXFP4: warp 22
 
 struct SmemPlan {
@@ -310,6 +322,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         static_cast<uint32_t>((kWeightTileRows * p.kscale + 15) / 16 * 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -324,7 +337,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(sm.tfull + b), static_cast<uint32_t>(n_iss));
             // pair: one arrival from each CTA's epilogue, on the even CTA's
-            mbar_init(smem_u32(sm.tempty + b), kPair ? 2u : static_cast<uint32_t>(kEpiThreads));
+            mbar_init(smem_u32(sm.tempty + b),
+                      kPair ? 2u : static_cast<uint32_t>(kEpiWarps<WF> * 32));
             mbar_init(smem_u32(sm.sfull + b), 1);
             mbar_init(smem_u32(sm.sempty + b), WF == 3 ? kMxScaleWarps : kConvTeams * kConvThreads);
         }
@@ -351,11 +365,24 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     if (kPair) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_base;
+    if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 1);
 
-    pdl_wait();                 // tiles, activations and outputs of earlier kernels
-    pdl_launch_dependents();
+    // The GEMM token tiles were written by the router, which has completed
+    // before this kernel starts: the launch order is router -> permutation
+    // -> gate_up -> down, and each of those kernels lets its successor start
+    // only after its own griddepcontrol.wait has returned, i.e. after its
+    // predecessor completed.  The token operand (gathered activations, or h)
+    // is written by the kernel launched just before this one and is read
+    // only after griddepcontrol.wait.  The producer therefore streams the
+    // first ring slots' weight tiles (and weight scales) before that wait,
+    // overlapping the previous kernel; every other role waits first.
+    if (warp != 0) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
-    const int num_units = p.num_tiles[0] * p.n_wblocks * p.ksplit;
+    // (read at L2: the producer reads it before griddepcontrol.wait)
+    const int num_units = __ldcg(p.num_tiles) * p.n_wblocks * p.ksplit;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -363,6 +390,111 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             const uint32_t w_bytes = WF == 1 ? kCodeStageBytes : WF == 3 ? kMxCodeTxBytes : kATileBytes;
+            // Loads of one ring slot: the weight part (`wpart`) and/or the
+            // token part; the slot's full barrier expects both.
+            const auto slot_loads = [&](const Unit& un, const int4& t, int st, int stage,
+                                        bool wpart, bool tpart, bool expect) {
+                const uint32_t fb = smem_u32(sm.full + stage);
+                const int mb = un.mb;
+                // full boxes are counted, zero-filled past K included;
+                // pair: the even CTA's barrier counts both CTAs' bytes
+                // MXFP4 x MXFP8: nk k-blocks (the K range's last slot may
+                // hold one), 8 KB of codes + the token tile each
+                const int nk = min(KPS, p.k_blocks - st * KPS);
+                if (expect && rank == 0)
+                    mbar_arrive_expect_tx(
+                        fb, WF == 3 ? static_cast<uint32_t>(nk) * (kMxCodeTxBytes + b_bytes)
+                                    : (kPair ? 2u : 1u) * (w_bytes + b_stage_bytes));
+                const uint32_t b_dst = smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
+                if (WF == 1) {
+                    // codes of k-blocks 4st..4st+3 (128 B per row), and the
+                    // token rows' K chunks 4st..4st+3 (chunk-major operand)
+                    if (wpart)
+                        tma_load_3d(smem_u32(sm.codes + static_cast<size_t>(stage) * kCodeStageBytes),
+                                    &tmap_w, fb, st * KPS * (kBlockK / 2), mb * kWeightTileRows, t.x,
+                                    pol_w);
+                    if (tpart) tma_load_3d(b_dst, &tmap_x, fb, 0, t.y, st * KPS, pol_x);
+                } else if (WF == 3) {
+                    // E2M1 codes of K 64c..64c+127 (c = 2 st, or the last
+                    // chunk starting 64 early), padded by TMA to 128 B rows
+                    for (int jj = 0; jj < nk; ++jj) {
+                        const int kb = st * KPS + jj;
+                        if (wpart)
+                            tma_load_4d(smem_u32(sm.a + (static_cast<size_t>(stage) * KPS + jj) *
+                                                            kATileBytes),
+                                        &tmap_w, fb, 0, min(2 * kb, p.mx_cmax),
+                                        mb * kWeightTileRows, t.x, pol_w);
+                        if (tpart)
+                            tma_load_2d(b_dst + static_cast<uint32_t>(jj) * b_bytes, &tmap_x, fb,
+                                        kb * kKB, t.y, pol_x);
+                    }
+                } else if (kPair) {
+                    // rows 128 * rank.. of the 256-row block; token rows
+                    // n/2 * rank.. of the tile (each CTA holds N/2 of B)
+                    const uint32_t fb0 = mapa_shared(fb, 0);
+                    const int half_n = ((t.z + 15) & ~15) / 2;
+                    if (wpart)
+                        tma_load_3d_pair(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
+                                         &tmap_w, fb0, st * kKB,
+                                         mb * kUnitRows + static_cast<int>(rank) * kWeightTileRows,
+                                         t.x, pol_w);
+                    if (tpart)
+                        tma_load_2d_pair(b_dst, &tmap_x, fb0, st * kKB,
+                                         t.y + static_cast<int>(rank) * half_n, pol_x);
+                } else {
+                    if (wpart)
+                        tma_load_3d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
+                                    &tmap_w, fb, st * kKB, mb * kWeightTileRows, t.x, pol_w);
+                    if (tpart) tma_load_2d(b_dst, &tmap_x, fb, st * kKB, t.y, pol_x);
+                }
+            };
+            // A unit's scale rows (MXFP4 and MXFP4 x MXFP8), one bulk copy
+            // into buffer sb: the weight scales and/or (MXFP4 x MXFP8) the
+            // token tile's scales, written by the previous kernel.
+            const auto scale_loads = [&](const Unit& un, const int4& t, int sb, bool wpart,
+                                         bool tpart, bool expect) {
+                const int rows = min(kWeightTileRows, p.w_rows - un.mb * kWeightTileRows);
+                const uint32_t bytes = static_cast<uint32_t>(rows * p.kscale);
+                const bool tok = WF == 3 && p.xs_mx != nullptr;
+                const uint32_t tbytes = tok ? static_cast<uint32_t>(t.z * p.xs_row_bytes) : 0u;
+                const uint32_t sf = smem_u32(sm.sfull + sb);
+                if (expect) mbar_arrive_expect_tx(sf, bytes + tbytes);
+                if (wpart)
+                    bulk_load(smem_u32(sm.scales + sb * scale_buf_bytes),
+                              p.scales + (static_cast<size_t>(t.x) * p.w_rows +
+                                          static_cast<size_t>(un.mb) * kWeightTileRows) * p.kscale,
+                              bytes, sf);
+                if (tok && tpart)
+                    bulk_load(smem_u32(sm.tscales + sb * tscale_buf_bytes),
+                              p.xs_mx + static_cast<size_t>(t.y) * p.xs_row_bytes, tbytes, sf);
+            };
+
+            // Before the wait: the weight parts of the first ring slots (at
+            // most one ring), and the first two units' weight scales.
+            int npre = 0, npre_units = 0;
+            {
+                int stage = 0, local = 0;
+                for (int u = cta0; u < num_units && npre < stages; u += ncta) {
+                    const Unit un = unit_of(u, p, n_st);
+                    const int4 t = __ldcg(p.tiles + un.tile);
+                    if (!tile_ok(t, p)) continue;
+                    if (WF == 1 || WF == 3) {
+                        if (local == 2) break;              // both scale buffers taken
+                        scale_loads(un, t, local & 1, true, false, true);
+                        npre_units = ++local;
+                    }
+                    for (int st = un.st_lo; st < un.st_hi && npre < stages; ++st) {
+                        slot_loads(un, t, st, stage, true, false, true);
+                        ++npre;
+                        ++stage;
+                    }
+                }
+            }
+            MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 2);
+            pdl_wait();
+            pdl_launch_dependents();
+            MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 3);
+
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -372,83 +504,34 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const Unit un = unit_of(u, p, n_st);
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
-                const int mb = un.mb;
                 if (WF == 1 || WF == 3) {
                     // this unit's scale rows, one bulk copy, double-buffered
                     // (MXFP4 x MXFP8: and the token tile's scale rows)
                     const int sb = local & 1;
                     const uint32_t sph = static_cast<uint32_t>(local >> 1) & 1u;
-                    if (!mbar_wait(smem_u32(sm.sempty + sb), sph ^ 1u, flags)) {
-                        raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
-                        ok = false;
-                        break;
+                    if (local < npre_units) {
+                        scale_loads(un, t, sb, false, true, false);
+                    } else {
+                        if (!mbar_wait(smem_u32(sm.sempty + sb), sph ^ 1u, flags)) {
+                            raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                        scale_loads(un, t, sb, true, true, true);
                     }
-                    const int rows = min(kWeightTileRows, p.w_rows - mb * kWeightTileRows);
-                    const uint32_t bytes = static_cast<uint32_t>(rows * p.kscale);
-                    const bool tok = WF == 3 && p.xs_mx != nullptr;
-                    const uint32_t tbytes = tok ? static_cast<uint32_t>(t.z * p.xs_row_bytes) : 0u;
-                    const uint32_t sf = smem_u32(sm.sfull + sb);
-                    mbar_arrive_expect_tx(sf, bytes + tbytes);
-                    bulk_load(smem_u32(sm.scales + sb * scale_buf_bytes),
-                              p.scales + (static_cast<size_t>(t.x) * p.w_rows +
-                                          static_cast<size_t>(mb) * kWeightTileRows) * p.kscale,
-                              bytes, sf);
-                    if (tok)
-                        bulk_load(smem_u32(sm.tscales + sb * tscale_buf_bytes),
-                                  p.xs_mx + static_cast<size_t>(t.y) * p.xs_row_bytes, tbytes, sf);
                 }
                 ++local;
                 for (int st = un.st_lo; st < un.st_hi; ++st) {
-                    if (!mbar_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
-                        raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = smem_u32(sm.full + stage);
-                    // full boxes are counted, zero-filled past K included;
-                    // pair: the even CTA's barrier counts both CTAs' bytes
-                    // MXFP4 x MXFP8: nk k-blocks (the K range's last slot may
-                    // hold one), 8 KB of codes + the token tile each
-                    const int nk = min(KPS, p.k_blocks - st * KPS);
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(
-                            fb, WF == 3 ? static_cast<uint32_t>(nk) * (kMxCodeTxBytes + b_bytes)
-                                        : (kPair ? 2u : 1u) * (w_bytes + b_stage_bytes));
-                    const uint32_t b_dst = smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
-                    if (WF == 1) {
-                        // codes of k-blocks 4st..4st+3 (128 B per row), and the
-                        // token rows' K chunks 4st..4st+3 (chunk-major operand)
-                        tma_load_3d(smem_u32(sm.codes + static_cast<size_t>(stage) * kCodeStageBytes),
-                                    &tmap_w, fb, st * KPS * (kBlockK / 2), mb * kWeightTileRows, t.x,
-                                    pol_w);
-                        tma_load_3d(b_dst, &tmap_x, fb, 0, t.y, st * KPS, pol_x);
-                    } else if (WF == 3) {
-                        // E2M1 codes of K 64c..64c+127 (c = 2 st, or the last
-                        // chunk starting 64 early), padded by TMA to 128 B rows
-                        for (int jj = 0; jj < nk; ++jj) {
-                            const int kb = st * KPS + jj;
-                            tma_load_4d(smem_u32(sm.a + (static_cast<size_t>(stage) * KPS + jj) *
-                                                            kATileBytes),
-                                        &tmap_w, fb, 0, min(2 * kb, p.mx_cmax),
-                                        mb * kWeightTileRows, t.x, pol_w);
-                            tma_load_2d(b_dst + static_cast<uint32_t>(jj) * b_bytes, &tmap_x, fb,
-                                        kb * kKB, t.y, pol_x);
-                        }
-                    } else if (kPair) {
-                        // rows 128 * rank.. of the 256-row block; token rows
-                        // n/2 * rank.. of the tile (each CTA holds N/2 of B)
-                        const uint32_t fb0 = mapa_shared(fb, 0);
-                        const int half_n = ((t.z + 15) & ~15) / 2;
-                        tma_load_3d_pair(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
-                                         &tmap_w, fb0, st * kKB,
-                                         mb * kUnitRows + static_cast<int>(rank) * kWeightTileRows,
-                                         t.x, pol_w);
-                        tma_load_2d_pair(b_dst, &tmap_x, fb0, st * kKB,
-                                         t.y + static_cast<int>(rank) * half_n, pol_x);
+                    if (issued < npre) {
+                        // weight part already in flight: the token part only
+                        slot_loads(un, t, st, stage, false, true, false);
                     } else {
-                        tma_load_3d(smem_u32(sm.a + static_cast<size_t>(stage) * kATileBytes),
-                                    &tmap_w, fb, st * kKB, mb * kWeightTileRows, t.x, pol_w);
-                        tma_load_2d(b_dst, &tmap_x, fb, st * kKB, t.y, pol_x);
+                        if (!mbar_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
+                            raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                        slot_loads(un, t, st, stage, true, true, true);
                     }
                     ++issued;
                     if (++stage == stages) {
@@ -477,6 +560,9 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                               nullptr);
                 }
             }
+        } else {
+            pdl_wait();
+            pdl_launch_dependents();
         }
     } else if (WF != 1 && warp == 1) {
         // ------------------------------------------------ MMA issuer (bf16)
@@ -491,6 +577,12 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             uint32_t phase = 0;
             int local = 0;
             bool ok = true;
+            // test fault: a wait on a barrier that nothing arrives on (the
+            // second drain barrier, unused by this issuer) runs out
+            if (!kPair && p.inject_stall && !warp_wait(smem_u32(sm.drain + 1), 0, flags)) {
+                if (leader) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                ok = false;
+            }
             for (int u = cta0; u < num_units && ok; u += ncta) {
                 const Unit un = unit_of(u, p, n_st);
                 const int4 t = p.tiles[un.tile];
@@ -515,6 +607,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                         ok = false;
                         break;
                     }
+                    if (local == 1 && st == un.st_lo && lane == 0)
+                        MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 4);
                     tc_fence_after();
                     // K steps of 16: +32 bytes along the swizzled rows, +2 in
                     // the descriptors' start-address field (address >> 4)
@@ -580,6 +674,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             }
             // Every MMA issued so far has finished once this arrives.
             if (leader) {
+                MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 5);
                 if constexpr (kPair)
                     tc_commit_pair(smem_u32(sm.drain));
                 else
@@ -677,10 +772,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             }
             __syncwarp();
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + kEpiWarps<WF>) {
         // ------------------------------------------------ epilogue
-        const int ep = threadIdx.x - 64;          // 0..127
+        constexpr int kEpiThreads = kEpiWarps<WF> * 32;
+        constexpr int kHalves = kEpiWarps<WF> / 4;     // warps per lane quadrant
+        const int ep = threadIdx.x - 64;          // 0 .. kEpiThreads-1
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
+        const int half = (warp - 2) >> 2;         // this warp's share of the columns
         const int row_in_tile = quad * 32 + lane;
         int local = 0;
         int sbase = 0;                            // ring use of the unit's first slot
@@ -699,9 +797,14 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             if (EPI == kEpiCombine) {
                 named_bar_sync(1, kEpiThreads);   // previous unit done with meta
                 for (int c = ep; c < t.z; c += kEpiThreads) {
+                    // a row the permutation could not fill (a bad expert id,
+                    // inconsistent counts) holds a stale entry: never let it
+                    // address memory outside this call's buffers
                     const int a = p.sorted_assign[t.y + c];
-                    sm.meta_tok[c] = a / p.top_k;
-                    sm.meta_w[c] = p.topk_w[a];
+                    const bool a_ok = a >= 0 && a < p.rows_total;
+                    if (!a_ok) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
+                    sm.meta_tok[c] = a_ok ? a / p.top_k : -1;
+                    sm.meta_w[c] = a_ok ? p.topk_w[a] : 0.f;
                 }
             } else if (WF == 2) {
                 // FP8 gate_up: the activation scale of each routed row
@@ -793,7 +896,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     const int c = c0 + i + (odd ? 8 : 0);
                     // rows past 2I exist only in the last 256-row block of
                     // CTA pairs (gate and up rows share their validity)
-                    if (c < t.z && row_ok) {
+                    if (c < t.z && row_ok &&
+                        MOE_BOUNDS(t.y + c < p.rows_total && hcol < hcols, p.status)) {
                         if (WF >= 2) {
                             uint8_t* dst = h8row0 + static_cast<size_t>(c) * h8stride;
                             *dst = static_cast<uint8_t>(
@@ -816,12 +920,15 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const size_t unit_off =
                     (static_cast<size_t>(mb) * p.rows_total + t.y) * kWeightTileRows + row_in_tile;
                 float* mine = p.partial + un.split * part_floats + unit_off;
-                for (int c0 = 0; c0 < n_mma; c0 += 16) {
+                for (int c0 = 16 * half; c0 < n_mma; c0 += 16 * kHalves) {
                     float v[16];
                     load_acc(c0, v);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (c0 + i < t.z) mine[static_cast<size_t>(c0 + i) * kWeightTileRows] = v[i];
+                        if (c0 + i < t.z &&
+                            MOE_BOUNDS(un.split < p.ksplit && mb < p.n_wblocks &&
+                                           t.y + c0 + i < p.rows_total, p.status))
+                            mine[static_cast<size_t>(c0 + i) * kWeightTileRows] = v[i];
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(sm.tempty + buf));
@@ -837,7 +944,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 if (!flags[3]) continue;
                 __threadfence();
                 const float* parts = p.partial + unit_off;
-                for (int c0 = 0; c0 < n_mma; c0 += 16) {
+                for (int c0 = 16 * half; c0 < n_mma; c0 += 16 * kHalves) {
                     float v[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = 0.f;
@@ -853,7 +960,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 continue;
             }
 
-            for (int c0 = 0; c0 < n_mma; c0 += 16) {
+            for (int c0 = 16 * half; c0 < n_mma; c0 += 16 * kHalves) {
                 float v[16];
                 load_acc(c0, v);
                 if (EPI == kEpiGlu) {
@@ -868,14 +975,26 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[i] += bias;
                     }
-                    if (row_ok) {
+                    if (row_ok && p.y_rows) {
+                        // deterministic combine: this slot's weighted row,
+                        // summed in slot order by a later kernel
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int c = c0 + i;
-                            if (c < t.z) {
-                                atomicAdd(p.out + static_cast<size_t>(sm.meta_tok[c]) * p.w_rows + wrow,
+                            if (c < t.z && MOE_BOUNDS(t.y + c < p.rows_total, p.status))
+                                p.y_rows[static_cast<size_t>(t.y + c) * p.w_rows + wrow] =
+                                    sm.meta_w[c] * v[i];
+                        }
+                    } else if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int c = c0 + i;
+                            const int tok = c < t.z ? sm.meta_tok[c] : -1;
+                            if (tok >= 0 &&
+                                MOE_BOUNDS(tok < p.rows_total / p.top_k && wrow < p.w_rows,
+                                           p.status))
+                                atomicAdd(p.out + static_cast<size_t>(tok) * p.w_rows + wrow,
                                           sm.meta_w[c] * v[i]);
-                            }
                         }
                     }
                 }
@@ -890,6 +1009,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 mbar_arrive(smem_u32(sm.tempty + buf));
             }
         }
+        if (ep == 0) MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 6);
     } else if (WF == 3) {
         // ------------------------------------------------ MX scale writers
         // Warps 6..9 (one per TMEM lane quadrant) copy each ring slot's
@@ -1137,6 +1257,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, static_cast<uint32_t>(p.tmem_cols));
     }
+    if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 7);
 }
 
 template <int EPI, int WF, int CG>
@@ -1185,6 +1306,10 @@ cudaError_t launch_gemm_t(const GemmParams& p, const CUtensorMap* tmap_w, const 
 
 }  // namespace
 
+size_t trace_copy_gemm(unsigned long long* dst, size_t cap) {
+    MOE_TRACE_COPY(g_trace_gemm, dst, cap);
+}
+
 cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUtensorMap* tmap_w,
                         const CUtensorMap* tmap_x, int grid, size_t smem, cudaStream_t s,
                         bool pdl) {
@@ -1231,7 +1356,68 @@ __global__ void to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __re
         reinterpret_cast<uint2*>(out)[i] = pk;
     }
 }
+// Ordered combine: one thread per 4 output columns of a token; the token's
+// slots are added in slot order (j = 0, 1, ...), starting from zero.
+__global__ void combine_rows_kernel(const float* __restrict__ y_rows,
+                                    const int32_t* __restrict__ assign_row,
+                                    const int32_t* __restrict__ topk_ids, int T, int H, int k,
+                                    int ex_lo, int ex_hi, float* __restrict__ out32,
+                                    __nv_bfloat16* __restrict__ out16) {
+    pdl_wait();
+    const int h4 = H / 4;
+    const size_t n = static_cast<size_t>(T) * h4;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(i / h4), c4 = static_cast<int>(i % h4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int a = t * k + j;
+            const int e = __ldg(topk_ids + a), row = __ldg(assign_row + a);
+            if (row < 0 || e < ex_lo || e >= ex_hi) continue;
+#ifdef MOE_DEBUG_BOUNDS
+            if (row >= T * k) continue;    // (no status word here: skip only)
+#endif
+            const float4 y = __ldcg(reinterpret_cast<const float4*>(
+                                        y_rows + static_cast<size_t>(row) * H) + c4);
+            acc.x += y.x;
+            acc.y += y.y;
+            acc.z += y.z;
+            acc.w += y.w;
+        }
+        if (out16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(out16)[i] = pk;
+        } else {
+            reinterpret_cast<float4*>(out32)[i] = acc;
+        }
+    }
+}
 }  // namespace
+
+cudaError_t launch_combine_rows(const float* y_rows, const int32_t* assign_row,
+                                const int32_t* topk_ids, int T, int H, int k, int ex_lo,
+                                int ex_hi, float* out32, __nv_bfloat16* out16, cudaStream_t s,
+                                bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    const size_t n = static_cast<size_t>(T) * (H / 4);
+    size_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks == 0) blocks = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, combine_rows_kernel, y_rows, assign_row, topk_ids, T, H, k,
+                              ex_lo, ex_hi, out32, out16);
+}
 
 cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, size_t n, cudaStream_t s,
                            bool pdl) {

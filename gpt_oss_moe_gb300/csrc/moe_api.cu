@@ -5,6 +5,7 @@
 // all on the caller's stream, with no host synchronisation (xserv
 // docs/19-gpt-oss-moe.md, "Phase 19: gpt-oss-20b", §2 "MoE 前向").
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cstdlib>
@@ -12,6 +13,7 @@
 #include <mutex>
 
 #include "moe_internal.cuh"
+#include "trace.cuh"
 #include "../../include/moe.h"
 
 namespace moe {
@@ -132,6 +134,12 @@ std::atomic<int> g_token_tile{0};
 std::atomic<int> g_ksplit_mode{0};  // 0: automatic, 1: never split, n >= 2: n parts
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_pair_mode{0};   // 0: automatic, 1: never, 2: always (bf16 and FP8 weights)
+// 1: the combine adds each token's k expert outputs in slot order (bitwise
+// reproducible); 0: fp32 atomics in the down projection's epilogue
+std::atomic<int> g_deterministic{0};
+// test faults (moe_set_tuning "inject"): 1 = a routed id out of range, 2 = a
+// GEMM tile naming an expert out of range, 4 = a gate_up wait that runs out
+std::atomic<int> g_inject{0};
 // bf16 token boxes from which the GEMMs run on CTA pairs (automatic mode):
 // measured on gpt-oss-20b, pairs are 3 % slower at a 128-row box (T = 128),
 // even at 256 (T = 256) and 2-5 % faster at T >= 512
@@ -181,6 +189,41 @@ void prof_finish() {
     if (g_prof.calls == 0) g_prof.n_first = g_prof.n;
     if (g_prof.n == g_prof.n_first) ++g_prof.calls;   // calls of another shape are dropped
     g_prof.n = -1;
+}
+
+// ------------------------------------------------------------ NVTX
+//
+// With MOE_NVTX=1 in the environment (read once per process), every call
+// opens an NVTX range ("moe_forward", ...) and every kernel launch a nested
+// range named after the kernel, for timeline tools.  Off, the ranges cost a
+// branch.
+
+bool nvtx_on() {
+    static const bool on = [] {
+        const char* v = std::getenv("MOE_NVTX");
+        return v != nullptr && v[0] == '1';
+    }();
+    return on;
+}
+struct NvtxRange {
+    bool on;
+    explicit NvtxRange(const char* name) : on(nvtx_on()) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~NvtxRange() {
+        if (on) nvtxRangePop();
+    }
+};
+
+// With MOE_CHECK_STAGES=1 (read once per process) every forward call
+// checks each stage's output for NaN / infinity and its largest magnitude
+// (stage_check.cu; read with moe_stage_stats).
+bool stage_checks_on() {
+    static const bool on = [] {
+        const char* v = std::getenv("MOE_CHECK_STAGES");
+        return v != nullptr && v[0] == '1';
+    }();
+    return on;
 }
 
 // ------------------------------------------------------------ validation
@@ -324,8 +367,13 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     rp.token_tile = token_tile;
     rp.ex_lo = ex_lo;
     rp.ex_n = ex_n;
+    rp.inject = g_inject.load() & 3;
     rp.status = status;
-    MOE_CUDA(launch_router(rp, &tm_x, &tm_wr, router_smem_bytes(stages), stream));
+    {
+        NvtxRange nv("moe.router_topk");
+        MOE_CUDA(launch_router(rp, &tm_x, &tm_wr, router_smem_bytes(stages), stream,
+                               g_pdl.load() != 0));
+    }
     prof_mark("router_topk", stream);
 
     PermuteParams pp{};
@@ -357,7 +405,10 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     pp.ex_lo = ex_lo;
     pp.ex_hi = ex_lo + ex_n;
     pp.status = status;
-    MOE_CUDA(launch_permute(pp, stream, g_pdl.load() != 0));
+    {
+        NvtxRange nv(x_perm ? "moe.permute_gather" : "moe.permute");
+        MOE_CUDA(launch_permute(pp, stream, g_pdl.load() != 0));
+    }
     prof_mark(x_perm ? "permute_gather" : "permute", stream);
     return MOE_OK;
 }
@@ -371,7 +422,8 @@ extern "C" {
 
 size_t moe_workspace_bytes(const moe_shape* shape) {
     if (check_shape(shape) != MOE_OK) return 0;
-    return ws_layout(shape->T, shape->H, shape->I, shape->E, shape->top_k).total;
+    return ws_layout(shape->T, shape->H, shape->I, shape->E, shape->top_k,
+                     g_deterministic.load() != 0).total;
 }
 
 moe_status moe_route(const moe_shape* shape, const void* hidden, const void* router_w,
@@ -400,6 +452,7 @@ moe_status moe_route(const moe_shape* shape, const void* hidden, const void* rou
     r.offsets = expert_offsets ? expert_offsets : reinterpret_cast<int32_t*>(ws + L.offsets);
     r.sorted_assign =
         sorted_assign ? sorted_assign : reinterpret_cast<int32_t*>(ws + L.sorted_assign);
+    NvtxRange nv("moe_route");
     std::lock_guard<std::mutex> lock(g_prof_mu);
     prof_reset(stream);
     const moe_status st = launch_routing(s, L, ws, hidden, router_w, router_b, r, nullptr,
@@ -449,7 +502,8 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
         return MOE_ERR_ALIGN;
     if ((topk_ids_out && !aligned16(topk_ids_out)) || (topk_w_out && !aligned16(topk_w_out)))
         return MOE_ERR_ALIGN;
-    const WsLayout L = ws_layout(s.T, s.H, s.I, s.E, s.top_k);
+    const bool det = g_deterministic.load() != 0;
+    const WsLayout L = ws_layout(s.T, s.H, s.I, s.E, s.top_k, det);
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
     DevInfo dev;
     MOE_TRY(device_info(&dev));
@@ -565,8 +619,20 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     r.w = topk_w_out ? topk_w_out : reinterpret_cast<float*>(ws + L.topk_w);
     r.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
     r.sorted_assign = reinterpret_cast<int32_t*>(ws + L.sorted_assign);
-    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r, out32, x_perm, box, dev,
-                           stream, ex_lo, ex_n));
+    const bool checks = stage_checks_on();
+    if (checks)
+        MOE_CUDA(cudaMemsetAsync(status + kStageStatsWord, 0, 2 * kNumStages * sizeof(int32_t),
+                                 stream));
+    // deterministic combine: the ordered sum writes every output element,
+    // so the output needs no clearing
+    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r, det ? nullptr : out32,
+                           x_perm, box, dev, stream, ex_lo, ex_n));
+    // element type of the GEMM token operands: E4M3 codes (FP8, MXFP8) or bf16
+    const int tok_dtype = (fp8 || mx) ? 2 : 0;
+    if (checks)
+        MOE_CUDA(launch_stage_check(x_perm,
+                                    static_cast<size_t>(R) * (mx ? mx_padded_k(s.H) : s.H),
+                                    tok_dtype, 0, status, stream));
 
     GemmParams g{};
     g.tiles = reinterpret_cast<const int4*>(ws + L.tiles);
@@ -640,7 +706,15 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     long long units = tiles_max * g.n_wblocks * g.ksplit;
     long long ctas = units * cg;
     int grid = static_cast<int>(ctas < dev.sms ? ctas : dev.sms);
-    MOE_CUDA(launch_gemm(kEpiGlu, wf, cg, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
+    g.inject_stall = (g_inject.load() & 4) && !mxfp4 ? 1 : 0;
+    {
+        NvtxRange nv("moe.gate_up_glu");
+        MOE_CUDA(launch_gemm(kEpiGlu, wf, cg, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
+    }
+    if (checks)
+        MOE_CUDA(launch_stage_check(h, static_cast<size_t>(R) * (mx ? mx_padded_k(s.I) : s.I),
+                                    tok_dtype, 1, status, stream));
+    g.inject_stall = 0;
     prof_mark("gate_up_glu", stream);
 
     // down + bias + weighted combine -> out (fp32 accumulation)
@@ -659,20 +733,36 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     g.mx_cmax = s.I / 64 - 2;
     g.xs_mx = nullptr;                      // h codes: every block scale 2^-3
     // the down projection adds its K parts through the output's atomics
-    g.ksplit = pair ? 1 : parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, kMaxKSplit);
+    // (deterministic combine: whole K ranges, one stored row per slot)
+    g.ksplit = pair || det ? 1 : parts_for(tiles_max * g.n_wblocks, (g.k_blocks + kb_per_slot - 1) / kb_per_slot, kMaxKSplit);
     g.partial = nullptr;
     g.tickets = nullptr;
+    g.y_rows = det ? reinterpret_cast<float*>(ws + L.y_rows) : nullptr;
     units = tiles_max * g.n_wblocks * g.ksplit;
     ctas = units * cg;
     grid = static_cast<int>(ctas < dev.sms ? ctas : dev.sms);
-    MOE_CUDA(launch_gemm(kEpiCombine, wf, cg, g, &tm_wd, &tm_h, grid, smem, stream, pdl));
+    {
+        NvtxRange nv("moe.down_combine");
+        MOE_CUDA(launch_gemm(kEpiCombine, wf, cg, g, &tm_wd, &tm_h, grid, smem, stream, pdl));
+    }
     prof_mark("down_combine", stream);
 
-    if (!out_is_fp32) {
+    if (det) {
+        NvtxRange nv("moe.combine_ordered");
+        MOE_CUDA(launch_combine_rows(
+            g.y_rows, reinterpret_cast<const int32_t*>(ws + L.assign_row), r.ids, s.T, s.H,
+            s.top_k, ex_lo, ex_lo + ex_n, out_is_fp32 ? static_cast<float*>(out) : nullptr,
+            out_is_fp32 ? nullptr : static_cast<__nv_bfloat16*>(out), stream, pdl));
+        prof_mark("combine_ordered", stream);
+    } else if (!out_is_fp32) {
+        NvtxRange nv("moe.to_bf16");
         MOE_CUDA(launch_to_bf16(out32, static_cast<__nv_bfloat16*>(out),
                                 static_cast<size_t>(s.T) * s.H, stream, pdl));
         prof_mark("to_bf16", stream);
     }
+    if (checks)
+        MOE_CUDA(launch_stage_check(out, static_cast<size_t>(s.T) * s.H, out_is_fp32 ? 1 : 0, 2,
+                                    status, stream));
     prof_finish();
     return MOE_OK;
 }
@@ -685,6 +775,7 @@ moe_status moe_forward(const moe_shape* shape, const void* hidden, const void* r
                        int out_is_fp32, int32_t* topk_ids_out, float* topk_w_out,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     if (!shape) return MOE_ERR_ARG;
+    NvtxRange nv("moe_forward");
     return forward_impl(shape, 0, shape->E, hidden, router_w, router_b, gate_up, down, out,
                         out_is_fp32, topk_ids_out, topk_w_out, workspace, workspace_bytes,
                         stream);
@@ -696,6 +787,7 @@ moe_status moe_forward_ep(const moe_shape* shape, int expert_start, int local_ex
                           int32_t* topk_ids_out, float* topk_w_out, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream) {
     if (!shape) return MOE_ERR_ARG;
+    NvtxRange nv("moe_forward_ep");
     return forward_impl(shape, expert_start, local_experts, hidden, router_w, router_b,
                         gate_up, down, out, out_is_fp32, topk_ids_out, topk_w_out, workspace,
                         workspace_bytes, stream);
@@ -708,6 +800,35 @@ moe_status moe_get_device_status(const void* workspace, int32_t* host_status) {
         return MOE_ERR_CUDA;
     *host_status = v;
     return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+moe_status moe_stage_stats(const void* workspace, int32_t nonfinite[3], float maxabs[3]) {
+    if (!workspace || !nonfinite || !maxabs) return MOE_ERR_ARG;
+    int32_t w[2 * kNumStages];
+    if (cudaMemcpy(w, static_cast<const int32_t*>(workspace) + kStageStatsWord, sizeof w,
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    for (int i = 0; i < kNumStages; ++i) {
+        nonfinite[i] = w[2 * i];
+        std::memcpy(&maxabs[i], &w[2 * i + 1], sizeof(float));
+    }
+    return MOE_OK;
+}
+
+moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count) {
+    if (!count) return MOE_ERR_ARG;
+    *count = 0;
+    if (!out) return MOE_ERR_ARG;
+    unsigned long long* o = reinterpret_cast<unsigned long long*>(out);
+    size_t n = trace_copy_router(o, cap);
+    if (n == 0) return MOE_ERR_UNSUPPORTED;
+    const size_t n2 = trace_copy_permute(o + n, cap - n);
+    if (n2 == 0) return MOE_ERR_UNSUPPORTED;
+    n += n2;
+    const size_t n3 = trace_copy_gemm(o + n, cap - n);
+    if (n3 == 0) return MOE_ERR_UNSUPPORTED;
+    *count = n + n3;
+    return MOE_OK;
 }
 
 moe_status moe_clear_device_status(void* workspace, cudaStream_t stream) {
@@ -732,6 +853,21 @@ moe_status moe_set_tuning(const char* key, int value) {
     if (std::strcmp(key, "pair") == 0) {
         if (value < 0 || value > 2) return MOE_ERR_ARG;
         g_pair_mode.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "inject") == 0) {
+        if (value < 0 || value > 7) return MOE_ERR_ARG;
+        g_inject.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "deterministic") == 0) {
+        if (value != 0 && value != 1) return MOE_ERR_ARG;
+        g_deterministic.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "noalloc_poison") == 0) {
+        if (value != 0 && value != 1) return MOE_ERR_ARG;
+        set_noalloc_poison(value);
         return MOE_OK;
     }
     if (std::strcmp(key, "pdl") == 0) {

@@ -26,6 +26,24 @@ constexpr int kMaxTokenTile = 256;     // MMA N upper bound
 constexpr int kStatusWord = 0;
 constexpr int kNumTilesWord = 1;
 constexpr int kGridCounterWord = 2;
+// Stage checks (MOE_CHECK_STAGES=1): per stage s, the non-finite count at
+// word kStageStatsWord + 2 s and the largest finite magnitude (fp32 bits,
+// ordered as integers) at word kStageStatsWord + 2 s + 1.
+constexpr int kStageStatsWord = 16;
+constexpr int kNumStages = 3;
+
+// MOE_DEBUG_BOUNDS builds check the index of every store of the layer's
+// kernels against its buffer and skip a store that fails, reporting
+// MOE_DEV_BOUNDS; other builds compile the checks away.
+#ifdef MOE_DEBUG_BOUNDS
+__device__ __forceinline__ bool bounds_ok(bool ok, int32_t* status) {
+    if (!ok) atomicOr(status, 0x10);
+    return ok;
+}
+#define MOE_BOUNDS(cond, status) ::moe::bounds_ok((cond), (status))
+#else
+#define MOE_BOUNDS(cond, status) true
+#endif
 
 // Router ticket counters live at a fixed offset, right after the status
 // region, with one slot for every (token block, expert group) pair that can
@@ -115,14 +133,17 @@ __host__ __device__ inline int mx_scale_row_bytes(int K) {
 
 struct WsLayout {
     size_t status, topk_ids, topk_w, blk_cnt, logits, partials, counters, offsets, gemm_partial;
-    size_t sorted_assign, assign_row, tiles, x_perm, x_scale, h, out_acc, total;
+    size_t sorted_assign, assign_row, tiles, x_perm, x_scale, h, out_acc, y_rows, total;
     size_t gemm_partial_bytes;
     int max_tiles;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
+// deterministic: room for the per-slot output rows of the ordered combine
+// (fp32 [T*k, H], after every other region so that the others keep their
+// offsets whatever the mode).
+inline WsLayout ws_layout(long long T, int H, int I, int E, int k, bool deterministic = false) {
     WsLayout L{};
     const size_t R = static_cast<size_t>(T) * k;
     const size_t nb = (static_cast<size_t>(T) + kRouterTokens - 1) / kRouterTokens;
@@ -173,6 +194,7 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k) {
         L.gemm_partial_bytes = static_cast<size_t>(kSplitPartsAlloc) * nwb * rstar * kWeightTileRows * 4;
         L.gemm_partial = take(L.gemm_partial_bytes);
     }
+    L.y_rows = take(deterministic ? R * H * 4 : 0);
     L.total = o;
     return L;
 }
@@ -199,6 +221,8 @@ struct RouterParams {
     // expert-parallel form: GEMM tiles only for experts [ex_lo, ex_lo + ex_n),
     // numbered from 0 (the local weight banks); 0, E for the whole layer
     int ex_lo, ex_n;
+    int inject;                  // test faults: 1 = token 0's first id set to E
+                                 // after counting, 2 = tile 0 names expert ex_n
     int32_t* status;             // status region (status word, tile count, counter)
 };
 
@@ -265,8 +289,10 @@ struct GemmParams {
     int xs_row_bytes;
     int h_pad;
     int h_tail0;
-    // kEpiCombine: out[t, w_rows] += w * y
+    // kEpiCombine: out[t, w_rows] += w * y (fp32 atomics), or, when y_rows
+    // is set (deterministic combine), y_rows[routed row, w_rows] = w * y
     float* out;
+    float* y_rows;
     const int32_t* sorted_assign;
     const float* topk_w;
     int top_k;
@@ -277,6 +303,9 @@ struct GemmParams {
     int ksplit;
     float* partial;
     int32_t* tickets;
+    // test fault: the MMA issuer first waits on a barrier that nothing
+    // arrives on (the wait gives up after its bound and the kernel aborts)
+    int inject_stall;
 };
 
 // Shared memory of one GEMM pipeline stage and of the fixed part (bytes,
@@ -318,13 +347,26 @@ size_t router_smem_bytes(int stages);
 int router_max_stages();
 int router_stage_multiple();
 cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tmap_x,
-                          const CUtensorMap* tmap_wr, size_t smem, cudaStream_t s);
+                          const CUtensorMap* tmap_wr, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s, bool pdl);
 // cg = 2 (bf16 only): CTA pairs (clusters of 2) on 256-row weight blocks,
 // each CTA holding token_box / 2 rows of every token tile; `grid` counts CTAs.
 cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUtensorMap* tmap_w,
                         const CUtensorMap* tmap_x, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
+// Stage check: counts the non-finite elements of buf (n elements of type
+// dtype: 0 = bf16, 1 = fp32, 2 = E4M3 codes) and their largest finite
+// magnitude into the stage's status words.
+cudaError_t launch_stage_check(const void* buf, size_t n, int dtype, int stage, int32_t* status,
+                               cudaStream_t s);
+// moe_forward_noalloc's test switch (moe_set_tuning "noalloc_poison").
+void set_noalloc_poison(int on);
+// Deterministic combine: out[t] = sum over j in order of y_rows[assign_row[t*k + j]]
+// for the slots whose expert lies in [ex_lo, ex_hi); fp32 out32 or bf16 out16.
+cudaError_t launch_combine_rows(const float* y_rows, const int32_t* assign_row,
+                                const int32_t* topk_ids, int T, int H, int k, int ex_lo,
+                                int ex_hi, float* out32, __nv_bfloat16* out16, cudaStream_t s,
+                                bool pdl);
 cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, size_t n, cudaStream_t s,
                            bool pdl);
 

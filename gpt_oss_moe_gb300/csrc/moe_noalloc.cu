@@ -15,6 +15,7 @@
 // host code its name is only a host-side stand-in, never a device address, so
 // the first call on each device looks the real address up with
 // cudaGetSymbolAddress (with that device current) and caches it.
+#include <atomic>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -30,6 +31,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxNoallocDevices] = {};
+// Test switch ("noalloc_poison" of moe_set_tuning): the next call first fills
+// the array's status word and counters with non-zero bytes, as a call that
+// gave up on the device could have left them.
+std::atomic<int> g_noalloc_poison{0};
 
 // Device address of the scratch array on the current device (set-up on the
 // first call per device).
@@ -49,6 +54,9 @@ moe_status noalloc_scratch(void** out) {
 }
 
 }  // namespace
+
+void set_noalloc_poison(int on) { g_noalloc_poison.store(on ? 1 : 0); }
+
 }  // namespace moe
 
 extern "C" moe_status moe_forward_noalloc(const moe_shape* shape, const void* hidden,
@@ -71,9 +79,19 @@ extern "C" moe_status moe_forward_noalloc(const moe_shape* shape, const void* hi
     void* scratch = nullptr;
     moe_status st = moe::noalloc_scratch(&scratch);
     if (st != MOE_OK) return st;
-    // The array keeps the previous call's contents; only the status word must
-    // start from zero (every other region is fully rewritten by the kernels).
-    if (cudaMemsetAsync(scratch, 0, 256, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    // The array keeps the previous call's contents.  The status word and the
+    // block of completion counters after it (router tickets, expert totals,
+    // GEMM K-split tickets) must start from zero: a call completes only if
+    // every counter it uses starts at zero, and a call that gave up on the
+    // device (a wait timeout, a bad tile) leaves some of them set.  A caller
+    // of this entry point cannot reach the array to clear it, so every call
+    // clears them itself (256 + 134,528 bytes).  Every other region is fully
+    // rewritten by the kernels before it is read.
+    const size_t clear_bytes = 256 + moe::kCounterBytes;
+    if (moe::g_noalloc_poison.exchange(0) &&
+        cudaMemsetAsync(scratch, 0x5A, clear_bytes, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, clear_bytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
     st = moe_forward(shape, hidden, router_w, router_b, gate_up, down, out, out_is_fp32,
                      topk_ids_out, topk_w_out, scratch, moe::kNoallocScratchBytes, stream);
     if (st != MOE_OK) return st;

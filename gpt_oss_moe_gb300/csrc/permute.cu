@@ -25,10 +25,13 @@
 //      E4M3 of x / scale) into the padded layout of mx_pos.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "trace.cuh"
 #include "../../include/moe.h"
 
 namespace moe {
 namespace {
+
+MOE_TRACE_ARRAY(g_trace_permute, 1);
 
 constexpr int kThreads = 256;
 constexpr int kRowVecUnroll = 12;   // 16-byte vectors per lane in flight (H <= 6144)
@@ -71,8 +74,11 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
     __shared__ int running[kMaxExperts];
     __shared__ int rows_s[kRouterTokens * kMaxTopK];
 
+    const int trace_cta = blockIdx.y * gridDim.x + blockIdx.x;
+    if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_permute, 0, trace_cta, 0);
     pdl_wait();                 // routing tables of the previous kernel
     pdl_launch_dependents();    // the GEMM may start its prologue
+    if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_permute, 0, trace_cta, 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E, k = p.top_k, b = blockIdx.x;
@@ -115,6 +121,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
     // Stable ranks of this block's assignments (warp 0, 32 at a time).
     const int a0 = b * kRouterTokens * k;
     const int a1 = min(p.T, (b + 1) * kRouterTokens) * k;
+    const int rows_total = p.T * k;
     if (warp == 0) {
         for (int ab = a0; ab < a1; ab += 32) {
             const int a = ab + lane;
@@ -130,19 +137,26 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
             __syncwarp();
             if (good && rank == 0) running[e] = r0 + __popc(peers);
             __syncwarp();
-            const int row = good ? base[e] + r0 + rank : -1;
+            int row = good ? base[e] + r0 + rank : -1;
+            // counts that do not add up (a corrupted counter region) must not
+            // place a row outside [0, T*k): report it and drop the row
+            if (good && (row < 0 || row >= rows_total)) {
+                if (blockIdx.y == 0) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
+                row = -1;
+            }
             if (valid) {
                 if (blockIdx.y == 0) {
-                    if (good) p.sorted_assign[row] = a;
+                    if (row >= 0) p.sorted_assign[row] = a;
                     p.assign_row[a] = row;
                 }
                 // the gather copies only the rows of this device's experts
-                rows_s[a - a0] = good && e >= p.ex_lo && e < p.ex_hi ? row : -1;
+                rows_s[a - a0] = row >= 0 && e >= p.ex_lo && e < p.ex_hi ? row : -1;
             }
         }
     }
     __syncthreads();
 
+    if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_permute, 0, trace_cta, 2);
     // Clear this CTA's share of the block's fp32 output rows (the down
     // projection's epilogue accumulates into them).
     if (p.zero_out) {
@@ -165,6 +179,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
         for (int la = l0 + warp; la < l1; la += kThreads / 32) {
             const int row = rows_s[la];
             if (row < 0) continue;
+            if (!MOE_BOUNDS(row < rows_total && (a0 + la) / k < p.T, p.status + kStatusWord))
+                continue;
             const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>((a0 + la) / k) * p.H);
             if (p.mx8) {
                 // MXFP8: a block of 32 elements is the 4 vectors of 4
@@ -268,9 +284,17 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
             }
         }
     }
+#ifdef MOE_TRACE
+    __syncthreads();
+    if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_permute, 0, trace_cta, 3);
+#endif
 }
 
 }  // namespace
+
+size_t trace_copy_permute(unsigned long long* dst, size_t cap) {
+    MOE_TRACE_COPY(g_trace_permute, dst, cap);
+}
 
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};

@@ -39,10 +39,13 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "trace.cuh"
 #include "../../include/moe.h"
 
 namespace moe {
 namespace {
+
+MOE_TRACE_ARRAY(g_trace_router, 1);
 
 constexpr int kComputeWarps = 4;
 constexpr int kThreads = (kComputeWarps + 1) * 32;   // + one producer warp
@@ -197,7 +200,10 @@ __device__ void topk_block(const RouterParams& p, const float* logits, int ls, c
     }
 #pragma unroll
     for (int s = 0; s < K; ++s) {
-        p.topk_ids[static_cast<size_t>(t) * K + s] = be[s];
+        // test fault (inject & 1): token 0's first id is written out of range
+        // after it was counted, as a corrupted id would arrive
+        const bool bad = (p.inject & 1) && t == 0 && s == 0 && p.E < kMaxExperts;
+        p.topk_ids[static_cast<size_t>(t) * K + s] = bad ? p.E : be[s];
         p.topk_w[static_cast<size_t>(t) * K + s] = ex[s] / denom;
         atomicAdd(&hist[be[s]], 1);
     }
@@ -238,14 +244,20 @@ __device__ void finish_routing(const RouterParams& p, int* total_s, int* offs_s,
         const int per = ((m + nt - 1) / nt + 15) / 16 * 16;
         for (int i = 0; i < nt; ++i) {
             const int slot = toff_s[e] + i;
-            if (slot < p.max_tiles)
+            if (slot < p.max_tiles &&
+                MOE_BOUNDS(offs_s[e] + i * per + min(per, m - i * per) <= p.T * p.top_k,
+                           p.status + kStatusWord))
                 p.tiles[slot] =
                     make_int4(e - p.ex_lo, offs_s[e] + i * per, min(per, m - i * per), 0);
             else
                 atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
         }
     }
+    // test fault (inject & 2): the first tile names an expert the GEMMs do
+    // not hold
+    __syncthreads();
     if (tid == 0) {
+        if ((p.inject & 2) && toff_s[E] > 0) p.tiles[0] = make_int4(p.ex_n, 0, 1, 0);
         p.status[kNumTilesWord] = min(toff_s[E], p.max_tiles);
         p.status[kGridCounterWord] = 0;   // ready for the next call
     }
@@ -280,6 +292,15 @@ __global__ void __launch_bounds__(kThreads)
     const int c_begin = q * per;
     const int nc = min(nchunks, c_begin + per) - c_begin;   // chunks of this slice
 
+    // Inputs, workspace and counters may be written by the kernel launched
+    // before this one (a previous call's last kernel, or the caller's): wait
+    // for it before the first global access.  The permutation kernel may
+    // launch now: it waits for this grid to complete.
+    const int trace_cta = (b * p.egroups + g) * p.ksplit + q;
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 0);
+    pdl_wait();
+    pdl_launch_dependents();
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 1);
     if (nc > S && S % kComputeWarps != 0) {
         // a slot would be shared by two consumer warps: refuse (the host
         // never asks for this)
@@ -383,6 +404,7 @@ __global__ void __launch_bounds__(kThreads)
             }
     }
     __syncthreads();
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 2);
     if (flag[0]) {
         if (tid == 0) atomicOr(p.status + kStatusWord, MOE_DEV_WAIT_TIMEOUT);
         return;   // block-uniform: flag read after the barrier
@@ -492,6 +514,7 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
 
     // Top-k + softmax, one lane per token (the partial buffer is free now).
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 3);
     switch (p.top_k) {
         case 1: topk_block<1>(p, logits, ls, bias_s, partial, t0, hist); break;
         case 2: topk_block<2>(p, logits, ls, bias_s, partial, t0, hist); break;
@@ -523,12 +546,18 @@ __global__ void __launch_bounds__(kThreads)
     } else {
         __syncthreads();
     }
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 4);
     finish_routing(p, hist, scan_a, scan_b, scan_c);
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 5);
 }
 
 }  // namespace
 
 size_t router_stage_bytes() { return kStageBytes; }
+
+size_t trace_copy_router(unsigned long long* dst, size_t cap) {
+    MOE_TRACE_COPY(g_trace_router, dst, cap);
+}
 
 // Shared memory for `stages` ring slots (at least the top-k logits), the
 // warp partials, barriers and scan buffers, plus 1 KB alignment slack.
@@ -542,14 +571,23 @@ int router_max_stages() { return kMaxStages; }
 int router_stage_multiple() { return kComputeWarps; }
 
 cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tx, const CUtensorMap* tw,
-                          size_t smem, cudaStream_t s) {
+                          size_t smem, cudaStream_t s, bool pdl) {
     if (p.stages < 1 || p.stages > kMaxStages) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(router_topk_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    router_topk_kernel<<<dim3(p.nblocks, p.egroups, p.ksplit), kThreads, smem, s>>>(p, *tx, *tw);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.nblocks, p.egroups, p.ksplit);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, router_topk_kernel, p, *tx, *tw);
 }
 
 }  // namespace moe

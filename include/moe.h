@@ -109,7 +109,12 @@ typedef struct {
 /* Device status word bits (moe_get_device_status). */
 #define MOE_DEV_BAD_EXPERT_ID  0x1   /* a routed id fell outside [0, E) */
 #define MOE_DEV_WAIT_TIMEOUT   0x2   /* a pipeline wait gave up (~1 s) */
-#define MOE_DEV_BAD_TILE       0x4   /* a work tile failed its bounds check */
+#define MOE_DEV_BAD_TILE       0x4   /* a work tile or a permutation row
+                                        failed its bounds check */
+#define MOE_DEV_NONFINITE      0x8   /* a stage check (MOE_CHECK_STAGES=1) met
+                                        a NaN or an infinity */
+#define MOE_DEV_BOUNDS         0x10  /* an index check of a MOE_DEBUG_BOUNDS
+                                        build failed (the access was skipped) */
 
 /* Bytes of device workspace moe_route / moe_forward need for this shape
  * (0 for an invalid shape).  The workspace is scratch owned by the caller.
@@ -147,7 +152,8 @@ moe_status moe_route(const moe_shape* shape, const void* hidden,
  *   topk_ids_out int32 [T, top_k], topk_w_out fp32 [T, top_k]: optional
  *        copies of the routing (NULL to skip).
  * The fp32 combine adds the top_k expert outputs of a token in an order that
- * may vary from run to run (last-bit differences only). */
+ * may vary from run to run (last-bit differences only), unless the
+ * "deterministic" switch of moe_set_tuning is on. */
 moe_status moe_forward(const moe_shape* shape, const void* hidden,
                        const void* router_w, const void* router_b,
                        moe_weight gate_up, moe_weight down,
@@ -180,7 +186,10 @@ moe_status moe_forward_ep(const moe_shape* shape, int expert_start, int local_ex
                           cudaStream_t stream);
 
 /* Size of the library-owned scratch array used by moe_forward_noalloc
- * (8 MiB per device that loads the library, held until the process exits). */
+ * (8 MiB per device that loads the library, held until the process exits).
+ * A shape fits when moe_workspace_bytes(shape) <= this size; with
+ * H = I = 2880 and top_k = 4 that is T <= 129 for E = 32 and T <= 121 for
+ * E = 128. */
 #define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* moe_forward for callers that cannot allocate device memory.  The source
@@ -194,13 +203,16 @@ moe_status moe_forward_ep(const moe_shape* shape, int expert_start, int local_ex
  * The scratch lives in one static device array of MOE_NOALLOC_SCRATCH_BYTES
  * inside the library; the call allocates and frees nothing.  Shapes whose
  * moe_workspace_bytes exceeds that size are rejected with MOE_ERR_WORKSPACE
- * (at H = I = 2880 and top_k = 4 this admits up to T = 128 tokens).
+ * (see MOE_NOALLOC_SCRATCH_BYTES for the token counts this admits).
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call shares the one array and it keeps
- * the last call's contents (the status word is cleared at the start of each
- * call): calls whose work overlaps on the GPU -- on different streams, or
- * from different threads -- race on it and must be serialised by the caller. */
+ * the last call's contents; each call first clears (on its stream) the
+ * status word and the completion counters that follow it, so a call that
+ * gave up on the device does not leave the next one with stale counters.
+ * Calls whose work overlaps on the GPU -- on different streams, or from
+ * different threads -- race on the array and must be serialised by the
+ * caller. */
 moe_status moe_forward_noalloc(const moe_shape* shape, const void* hidden,
                                const void* router_w, const void* router_b,
                                moe_weight gate_up, moe_weight down,
@@ -218,6 +230,34 @@ moe_status moe_get_device_status(const void* workspace, int32_t* host_status);
  * (enqueued on `stream`). */
 moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
 
+/* Stage checks, for finding the first stage of the layer that goes wrong
+ * (§3 and §4 of the source page bisect their bugs this way: NaN and
+ * magnitude checks after every stage behind an environment switch).  With
+ * MOE_CHECK_STAGES=1 in the environment (read once per process), every
+ * moe_forward / moe_forward_ep call also runs, after each stage, a check of
+ * that stage's output: stage 0 the gathered activation rows (T * top_k rows
+ * in the GEMM operand's format), stage 1 the GLU output h, stage 2 the
+ * layer output.  Each check counts the elements that are NaN or infinite
+ * and takes the largest finite magnitude; a count above zero also sets
+ * MOE_DEV_NONFINITE.  This call copies the last checked call's figures to
+ * the host (synchronising, like moe_get_device_status): nonfinite[3] and
+ * maxabs[3], one entry per stage (0 and 0 when the checks are off). */
+moe_status moe_stage_stats(const void* workspace, int32_t nonfinite[3], float maxabs[3]);
+
+/* Phase timestamps of the last call's kernels, for timeline analysis.
+ * Only the "trace" build of the library (compiled with MOE_TRACE) records
+ * them; other builds return MOE_ERR_UNSUPPORTED.  Each kernel records the
+ * GPU's global timer (ns) at fixed points of each of its first 512 CTAs
+ * (CTA i: the linear block index).  *count receives the number of uint64
+ * values written to out (cap at least 16384): the router's [512][8] (entry,
+ * past the dependency wait, loads done, logits ready, routing tables
+ * started, done), the permutation's [512][8] (entry, past the wait, ranks
+ * done, exit), then the two GEMMs' [2][512][8] (gate_up, down: entry,
+ * set-up done, weight loads issued before the wait, producer past the wait,
+ * first MMA slot ready, last MMA commit, epilogue done, exit); unrecorded
+ * points hold earlier values.  Synchronises with the device. */
+moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
+
 /* Process-wide tuning switches for tests and benchmarks:
  *   "token_tile": rows of tokens per GEMM tile, 0 = automatic, else a
  *                 multiple of 16 in [16, 256] (MXFP4 and MXFP4 x MXFP8
@@ -229,6 +269,31 @@ moe_status moe_clear_device_status(void* workspace, cudaStream_t stream);
  *                 sums its K range in one fixed order), 2..8 = split every
  *                 small-batch unit into that many parts (at most one per
  *                 two ring slots, and as many as the workspace holds);
+ *   "deterministic": 1 = the down projection stores each slot's weighted
+ *                 output row (fp32, T * top_k rows of H) and a last kernel
+ *                 adds each token's top_k rows in slot order, so that the
+ *                 output is bitwise reproducible run to run (the down
+ *                 projection's K range is then never split);
+ *                 moe_workspace_bytes includes those rows while the switch
+ *                 is on, so query it after setting the switch (a workspace
+ *                 sized without them is refused with MOE_ERR_WORKSPACE);
+ *                 0 = fp32 atomics in the down projection (default);
+ *   "inject":     test faults that the device status word must report, as
+ *                 a bit mask (0 = none, default): 1 = token 0's first
+ *                 routed id is written as E (after it was counted), so the
+ *                 permutation reports MOE_DEV_BAD_EXPERT_ID; 2 = the first
+ *                 GEMM tile names an expert outside the banks, so the GEMMs
+ *                 skip it and report MOE_DEV_BAD_TILE; 4 = the gate_up
+ *                 GEMM's MMA issuer (bf16, FP8, MXFP4 x MXFP8 weights, no
+ *                 CTA pairs) first waits on a barrier that nothing arrives
+ *                 on, so the wait gives up after its ~1 s bound, the kernel
+ *                 aborts and MOE_DEV_WAIT_TIMEOUT is reported.  The outputs
+ *                 of such a call are not meaningful; clear the workspace
+ *                 (moe_clear_device_status) before its next use;
+ *   "noalloc_poison": 1 = the next moe_forward_noalloc call first fills the
+ *                 status word and completion counters of its scratch with
+ *                 non-zero bytes, as a failed call could leave them (a test
+ *                 of the clear that follows); 0 = off (default);
  *   "pair":       0 = run the bf16 and FP8 GEMMs on CTA pairs (M = 256 MMAs
  *                 over two SMs, 256-row weight blocks) when the token box is
  *                 256 rows and, for FP8, T * top_k < 128 * E (default),
