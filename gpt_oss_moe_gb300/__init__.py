@@ -25,7 +25,7 @@ LIB_PATH = os.environ.get("GPT_OSS_MOE_LIB") or os.path.join(_PKG, "libgpt_oss_m
 
 MOE_W_BF16, MOE_W_MXFP4, MOE_W_FP8, MOE_W_MXFP4_MXFP8 = 0, 1, 2, 3
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_BAD_TILE = 0x1, 0x2, 0x4
-MOE_DEV_NONFINITE, MOE_DEV_BOUNDS = 0x8, 0x10
+MOE_DEV_NONFINITE, MOE_DEV_BOUNDS, MOE_DEV_RANGE = 0x8, 0x10, 0x20
 
 # Every function the C header declares, in order (checked by the tests).
 EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_ep",

@@ -57,6 +57,8 @@
 // flight, the MMA issuer for its last MMAs, and TMEM is freed before exit.
 #include <type_traits>
 
+#include <cuda_fp16.h>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "trace.cuh"
@@ -95,9 +97,16 @@ constexpr int kMxScaleWarps = 4;        // MXFP4 x MXFP8: warps 6..9 write the s
 // (their other warps convert or write scales).
 template <int WF>
 constexpr int kEpiWarps = (WF == 0 || WF == 2) ? 8 : 4;
+// bf16 kernels: one more warp gathers token rows from the layer input for
+// small batches (GemmParams::gather_x), the last warp of the CTA.
+template <int WF>
+constexpr int kGatherWarpOf = WF == 0 ? 2 + kEpiWarps<WF> : -1;
 template <int WF>
 constexpr int kThreadsOf = WF == 1 ? 192 + kConvTeams * kConvThreads + 32
-                         : WF == 3 ? 192 + kMxScaleWarps * 32 : 64 + kEpiWarps<WF> * 32;
+                         : WF == 3 ? 192 + kMxScaleWarps * 32
+                         : 64 + kEpiWarps<WF> * 32 + (kGatherWarpOf<WF> >= 0 ? 32 : 0);
+// token-row copies of the gather warp in flight, in ring slots
+constexpr int kGatherLag = 3;
 constexpr int kSecondIssuerWarp = 6 + kConvTeams * kConvThreads / 32;    // MXFP4: warp 22
 
 struct SmemPlan {
@@ -117,6 +126,7 @@ struct SmemPlan {
     uint64_t* sfull;     // [2] scales landed (MXFP4)
     uint64_t* sempty;    // [2] scales consumed (MXFP4)
     uint64_t* drain;     // [2] one per MMA issuer
+    uint64_t* gfull;     // [stages] gathered token rows landed (bf16 small batches)
     uint32_t* tmem_base;
     int* flags;          // [0] abort, [1..2] epilogue broadcast (alternating),
                          // [3] K-split: this epilogue holds the last part
@@ -162,7 +172,8 @@ __device__ __forceinline__ SmemPlan plan_smem(uint8_t* raw, int stages, int asta
     s.sfull = s.tempty + 2;
     s.sempty = s.sfull + 2;
     s.drain = s.sempty + 2;
-    s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 2);
+    s.gfull = s.drain + 2;
+    s.tmem_base = reinterpret_cast<uint32_t*>(s.gfull + stages);
     s.flags = reinterpret_cast<int*>(s.tmem_base + 1);
     return s;
 }
@@ -243,6 +254,19 @@ __device__ __forceinline__ int kperm8_pos(int c) {
     return (c & ~7) | ((c & 3) << 1) | ((c >> 2) & 1);
 }
 
+// f16 mode of the MXFP4 kernels: scale bytes whose every E2M1 multiple is
+// an f16 (0.5 * 2^(s-127) >= 2^-24, 6 * 2^(s-127) <= 65504).
+constexpr uint32_t kF16ScaleLo = 104;
+constexpr uint32_t kF16ScaleHi = 140;
+
+// 2^e as f16x2, -24 <= e <= 15 (subnormal below 2^-14).
+__device__ __forceinline__ __half2 f16_pow2_x2(int e) {
+    const uint32_t h = e >= -14 ? static_cast<uint32_t>(e + 15) << 10
+                                : 1u << static_cast<uint32_t>(e + 24);
+    const uint32_t hh = h | (h << 16);
+    return *reinterpret_cast<const __half2*>(&hh);
+}
+
 // The factor(s) that turn an embedded code into e2m1(code) * 2^(s-127),
 // as bf16x2: 2^(s-1) when s <= 128 (bf16 exponent field s + 126), else
 // 2^127 then 2^(s-128).  Scale bytes 0 and 255 (zero, NaN) are not produced
@@ -302,6 +326,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         p.ksplit < 1 || p.ksplit > kMaxKSplit ||
         (EPI == kEpiGlu && p.ksplit > 1 && (p.partial == nullptr || p.tickets == nullptr)) ||
         (kPair && (WF == 1 || WF == 3 || p.ksplit != 1 || (gridDim.x & 1u) || (box & 15))) ||
+        (p.gather_x != nullptr && (WF != 0 || kPair || stages <= kGatherLag || box > 64 ||
+                                   p.sorted_assign == nullptr || p.top_k < 1)) ||
         (WF == 3 && (box > 128 || p.mx_cmax < 0 ||
                      sf_col0 + 8u * KPS * static_cast<uint32_t>(stages) >
                          static_cast<uint32_t>(p.tmem_cols))) ||
@@ -328,6 +354,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         for (int s = 0; s < stages; ++s) {
             // MXFP4 x MXFP8: the producer's arrival + one per scale warp
             mbar_init(smem_u32(sm.full + s), WF == 3 ? 1 + kMxScaleWarps : 1);
+            mbar_init(smem_u32(sm.gfull + s), 1);
             mbar_init(smem_u32(sm.empty + s), 1);
         }
         for (int s = 0; s < astages; ++s) {
@@ -367,15 +394,18 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
     const uint32_t tmem_base = *sm.tmem_base;
     if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 1);
 
-    // The GEMM token tiles were written by the router, which has completed
-    // before this kernel starts: the launch order is router -> permutation
-    // -> gate_up -> down, and each of those kernels lets its successor start
-    // only after its own griddepcontrol.wait has returned, i.e. after its
-    // predecessor completed.  The token operand (gathered activations, or h)
-    // is written by the kernel launched just before this one and is read
-    // only after griddepcontrol.wait.  The producer therefore streams the
-    // first ring slots' weight tiles (and weight scales) before that wait,
-    // overlapping the previous kernel; every other role waits first.
+    // The GEMM token tiles were written by the router.  With p.prewait set
+    // the router has completed before this kernel starts: the launch order
+    // is router -> permutation -> gate_up -> down, and each of the later
+    // kernels lets its successor start only after its own
+    // griddepcontrol.wait has returned, i.e. after its predecessor
+    // completed.  The token operand (gathered activations, or h) is written
+    // by the kernel launched just before this one and is read only after
+    // griddepcontrol.wait.  The producer therefore streams the first ring
+    // slots' weight tiles (and weight scales) before that wait, overlapping
+    // the previous kernel; every other role waits first.  Without p.prewait
+    // (small batches: the router launched just before gate_up) the producer
+    // too waits before reading the tile list.
     if (warp != 0) {
         pdl_wait();
         pdl_launch_dependents();
@@ -394,6 +424,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             // token part; the slot's full barrier expects both.
             const auto slot_loads = [&](const Unit& un, const int4& t, int st, int stage,
                                         bool wpart, bool tpart, bool expect) {
+                (void)tpart;
                 const uint32_t fb = smem_u32(sm.full + stage);
                 const int mb = un.mb;
                 // full boxes are counted, zero-filled past K included;
@@ -401,10 +432,14 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 // MXFP4 x MXFP8: nk k-blocks (the K range's last slot may
                 // hold one), 8 KB of codes + the token tile each
                 const int nk = min(KPS, p.k_blocks - st * KPS);
+                // (gathered token rows arrive through the gather warp)
+                const bool gathered = WF == 0 && p.gather_x != nullptr;
+                if (gathered) tpart = false;
                 if (expect && rank == 0)
                     mbar_arrive_expect_tx(
                         fb, WF == 3 ? static_cast<uint32_t>(nk) * (kMxCodeTxBytes + b_bytes)
-                                    : (kPair ? 2u : 1u) * (w_bytes + b_stage_bytes));
+                                    : (kPair ? 2u : 1u) *
+                                          (w_bytes + (gathered ? 0u : b_stage_bytes)));
                 const uint32_t b_dst = smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
                 if (WF == 1) {
                     // codes of k-blocks 4st..4st+3 (128 B per row), and the
@@ -472,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             // Before the wait: the weight parts of the first ring slots (at
             // most one ring), and the first two units' weight scales.
             int npre = 0, npre_units = 0;
-            {
+            if (p.prewait) {
                 int stage = 0, local = 0;
                 for (int u = cta0; u < num_units && npre < stages; u += ncta) {
                     const Unit un = unit_of(u, p, n_st);
@@ -494,13 +529,17 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             pdl_wait();
             pdl_launch_dependents();
             MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 3);
+            // without the early pass the tile list may come from the kernel
+            // just before this one: count the units only now
+            const int num_units_p =
+                p.prewait ? num_units : __ldcg(p.num_tiles) * p.n_wblocks * p.ksplit;
 
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
             int local = 0;
             bool ok = true;
-            for (int u = cta0; u < num_units && ok; u += ncta) {
+            for (int u = cta0; u < num_units_p && ok; u += ncta) {
                 const Unit un = unit_of(u, p, n_st);
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
@@ -602,7 +641,10 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * acc_stride;
                 for (int st = un.st_lo; st < un.st_hi; ++st) {
-                    if (!warp_wait(smem_u32(sm.full + stage), phase, flags)) {
+                    // (gathered token rows: their own barrier)
+                    if (!warp_wait(smem_u32(sm.full + stage), phase, flags) ||
+                        (p.gather_x != nullptr &&
+                         !warp_wait(smem_u32(sm.gfull + stage), phase, flags))) {
                         if (leader) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
                         ok = false;
                         break;
@@ -704,7 +746,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 const int4 t = p.tiles[un.tile];
                 if (!tile_ok(t, p)) continue;
                 const uint32_t n_mma = static_cast<uint32_t>((t.z + 15) & ~15);
-                const uint32_t idesc = idesc_bf16_f32(kWeightTileRows, n_mma);
+                const uint32_t idesc = p.mx_f16 ? idesc_f16_f32(kWeightTileRows, n_mma)
+                                                : idesc_bf16_f32(kWeightTileRows, n_mma);
                 const int buf = local & 1;
                 const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
                 ++local;
@@ -780,6 +823,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int half = (warp - 2) >> 2;         // this warp's share of the columns
         const int row_in_tile = quad * 32 + lane;
+        if (p.zero_out != nullptr) {
+            // the output rows the down projection will accumulate into
+            float4* z = reinterpret_cast<float4*>(p.zero_out);
+            for (size_t i = static_cast<size_t>(blockIdx.x) * kEpiThreads + ep; i < p.n_zero / 4;
+                 i += static_cast<size_t>(gridDim.x) * kEpiThreads)
+                z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         int local = 0;
         int sbase = 0;                            // ring use of the unit's first slot
         for (int u = cta0; u < num_units; u += ncta) {
@@ -864,7 +914,8 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                 // MXFP4: h is the down projection's token operand in its
                 // layout -- chunk-major [I/64][T*k][64], each group of 8
                 // columns in the order 0,4,1,5,2,6,3,7
-                const int hcol = WF == 1 ? kperm8_pos(wrow >> 1) : (wrow >> 1);
+                // (f16 mode: natural order, f16 values)
+                const int hcol = WF == 1 && !p.mx_f16 ? kperm8_pos(wrow >> 1) : (wrow >> 1);
                 __nv_bfloat16* hrow0 =
                     WF == 1 ? p.h + (static_cast<size_t>(hcol >> 6) * p.rows_total + t.y) * 64 +
                                   (hcol & 63)
@@ -903,9 +954,13 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                             *dst = static_cast<uint8_t>(
                                 cvt_e4m3x2(clamped_glu(gate, up) * (1.f / kFp8HScale), 0.f));
                             if (h8gap) dst[-64] = 0;
-                        } else
+                        } else if (WF == 1 && p.mx_f16) {
+                            reinterpret_cast<__half*>(hrow0)[static_cast<size_t>(c) * hstride] =
+                                __float2half_rn(clamped_glu(gate, up));
+                        } else {
                             hrow0[static_cast<size_t>(c) * hstride] =
                                 __float2bfloat16_rn(clamped_glu(gate, up));
+                        }
                     }
                 }
             };
@@ -1010,6 +1065,88 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
             }
         }
         if (ep == 0) MOE_TRACE_POINT(g_trace_gemm, EPI, blockIdx.x, 6);
+    } else if (kGatherWarpOf<WF> >= 0 && warp == kGatherWarpOf<WF>) {
+        // ------------------------------------------------ token-row gather
+        // Small batches (bf16 gate_up): each ring slot's token tile is copied
+        // here from the layer input, row r of tile t being input row
+        // sorted_assign[t.y + r] / top_k, 16 bytes per lane with cp.async into
+        // the 128-byte-swizzled layout TMA would have written (chunk c of row
+        // r at chunk c ^ (r % 8)).  Copies of kGatherLag slots stay in
+        // flight; a slot's copies are awaited, made visible to the tensor
+        // cores (proxy fence) and announced with one arrival.  Rows past the
+        // tile keep whatever they held: their products are never stored.
+        // (The slot's own "gfull" barrier, not "full", takes the arrival, so
+        // that "full" still tracks the TMA bytes alone for the producer's
+        // bounded drain after an abort.)
+        if (p.gather_x != nullptr) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int inflight = 0;
+            bool ok = true;
+            const auto announce_oldest = [&](int pending) {
+                int s0 = stage - (pending - 1);
+                if (s0 < 0) s0 += stages;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(sm.gfull + s0));
+            };
+            for (int u = cta0; u < num_units && ok; u += ncta) {
+                const Unit un = unit_of(u, p, n_st);
+                const int4 t = p.tiles[un.tile];
+                if (!tile_ok(t, p)) continue;
+                // input rows of tile rows lane and lane + 32 (t.z <= 64 here)
+                int tok0 = -1, tok1 = -1;
+                if (lane < t.z) {
+                    const int a = p.sorted_assign[t.y + lane];
+                    if (a >= 0 && a < p.rows_total) tok0 = a / p.top_k;
+                }
+                if (lane + 32 < t.z) {
+                    const int a = p.sorted_assign[t.y + lane + 32];
+                    if (a >= 0 && a < p.rows_total) tok1 = a / p.top_k;
+                }
+                const int nchunk = t.z * 8;
+                for (int st = un.st_lo; st < un.st_hi; ++st) {
+                    if (!warp_wait(smem_u32(sm.empty + stage), phase ^ 1u, flags)) {
+                        if (lane == 0) raise_abort(flags, p.status, MOE_DEV_WAIT_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t b_dst = smem_u32(sm.b + static_cast<size_t>(stage) * b_stage_bytes);
+                    for (int base = 0; base < nchunk; base += 32) {
+                        const int i = base + lane, r = i >> 3, c = i & 7;
+                        const int ta = __shfl_sync(0xffffffffu, tok0, r & 31);
+                        const int tb = __shfl_sync(0xffffffffu, tok1, r & 31);
+                        const int tk = r < 32 ? ta : tb;
+                        if (i < nchunk && tk >= 0)
+                            cp_async_16(b_dst + static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)),
+                                        p.gather_x + static_cast<size_t>(tk) * p.gather_K +
+                                            st * kBlockK + c * 8);
+                    }
+                    cp_async_commit();
+                    if (++inflight > kGatherLag) {
+                        cp_async_wait<kGatherLag>();
+                        announce_oldest(inflight);
+                        --inflight;
+                    }
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // the last slots: every copy landed (also on an abort, before the
+            // CTA's shared memory is released)
+            cp_async_wait<0>();
+            if (ok) {
+                for (; inflight > 0; --inflight) {
+                    int s0 = stage - inflight;
+                    if (s0 < 0) s0 += stages;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(sm.gfull + s0));
+                }
+            }
+        }
     } else if (WF == 3) {
         // ------------------------------------------------ MX scale writers
         // Warps 6..9 (one per TMEM lane quadrant) copy each ring slot's
@@ -1224,10 +1361,39 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
                     if (jj < nk) {
                         cw[jj] = code_of(jj);
                         sb[jj] = scale_of(jj);
-                        big |= sb[jj] > 128u;
+                        big |= p.mx_f16 ? (sb[jj] < kF16ScaleLo || sb[jj] > kF16ScaleHi)
+                                        : sb[jj] > 128u;
                     }
                 }
-                if (__any_sync(0xffffffffu, big)) {
+                if (p.mx_f16) {
+                    // f16 operands: each byte of codes is two f16 values by
+                    // the hardware conversion, times 2^(s-127) in f16 (one
+                    // multiply per pair, exact for scale bytes in
+                    // [kF16ScaleLo, kF16ScaleHi]); a scale outside that
+                    // range is clamped into it and reported
+                    if (__any_sync(0xffffffffu, big) && lane == 0)
+                        atomicOr(p.status + kStatusWord, MOE_DEV_RANGE);
+#pragma unroll
+                    for (int jj = 0; jj < KPS; ++jj) {
+                        if (jj >= nk) break;
+                        const uint32_t sc = min(max(sb[jj], kF16ScaleLo), kF16ScaleHi);
+                        const __half2 f = f16_pow2_x2(static_cast<int>(sc) - 127);
+                        const uint32_t words[4] = {cw[jj].x, cw[jj].y, cw[jj].z, cw[jj].w};
+                        uint32_t v[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 q = e2m1x8_to_f16x8(words[c]);
+                            const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __half2 m =
+                                    __hmul2(*reinterpret_cast<const __half2*>(&qq[e]), f);
+                                v[4 * c + e] = *reinterpret_cast<const uint32_t*>(&m);
+                            }
+                        }
+                        tmem_st16(a_tm + 32u * static_cast<uint32_t>(jj), v);
+                    }
+                } else if (__any_sync(0xffffffffu, big)) {
 #pragma unroll
                     for (int jj = 0; jj < KPS; ++jj)
                         if (jj < nk) convert_store(std::true_type{}, jj, cw[jj], sb[jj]);

@@ -140,6 +140,14 @@ std::atomic<int> g_deterministic{0};
 // test faults (moe_set_tuning "inject"): 1 = a routed id out of range, 2 = a
 // GEMM tile naming an expert out of range, 4 = a gate_up wait that runs out
 std::atomic<int> g_inject{0};
+// 1: small bf16 batches skip the permutation kernel (the router permutes,
+// gate_up gathers token rows itself); 0: always the permutation kernel
+std::atomic<int> g_small_path{1};
+// 1: MXFP4 weights with bf16 activations run on f16 operands (hardware E2M1
+// conversion; exact for scale bytes in [104, 140] and activations within
+// +-65504, others reported as MOE_DEV_RANGE); 0: bf16 operands, exact for
+// every scale
+std::atomic<int> g_mxfp4_f16{1};
 // bf16 token boxes from which the GEMMs run on CTA pairs (automatic mode):
 // measured on gpt-oss-20b, pairs are 3 % slower at a 128-row box (T = 128),
 // even at 256 (T = 256) and 2-5 % faster at T >= 512
@@ -310,10 +318,14 @@ struct Routing {
 };
 
 // K1 + K2.  x_perm null = no gather (routing only).
+// small_perm: the router's last CTA writes the permutation (T * top_k <=
+// kSmallPermRows) and the permutation kernel is not launched (the GEMM
+// then gathers the token rows and clears the output itself).
 moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, const void* hidden,
                           const void* router_w, const void* router_b, const Routing& r,
                           float* zero_out, __nv_bfloat16* x_perm, int token_tile,
-                          const DevInfo& dev, cudaStream_t stream, int ex_lo, int ex_n) {
+                          const DevInfo& dev, cudaStream_t stream, int ex_lo, int ex_n,
+                          bool small_perm = false) {
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     const int nb = (s.T + kRouterTokens - 1) / kRouterTokens;
 
@@ -356,7 +368,6 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     rp.ksplit = router_ksplit(nb * rp.egroups, nchunks);
     rp.stages = stages;
     rp.logits = reinterpret_cast<float*>(ws + L.logits);
-    rp.partials = reinterpret_cast<float*>(ws + L.partials);
     rp.counters = reinterpret_cast<int32_t*>(ws + L.counters);
     rp.topk_ids = r.ids;
     rp.topk_w = r.w;
@@ -368,6 +379,9 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     rp.ex_lo = ex_lo;
     rp.ex_n = ex_n;
     rp.inject = g_inject.load() & 3;
+    rp.small_perm = small_perm ? 1 : 0;
+    rp.sorted_assign = r.sorted_assign;
+    rp.assign_row = reinterpret_cast<int32_t*>(ws + L.assign_row);
     rp.status = status;
     {
         NvtxRange nv("moe.router_topk");
@@ -375,6 +389,8 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
                                g_pdl.load() != 0));
     }
     prof_mark("router_topk", stream);
+
+    if (small_perm) return MOE_OK;
 
     PermuteParams pp{};
     pp.topk_ids = r.ids;
@@ -399,6 +415,7 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     pp.assign_row = reinterpret_cast<int32_t*>(ws + L.assign_row);
     pp.x_perm = x_perm;
     pp.mx_layout = s.wfmt == MOE_W_MXFP4 ? 1 : 0;
+    pp.mx_f16 = s.wfmt == MOE_W_MXFP4 && g_mxfp4_f16.load() != 0 ? 1 : 0;
     pp.fp8 = s.wfmt == MOE_W_FP8 ? 1 : 0;
     pp.mx8 = s.wfmt == MOE_W_MXFP4_MXFP8 ? 1 : 0;
     pp.x_scale = reinterpret_cast<float*>(ws + L.x_scale);
@@ -623,15 +640,22 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     if (checks)
         MOE_CUDA(cudaMemsetAsync(status + kStageStatsWord, 0, 2 * kNumStages * sizeof(int32_t),
                                  stream));
+    // Small bf16 batches: the router makes the permutation and gate_up
+    // gathers its token rows from `hidden` (no permutation kernel, no x_perm
+    // round trip; gate_up clears the output rows)
+    const bool small = g_small_path.load() != 0 && !mxfp4 && !fp8 && !mx && !pair &&
+                       R <= kSmallPermRows && box <= 64 && stages > 4;
     // deterministic combine: the ordered sum writes every output element,
     // so the output needs no clearing
-    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r, det ? nullptr : out32,
-                           x_perm, box, dev, stream, ex_lo, ex_n));
+    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r,
+                           det || small ? nullptr : out32, small ? nullptr : x_perm, box, dev,
+                           stream, ex_lo, ex_n, small));
     // element type of the GEMM token operands: E4M3 codes (FP8, MXFP8) or bf16
-    const int tok_dtype = (fp8 || mx) ? 2 : 0;
+    const int tok_dtype = (fp8 || mx) ? 2 : (mxfp4 && g_mxfp4_f16.load() != 0) ? 3 : 0;
     if (checks)
-        MOE_CUDA(launch_stage_check(x_perm,
-                                    static_cast<size_t>(R) * (mx ? mx_padded_k(s.H) : s.H),
+        MOE_CUDA(launch_stage_check(small ? hidden : static_cast<const void*>(x_perm),
+                                    small ? static_cast<size_t>(s.T) * s.H
+                                          : static_cast<size_t>(R) * (mx ? mx_padded_k(s.H) : s.H),
                                     tok_dtype, 0, status, stream));
 
     GemmParams g{};
@@ -645,6 +669,7 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     g.num_experts = ex_n;            // tiles number the local experts from 0
     g.rows_total = R;
     g.status = status;
+    g.mx_f16 = mxfp4 && g_mxfp4_f16.load() != 0 ? 1 : 0;
 
     const int unit_rows = pair ? 2 * kWeightTileRows : kWeightTileRows;
     const int cg = pair ? 2 : 1;
@@ -707,6 +732,18 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     long long ctas = units * cg;
     int grid = static_cast<int>(ctas < dev.sms ? ctas : dev.sms);
     g.inject_stall = (g_inject.load() & 4) && !mxfp4 ? 1 : 0;
+    // small batches: token rows gathered from the input; the tile list comes
+    // from the router, the kernel just before, so nothing starts before the
+    // dependency wait; the output rows are cleared here
+    g.gather_x = small ? static_cast<const __nv_bfloat16*>(hidden) : nullptr;
+    g.gather_K = s.H;
+    // (the gather reads the permutation: row r of a tile is assignment
+    // sorted_assign[r] of token sorted_assign[r] / top_k)
+    g.sorted_assign = r.sorted_assign;
+    g.top_k = s.top_k;
+    g.zero_out = small && !det ? out32 : nullptr;
+    g.n_zero = static_cast<size_t>(s.T) * s.H;
+    g.prewait = small ? 0 : 1;
     {
         NvtxRange nv("moe.gate_up_glu");
         MOE_CUDA(launch_gemm(kEpiGlu, wf, cg, g, &tm_wgu, &tm_x, grid, smem, stream, pdl));
@@ -715,6 +752,9 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
         MOE_CUDA(launch_stage_check(h, static_cast<size_t>(R) * (mx ? mx_padded_k(s.I) : s.I),
                                     tok_dtype, 1, status, stream));
     g.inject_stall = 0;
+    g.gather_x = nullptr;
+    g.zero_out = nullptr;
+    g.prewait = 1;           // tiles from the router, two kernels back
     prof_mark("gate_up_glu", stream);
 
     // down + bias + weighted combine -> out (fp32 accumulation)
@@ -853,6 +893,16 @@ moe_status moe_set_tuning(const char* key, int value) {
     if (std::strcmp(key, "pair") == 0) {
         if (value < 0 || value > 2) return MOE_ERR_ARG;
         g_pair_mode.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "mxfp4_f16") == 0) {
+        if (value != 0 && value != 1) return MOE_ERR_ARG;
+        g_mxfp4_f16.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "small_path") == 0) {
+        if (value != 0 && value != 1) return MOE_ERR_ARG;
+        g_small_path.store(value);
         return MOE_OK;
     }
     if (std::strcmp(key, "inject") == 0) {

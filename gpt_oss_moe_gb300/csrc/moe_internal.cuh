@@ -105,9 +105,13 @@ constexpr int kExpertTotalsOffset = kPairSlots + kMaxTokenBlocks + kSplitTargetU
 // on an SM; sized for GB300's 152 SMs; each slice keeps at least 4 chunks of
 // 64).  Measured at T = 4096: 3 slices (384 CTAs) left the last CTAs
 // starting 8 us after the first.
+// The slices of one pair form a thread-block cluster (at most the portable
+// 8 CTAs), which adds their partial logits through distributed shared memory.
+constexpr int kMaxRouterSlices = 8;
 inline int router_ksplit(int pairs, int nchunks) {
     if (pairs < 1 || nchunks < 1) return 1;
     int ks = 304 / pairs;                            // one wave of 2 CTAs per SM
+    if (ks > kMaxRouterSlices) ks = kMaxRouterSlices;
     const int cap = nchunks / 4 > 1 ? nchunks / 4 : 1;
     if (ks > cap) ks = cap;
     if (ks < 1) ks = 1;
@@ -162,7 +166,8 @@ inline WsLayout ws_layout(long long T, int H, int I, int E, int k, bool determin
     const size_t eg = (static_cast<size_t>(E) + 31) / 32;
     const int ks = router_ksplit(static_cast<int>(nb * eg), H / kBlockK);
     L.logits = take(eg > 1 ? nb * kRouterTokens * E * 4 : 0);
-    L.partials = take(ks > 1 ? nb * eg * ks * kRouterTokens * 32 * 4 : 0);
+    (void)ks;                              // (slices merge in shared memory)
+    L.partials = take(0);
     L.offsets = take((E + 1) * 4);
     L.sorted_assign = take(R * 4);
     L.assign_row = take(R * 4);
@@ -209,7 +214,6 @@ struct RouterParams {
     int ksplit;
     int stages;                  // TMA ring depth
     float* logits;               // [nblocks, 32, E] when egroups > 1
-    float* partials;             // [nblocks, egroups, ksplit, 32, 32] when ksplit > 1
     int32_t* counters;           // fixed counter region, zero between calls
     int32_t* topk_ids;           // [T, k]
     float* topk_w;               // [T, k]
@@ -223,8 +227,15 @@ struct RouterParams {
     int ex_lo, ex_n;
     int inject;                  // test faults: 1 = token 0's first id set to E
                                  // after counting, 2 = tile 0 names expert ex_n
+    // small batches (T * top_k <= kSmallPermRows): the last CTA also writes
+    // the stable permutation (no permutation kernel)
+    int small_perm;
+    int32_t* sorted_assign;      // [T*k] (small_perm)
+    int32_t* assign_row;         // [T*k] (small_perm)
     int32_t* status;             // status region (status word, tile count, counter)
 };
+// Largest T * top_k whose permutation the router's last CTA makes itself.
+constexpr int kSmallPermRows = 256;
 
 // ------------------------------------------------------------ permutation (K2)
 
@@ -245,6 +256,8 @@ struct PermuteParams {
     int fp8;                     // FP8 W8A8: x_perm holds E4M3 codes [T*k, H]
     float* x_scale;              // FP8: [T*k] scale of each routed row's codes
     int ex_lo, ex_hi;            // gather only the rows of experts [ex_lo, ex_hi)
+    int mx_f16;                  // with mx_layout: f16 values in natural order
+                                 // (values beyond +-65504 reported, saturated)
     int mx8;                     // MXFP8 activations: x_perm holds E4M3 codes
                                  // [T*k, mx_padded_k(H)] and x_scale UE8M0
                                  // bytes [T*k, mx_padded_k(H) / 32]
@@ -306,6 +319,21 @@ struct GemmParams {
     // test fault: the MMA issuer first waits on a barrier that nothing
     // arrives on (the wait gives up after its bound and the kernel aborts)
     int inject_stall;
+    // small batches, bf16 gate_up: token rows come straight from the layer
+    // input (row = sorted_assign[tile row] / top_k), gathered by the kernel
+    // (null: the token operand is read through tmap_x); zero_out[0, n_zero)
+    // fp32 is cleared first (the output the down projection accumulates
+    // into); prewait = 0: the tile list comes from the immediately preceding
+    // kernel, so no load may start before the dependency wait
+    // MXFP4 (WF = 1) f16 mode: the token operands hold f16 in natural K
+    // order and the converters expand E2M1 to f16 (else bf16, with the
+    // 0,4,1,5,2,6,3,7 order within groups of 8)
+    int mx_f16;
+    const __nv_bfloat16* gather_x;
+    int gather_K;                // elements per row of gather_x
+    float* zero_out;
+    size_t n_zero;
+    int prewait;
 };
 
 // Shared memory of one GEMM pipeline stage and of the fixed part (bytes,
@@ -355,7 +383,7 @@ cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUte
                         const CUtensorMap* tmap_x, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
 // Stage check: counts the non-finite elements of buf (n elements of type
-// dtype: 0 = bf16, 1 = fp32, 2 = E4M3 codes) and their largest finite
+// dtype: 0 = bf16, 1 = fp32, 2 = E4M3 codes, 3 = f16) and their largest finite
 // magnitude into the stage's status words.
 cudaError_t launch_stage_check(const void* buf, size_t n, int dtype, int stage, int32_t* status,
                                cudaStream_t s);

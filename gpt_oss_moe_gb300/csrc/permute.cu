@@ -23,6 +23,8 @@
 //      With MXFP8 activations every block of 32 elements is quantised by the
 //      OCP MX rule (scale 2^(floor(log2 max|x|) - 8) as a UE8M0 byte, codes
 //      E4M3 of x / scale) into the padded layout of mx_pos.
+#include <cuda_fp16.h>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "trace.cuh"
@@ -44,6 +46,24 @@ __device__ __forceinline__ uint4 kperm8(const uint4 v) {
     r.z = __byte_perm(v.y, v.w, 0x5410);
     r.w = __byte_perm(v.y, v.w, 0x7632);
     return r;
+}
+
+// Eight bf16 values to eight f16 values in the same order (round to
+// nearest even; exact for magnitudes in [2^-14, 65504]); magnitudes beyond
+// the f16 range saturate to +-65504 and set *range.
+__device__ __forceinline__ uint4 f16x8(const uint4 v, bool& range) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+        range |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+        lo = fminf(fmaxf(lo, -65504.f), 65504.f);
+        hi = fminf(fmaxf(hi, -65504.f), 65504.f);
+        const __half2 h = __floats2half2_rn(lo, hi);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Largest magnitude of eight bf16 values (exact, in fp32).
@@ -272,15 +292,19 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteParams p
                     if (v < vec_per_row) buf[u] = src[v];
                 }
 #pragma unroll
+                bool range = false;
+#pragma unroll
                 for (int u = 0; u < kRowVecUnroll; ++u) {
                     const int v = v0 + u * 32 + lane;
                     if (v < vec_per_row) {
                         if (p.mx_layout)
-                            dst_mx[static_cast<size_t>(v >> 3) * chunk_vecs + (v & 7)] = kperm8(buf[u]);
+                            dst_mx[static_cast<size_t>(v >> 3) * chunk_vecs + (v & 7)] =
+                                p.mx_f16 ? f16x8(buf[u], range) : kperm8(buf[u]);
                         else
                             dst[v] = buf[u];
                     }
                 }
+                if (range) atomicOr(p.status + kStatusWord, MOE_DEV_RANGE);
             }
         }
     }

@@ -125,6 +125,12 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  ::"r"(cluster_addr) : "memory");
 }
 
+// Stores v to a shared-memory word of any CTA of the cluster (address from
+// mapa_shared).
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t cluster_addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
 // Every thread of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
@@ -189,6 +195,21 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// 16-byte global -> shared copy that completes asynchronously (cached at L2
+// only); cp_async_commit closes a group of them, cp_async_wait<N> waits
+// until at most N of this thread's groups are still in flight.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later
@@ -426,6 +447,29 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t
          | (1u << 10)           // B = bf16
          | ((N >> 3) << 17)
          | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16: f16 A and B (both K-major), fp32 D.
+__host__ __device__ __forceinline__ uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+    return (1u << 4)            // D = f32
+         | ((N >> 3) << 17)
+         | ((M >> 4) << 24);    // A = B = f16 (format 0)
+}
+
+// Four bytes of E2M1 code pairs (element 2i in the low nibble of byte i) to
+// four f16x2 words, elements (0,1), (2,3), (4,5), (6,7), by the hardware
+// conversion (exact: every E2M1 value is an f16).
+__device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w) {
+    uint4 r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "r"(w));
+    return r;
 }
 
 // Instruction descriptor, kind::f8f6f4: E4M3 A and B (format 0, both

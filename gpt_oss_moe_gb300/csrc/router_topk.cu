@@ -147,7 +147,7 @@ __device__ __forceinline__ void topk_insert(float (&bv)[K], int (&be)[K], float 
 // order.  cand: [kComputeWarps][32][K] values then indices (scratch smem).
 template <int K>
 __device__ void topk_block(const RouterParams& p, const float* logits, int ls, const float* bias_s,
-                           float* cand, int t0, int* hist) {
+                           float* cand, int t0, int* hist, int* ids_s) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
     float* cv = cand;
@@ -204,6 +204,84 @@ __device__ void topk_block(const RouterParams& p, const float* logits, int ls, c
         // after it was counted, as a corrupted id would arrive
         const bool bad = (p.inject & 1) && t == 0 && s == 0 && p.E < kMaxExperts;
         p.topk_ids[static_cast<size_t>(t) * K + s] = bad ? p.E : be[s];
+        // (small batches: kept for the permutation made by the last CTA)
+        if (p.small_perm) ids_s[t * K + s] = bad ? p.E : be[s];
+        p.topk_w[static_cast<size_t>(t) * K + s] = ex[s] / denom;
+        atomicAdd(&hist[be[s]], 1);
+    }
+}
+
+// Top-K selection and softmax for a block of at most kThreads / 32 valid
+// tokens, one warp per token: lane l holds experts l, l + 32, ...; each of
+// the K rounds takes the warp's best remaining (logit descending, expert
+// ascending, NaN as the lowest value), so the selection, its order and the
+// softmax are those of topk_block.  With few tokens this is a few dozen
+// dependent instructions instead of a scan over every expert by one lane.
+template <int K>
+__device__ void topk_warp(const RouterParams& p, const float* logits, int ls, const float* bias_s,
+                          int t0, int n_valid, int* hist, int* ids_s) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= n_valid) return;
+    const int E = p.E;
+    constexpr int kPerLane = kMaxExperts / 32;
+    float v[kPerLane];
+    const float* row = logits + warp * ls;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+        const int e = lane + 32 * j;
+        float x = -INFINITY;                 // not an expert: never selected
+        if (e < E) {
+            x = row[e] + bias_s[e];
+            if (!(x == x)) x = -FLT_MAX;
+        }
+        v[j] = x;
+    }
+    float bv[K];
+    int be[K];
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+        // this lane's best remaining candidate (lower expert first on ties)
+        float mv = -INFINITY;
+        int me = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j)
+            if (v[j] > mv) {
+                mv = v[j];
+                me = lane + 32 * j;
+            }
+        // the warp's best
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, mv, d);
+            const int oe = __shfl_xor_sync(0xffffffffu, me, d);
+            if (ov > mv || (ov == mv && oe < me)) {
+                mv = ov;
+                me = oe;
+            }
+        }
+        bv[s] = mv;
+        be[s] = me;
+        // the winner's lane retires it
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j)
+            if (lane + 32 * j == me) v[j] = -INFINITY;
+    }
+    if (lane != 0) return;
+    const int t = t0 + warp;
+    float ex[K];
+    float denom = 0.f;
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+        ex[s] = expf(bv[s] - bv[0]);
+        denom += ex[s];
+    }
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+        // test fault (inject & 1): as in topk_block
+        const bool bad = (p.inject & 1) && t == 0 && s == 0 && p.E < kMaxExperts;
+        p.topk_ids[static_cast<size_t>(t) * K + s] = bad ? p.E : be[s];
+        // (small batches: kept for the permutation made by the last CTA)
+        if (p.small_perm) ids_s[t * K + s] = bad ? p.E : be[s];
         p.topk_w[static_cast<size_t>(t) * K + s] = ex[s] / denom;
         atomicAdd(&hist[be[s]], 1);
     }
@@ -215,8 +293,10 @@ __device__ void topk_block(const RouterParams& p, const float* logits, int ls, c
 // place each block's rows are left to the permutation kernel, whose CTAs
 // sum the earlier blocks' counts in parallel: done here by one CTA, that
 // scan took 14 us at T = 4096 and 37 us at E = 128, T = 8192.
+// ids_s: the routed ids of all tokens (small_perm; this block's already
+// there, the others' loaded here).
 __device__ void finish_routing(const RouterParams& p, int* total_s, int* offs_s, int* tcnt_s,
-                               int* toff_s) {
+                               int* toff_s, int* ids_s) {
     const int tid = threadIdx.x, warp = tid >> 5;
     const int E = p.E;
     if (p.nblocks > 1) {
@@ -261,6 +341,52 @@ __device__ void finish_routing(const RouterParams& p, int* total_s, int* offs_s,
         p.status[kNumTilesWord] = min(toff_s[E], p.max_tiles);
         p.status[kGridCounterWord] = 0;   // ready for the next call
     }
+    if (p.small_perm) {
+        // Small batches: the stable permutation is made here (the
+        // permutation kernel is not launched).  Rows are sorted by (expert,
+        // a): warp 0 ranks 32 assignments at a time against a running count
+        // per expert, as the permutation kernel does per token block.  The
+        // ids come from shared memory: this block's own (ids_s, kept by the
+        // top-k), the other token blocks' loaded from global memory by every
+        // thread at once (their writes were made visible before the ticket
+        // that chose this CTA).
+        int* running = tcnt_s;                 // free now
+        const int R = p.T * p.top_k;
+        // this CTA's token block (the last to finish, not necessarily the
+        // last block) holds assignments [own0, own1)
+        const int own0 = static_cast<int>(blockIdx.x) * kRouterTokens * p.top_k;
+        const int own1 = min(R, own0 + kRouterTokens * p.top_k);
+        for (int e = tid; e < E; e += kThreads) running[e] = 0;
+        for (int a = tid; a < R; a += kThreads)
+            if (a < own0 || a >= own1) ids_s[a] = __ldcg(p.topk_ids + a);
+        __syncthreads();
+        if (warp == 0) {
+            const int lane = tid & 31;
+            for (int ab = 0; ab < R; ab += 32) {
+                const int a = ab + lane;
+                const bool valid = a < R;
+                int e = valid ? ids_s[a] : -1;
+                const bool good = valid && e >= 0 && e < E;
+                if (valid && !good) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_EXPERT_ID);
+                if (!good) e = -1 - lane;       // unique per lane: never a real expert
+                const unsigned peers = __match_any_sync(0xffffffffu, e);
+                const int rank = __popc(peers & ((1u << lane) - 1u));
+                const int r0 = good ? running[e] : 0;
+                __syncwarp();
+                if (good && rank == 0) running[e] = r0 + __popc(peers);
+                __syncwarp();
+                int row = good ? offs_s[e] + r0 + rank : -1;
+                if (good && (row < 0 || row >= R)) {
+                    atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
+                    row = -1;
+                }
+                if (valid) {
+                    if (row >= 0) p.sorted_assign[row] = a;
+                    p.assign_row[a] = row;
+                }
+            }
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -282,6 +408,7 @@ __global__ void __launch_bounds__(kThreads)
     int* scan_c = scan_b + kMaxExperts;                                     // [257]
     volatile int* flag = scan_c + kMaxExperts + 1;                          // [4]
     float* bias_s = reinterpret_cast<float*>(scan_c + kMaxExperts + 5);      // [256]
+    int* ids_s = reinterpret_cast<int*>(bias_s + kMaxExperts);              // [256] (small_perm)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x, g = blockIdx.y, q = blockIdx.z;
@@ -301,12 +428,10 @@ __global__ void __launch_bounds__(kThreads)
     pdl_wait();
     pdl_launch_dependents();
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 1);
-    if (nc > S && S % kComputeWarps != 0) {
-        // a slot would be shared by two consumer warps: refuse (the host
-        // never asks for this)
-        if (tid == 0) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
-        return;
-    }
+    // a slot would be shared by two consumer warps: refuse (the host never
+    // asks for this); the CTA still takes part in its cluster's barriers
+    const bool bad_cfg = nc > S && S % kComputeWarps != 0;
+    if (bad_cfg && tid == 0) atomicOr(p.status + kStatusWord, MOE_DEV_BAD_TILE);
     for (int e = tid; e < kMaxExperts; e += kThreads) {
         hist[e] = 0;
         bias_s[e] = e < E ? __bfloat162float(p.br[e]) : 0.f;
@@ -316,7 +441,7 @@ __global__ void __launch_bounds__(kThreads)
             mbar_init(smem_u32(full + s), 1);
             mbar_init(smem_u32(empty + s), 1);
         }
-        flag[0] = 0;
+        flag[0] = bad_cfg ? 1 : 0;
         flag[1] = 0;
         flag[2] = 0;
         flag[3] = 0;
@@ -332,7 +457,9 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[m][j][r] = 0.f;
 
-    if (warp == kComputeWarps) {
+    if (bad_cfg) {
+        // nothing loaded or computed
+    } else if (warp == kComputeWarps) {
         // ---------------- producer: one lane issues every chunk's two loads
         if (lane == 0) {
             tma_prefetch_desc(&tmap_x);
@@ -406,8 +533,11 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 2);
     if (flag[0]) {
-        if (tid == 0) atomicOr(p.status + kStatusWord, MOE_DEV_WAIT_TIMEOUT);
-        return;   // block-uniform: flag read after the barrier
+        if (tid == 0 && !bad_cfg) atomicOr(p.status + kStatusWord, MOE_DEV_WAIT_TIMEOUT);
+        // block-uniform (flag read after the barrier); the K slices of a
+        // cluster must all reach its barriers, so they carry on (with
+        // meaningless logits: the status word reports the failure)
+        if (p.ksplit == 1) return;
     }
 
     // This slice's 32 x 32 block: the warp partials added in warp order.
@@ -425,46 +555,31 @@ __global__ void __launch_bounds__(kThreads)
 
     const int pair = b * p.egroups + g;
     if (p.ksplit > 1) {
-        // The last K slice of (b, g) adds all slices' blocks in slice order.
-        float* mine = p.partials + (static_cast<size_t>(pair) * p.ksplit + q) * kRouterTokens * kGroup;
-        for (int i = tid; i < kRouterTokens * kGroup; i += kThreads)
-            mine[i] = blk[(i / kGroup) * kPartStride + (i % kGroup)];
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const int ticket = atomicAdd(p.counters + pair, 1);
-            flag[1] = (ticket == p.ksplit - 1);
-            if (flag[1]) p.counters[pair] = 0;
+        // The K slices of (b, g) form one thread-block cluster.  Once every
+        // slice is done with its ring (first cluster barrier), slices 1..
+        // store their blocks into slot q of slice 0's ring region (remote
+        // shared-memory stores); after the second barrier slice 0 adds the
+        // slots in slice order and the others leave.  (Measured on GB300 at
+        // 20b T=1: the former merge through global memory and a ticket took
+        // ~4 us from the last slice's loads to the summed block.)
+        float* slots = reinterpret_cast<float*>(ring);   // [ksplit][32][32], slice 0
+        const uint32_t rank = cluster_ctarank();
+        cluster_sync();
+        if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 6);
+        if (rank != 0) {
+            const uint32_t dst = mapa_shared(smem_u32(slots + rank * kRouterTokens * kGroup), 0);
+            for (int i = tid; i < kRouterTokens * kGroup; i += kThreads)
+                st_shared_cluster_f32(dst + 4u * static_cast<uint32_t>(i),
+                                      blk[(i / kGroup) * kPartStride + (i % kGroup)]);
         }
-        __syncthreads();
-        if (!flag[1]) return;   // block-uniform
-        __threadfence();
-        const float* all = p.partials + static_cast<size_t>(pair) * p.ksplit * kRouterTokens * kGroup;
-        constexpr int kPerThread = (kRouterTokens * kGroup + kThreads - 1) / kThreads;   // 7
-        float sum[kPerThread];
-#pragma unroll
-        for (int r = 0; r < kPerThread; ++r) sum[r] = 0.f;
-        for (int s0 = 0; s0 < p.ksplit; s0 += 4) {
-            float v[4][kPerThread];
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-#pragma unroll
-                for (int r = 0; r < kPerThread; ++r) {
-                    const int i = tid + r * kThreads;
-                    v[s][r] = (s0 + s < p.ksplit && i < kRouterTokens * kGroup)
-                                  ? __ldcg(all + static_cast<size_t>(s0 + s) * kRouterTokens * kGroup + i)
-                                  : 0.f;
-                }
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-#pragma unroll
-                for (int r = 0; r < kPerThread; ++r)
-                    if (s0 + s < p.ksplit) sum[r] += v[s][r];
-        }
-#pragma unroll
-        for (int r = 0; r < kPerThread; ++r) {
-            const int i = tid + r * kThreads;
-            if (i < kRouterTokens * kGroup) blk[(i / kGroup) * kPartStride + (i % kGroup)] = sum[r];
+        cluster_sync();
+        if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 7);
+        if (rank != 0) return;   // CTA-uniform
+        for (int i = tid; i < kRouterTokens * kGroup; i += kThreads) {
+            const int row = i / kGroup, col = i - row * kGroup;
+            float v = blk[row * kPartStride + col];
+            for (int q2 = 1; q2 < p.ksplit; ++q2) v += slots[q2 * kRouterTokens * kGroup + i];
+            blk[row * kPartStride + col] = v;   // only this thread reads this slot
         }
         __syncthreads();
     }
@@ -515,15 +630,29 @@ __global__ void __launch_bounds__(kThreads)
 
     // Top-k + softmax, one lane per token (the partial buffer is free now).
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 3);
-    switch (p.top_k) {
-        case 1: topk_block<1>(p, logits, ls, bias_s, partial, t0, hist); break;
-        case 2: topk_block<2>(p, logits, ls, bias_s, partial, t0, hist); break;
-        case 3: topk_block<3>(p, logits, ls, bias_s, partial, t0, hist); break;
-        case 4: topk_block<4>(p, logits, ls, bias_s, partial, t0, hist); break;
-        case 5: topk_block<5>(p, logits, ls, bias_s, partial, t0, hist); break;
-        case 6: topk_block<6>(p, logits, ls, bias_s, partial, t0, hist); break;
-        case 7: topk_block<7>(p, logits, ls, bias_s, partial, t0, hist); break;
-        default: topk_block<8>(p, logits, ls, bias_s, partial, t0, hist); break;
+    const int n_valid = min(kRouterTokens, p.T - t0);
+    if (n_valid <= kThreads / 32) {
+        switch (p.top_k) {
+            case 1: topk_warp<1>(p, logits, ls, bias_s, t0, n_valid, hist, ids_s); break;
+            case 2: topk_warp<2>(p, logits, ls, bias_s, t0, n_valid, hist, ids_s); break;
+            case 3: topk_warp<3>(p, logits, ls, bias_s, t0, n_valid, hist, ids_s); break;
+            case 4: topk_warp<4>(p, logits, ls, bias_s, t0, n_valid, hist, ids_s); break;
+            case 5: topk_warp<5>(p, logits, ls, bias_s, t0, n_valid, hist, ids_s); break;
+            case 6: topk_warp<6>(p, logits, ls, bias_s, t0, n_valid, hist, ids_s); break;
+            case 7: topk_warp<7>(p, logits, ls, bias_s, t0, n_valid, hist, ids_s); break;
+            default: topk_warp<8>(p, logits, ls, bias_s, t0, n_valid, hist, ids_s); break;
+        }
+    } else {
+        switch (p.top_k) {
+            case 1: topk_block<1>(p, logits, ls, bias_s, partial, t0, hist, ids_s); break;
+            case 2: topk_block<2>(p, logits, ls, bias_s, partial, t0, hist, ids_s); break;
+            case 3: topk_block<3>(p, logits, ls, bias_s, partial, t0, hist, ids_s); break;
+            case 4: topk_block<4>(p, logits, ls, bias_s, partial, t0, hist, ids_s); break;
+            case 5: topk_block<5>(p, logits, ls, bias_s, partial, t0, hist, ids_s); break;
+            case 6: topk_block<6>(p, logits, ls, bias_s, partial, t0, hist, ids_s); break;
+            case 7: topk_block<7>(p, logits, ls, bias_s, partial, t0, hist, ids_s); break;
+            default: topk_block<8>(p, logits, ls, bias_s, partial, t0, hist, ids_s); break;
+        }
     }
     __syncthreads();
     for (int e = tid; e < E; e += kThreads) {
@@ -547,7 +676,7 @@ __global__ void __launch_bounds__(kThreads)
         __syncthreads();
     }
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 4);
-    finish_routing(p, hist, scan_a, scan_b, scan_c);
+    finish_routing(p, hist, scan_a, scan_b, scan_c, ids_s);
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, trace_cta, 5);
 }
 
@@ -564,7 +693,7 @@ size_t trace_copy_router(unsigned long long* dst, size_t cap) {
 size_t router_smem_bytes(int stages) {
     const size_t ring = static_cast<size_t>(stages) * kStageBytes;
     return 1024 + (ring > kLogitsBytes ? ring : kLogitsBytes) + kPartialBytes +
-           2 * kMaxStages * 8 + (5 * kMaxExperts + 8) * 4;
+           2 * kMaxStages * 8 + (6 * kMaxExperts + 8) * 4;
 }
 
 int router_max_stages() { return kMaxStages; }
@@ -573,6 +702,7 @@ int router_stage_multiple() { return kComputeWarps; }
 cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tx, const CUtensorMap* tw,
                           size_t smem, cudaStream_t s, bool pdl) {
     if (p.stages < 1 || p.stages > kMaxStages) return cudaErrorInvalidValue;
+    if (p.ksplit < 1 || p.ksplit > kMaxRouterSlices) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(router_topk_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
@@ -582,11 +712,23 @@ cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tx, const CU
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (p.ksplit > 1) {
+        // the K slices of one (token block, expert group) form a cluster
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = static_cast<unsigned>(p.ksplit);
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, router_topk_kernel, p, *tx, *tw);
 }
 

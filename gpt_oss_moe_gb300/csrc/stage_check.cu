@@ -4,6 +4,7 @@
 // magnitude checks after each stage behind an environment switch).  Off by
 // default; moe_api.cu launches one check after each stage when
 // MOE_CHECK_STAGES=1.
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "moe_internal.cuh"
@@ -17,6 +18,7 @@ constexpr int kThreads = 256;
 
 __device__ __forceinline__ float value_of(const void* buf, size_t i, int dtype) {
     if (dtype == 1) return static_cast<const float*>(buf)[i];
+    if (dtype == 3) return __half2float(static_cast<const __half*>(buf)[i]);
     if (dtype == 2) {
         __nv_fp8_e4m3 c;
         c.__x = static_cast<const uint8_t*>(buf)[i];

@@ -115,6 +115,11 @@ typedef struct {
                                         a NaN or an infinity */
 #define MOE_DEV_BOUNDS         0x10  /* an index check of a MOE_DEBUG_BOUNDS
                                         build failed (the access was skipped) */
+#define MOE_DEV_RANGE          0x20  /* MXFP4 weights, f16 mode: a scale byte
+                                        outside [104, 140] or an activation
+                                        beyond +-65504 was clamped; the
+                                        result is inexact (rerun with the
+                                        "mxfp4_f16" switch off) */
 
 /* Bytes of device workspace moe_route / moe_forward need for this shape
  * (0 for an invalid shape).  The workspace is scratch owned by the caller.
@@ -188,7 +193,7 @@ moe_status moe_forward_ep(const moe_shape* shape, int expert_start, int local_ex
 /* Size of the library-owned scratch array used by moe_forward_noalloc
  * (8 MiB per device that loads the library, held until the process exits).
  * A shape fits when moe_workspace_bytes(shape) <= this size; with
- * H = I = 2880 and top_k = 4 that is T <= 129 for E = 32 and T <= 121 for
+ * H = I = 2880 and top_k = 4 that is T <= 132 for E = 32 and T <= 131 for
  * E = 128. */
 #define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 
@@ -278,6 +283,17 @@ moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
  *                 is on, so query it after setting the switch (a workspace
  *                 sized without them is refused with MOE_ERR_WORKSPACE);
  *                 0 = fp32 atomics in the down projection (default);
+ *   "mxfp4_f16":  MOE_W_MXFP4 layers: 1 = the GEMMs run on f16 operands
+ *                 (the activations and h rounded to f16, the weights
+ *                 expanded by the hardware E2M1 conversion), exact for scale
+ *                 bytes in [104, 140] and activations within +-65504; a
+ *                 value outside is clamped and MOE_DEV_RANGE reported
+ *                 (default); 0 = bf16 operands, exact for every scale;
+ *   "small_path": 1 = batches of bf16 weights with T * top_k <= 256 (and
+ *                 T <= 64) skip the permutation kernel: the router's last
+ *                 block computes the permutation and the gate_up GEMM copies
+ *                 its token rows from `hidden` itself (default); 0 = always
+ *                 the permutation kernel and the gathered activation rows;
  *   "inject":     test faults that the device status word must report, as
  *                 a bit mask (0 = none, default): 1 = token 0's first
  *                 routed id is written as E (after it was counted), so the

@@ -219,9 +219,12 @@ def test_stage_checks_count_nonfinite_values_per_stage(moe):
     (nf0, m0), (nf1, m1), (nf2, m2) = res["stats"]
     assert nf0 == nf1 == nf2 == 0
     assert 0 < m0 < 10 and 0 < m1 < 56 and abs(m2 - res["max_out"]) <= 1e-6 * res["max_out"]
-    # the planted NaN shows from the first stage on, and sets its status bit
+    # the planted NaN shows from the first stage on, and sets its status bit;
+    # this batch (37 tokens, top-4, bf16) takes the small-batch path, whose
+    # first stage is the layer input itself (the gathered copies are not
+    # stored), so the NaN counts once
     assert res["nan_status"] & 0x8
-    assert res["nan_stats"][0][0] == 4          # the token's row, gathered for 4 experts
+    assert res["nan_stats"][0][0] == 1
 
 
 def test_nvtx_ranges_switch(moe):

@@ -404,16 +404,60 @@ def test_mxfp4_dequant_is_exact(moe, oracle_lib, synth_lib, T, scale_lo, scale_h
         w_gu=oracle_lib.dequant_mxfp4(Lq.w_gu, Lq.s_gu).to(torch.bfloat16).contiguous(),
         w_d=oracle_lib.dequant_mxfp4(Lq.w_d, Lq.s_d).to(torch.bfloat16).contiguous())
     # one K order in both paths: no K split (it would differ between the
-    # 4-k-block MXFP4 ring and the 1-k-block bf16 ring)
+    # 4-k-block MXFP4 ring and the 1-k-block bf16 ring); bf16 operands (the
+    # f16 mode rounds the activations and h to f16 instead)
     moe.moe_set_tuning("ksplit", 1)
+    moe.moe_set_tuning("mxfp4_f16", 0)
     try:
         iq, wq, oq, wsq = gpu_forward(moe, Lq)
         ib, wb, ob, wsb = gpu_forward(moe, Lb)
     finally:
         moe.moe_set_tuning("ksplit", 0)
+        moe.moe_set_tuning("mxfp4_f16", 1)
     assert moe.moe_get_device_status(wsq) == 0
     assert torch.equal(iq, ib) and torch.equal(wq, wb)
     assert torch.equal(oq, ob)
+
+
+@pytest.mark.parametrize("lo,hi,flag", [(104, 110, False), (134, 140, False), (103, 110, True),
+                                         (134, 141, True)])
+def test_mxfp4_f16_mode_scale_range(moe, oracle_lib, synth_lib, lo, hi, flag):
+    """The f16 mode expands E2M1 codes exactly for scale bytes 104..140 (its
+    operands then differ from the oracle's only by the rounding of the
+    activations and h to f16, well inside 2e-3 of the output's magnitude); a
+    scale byte outside is clamped and reported as MOE_DEV_RANGE, and the
+    bf16 mode computes the same layer exactly with no report."""
+    L = synth_lib.make_layer(E=4, T=40, H=320, I=192, top_k=2, seed=17 + lo + hi, wfmt="mxfp4",
+                             scale_lo=lo, scale_hi=hi, router_w_std=0.05)
+    if lo < 110:
+        # small scales: activations large enough that the products matter
+        L.x = (L.x.float() * 64).to(torch.bfloat16)
+    _, _, o_out = oracle_lib.forward(L)
+    ref = o_out.abs().max().item()
+    ids, w, out, ws = gpu_forward(moe, L)
+    status = moe.moe_get_device_status(ws)
+    if flag:
+        assert status == moe.MOE_DEV_RANGE
+    else:
+        assert status == 0
+        assert (out.cpu() - o_out).abs().max().item() <= 2e-3 * ref
+    moe.moe_set_tuning("mxfp4_f16", 0)
+    try:
+        ids, w, out, ws = gpu_forward(moe, L)
+    finally:
+        moe.moe_set_tuning("mxfp4_f16", 1)
+    assert moe.moe_get_device_status(ws) == 0
+    assert (out.cpu() - o_out).abs().max().item() <= 1e-2 * ref
+
+
+def test_mxfp4_f16_mode_activation_range(moe, oracle_lib, synth_lib):
+    """An activation beyond the f16 range is reported (MOE_DEV_RANGE)."""
+    L = synth_lib.make_layer(E=4, T=10, H=128, I=128, top_k=2, seed=23, wfmt="mxfp4",
+                             router_w_std=0.05)
+    L.x = L.x.clone()
+    L.x[2, 5] = 1e6
+    ids, w, out, ws = gpu_forward(moe, L)
+    assert moe.moe_get_device_status(ws) & moe.MOE_DEV_RANGE
 
 
 @pytest.mark.parametrize("ksplit", [1, 0])
@@ -659,3 +703,37 @@ def test_one_workspace_serves_successive_shapes(moe, synth_lib):
         assert moe.moe_get_device_status(big) == 0
         assert torch.equal(ids_a, ids_b) and torch.equal(w_a, w_b)
         assert (out_a - out_b).abs().max().item() <= 1e-5 * out_b.abs().max().item()
+
+
+# ------------------------------------------- small batches without a permutation kernel
+
+SMALL_PATH_CASES = [
+    # E, k, H, I, T     (bf16 weights, T * k <= 256 and T <= 64: the router
+    #                    permutes and gate_up gathers the token rows itself)
+    (32, 4, 2880, 2880, 1),
+    (32, 4, 2880, 2880, 16),
+    (128, 4, 2880, 2880, 3),
+    (8, 4, 320, 192, 37),        # weight-row tail, 48-row token tiles
+    (8, 1, 128, 128, 64),        # top-1, 64-row tiles (rows 32..63 of a tile)
+    (256, 8, 128, 128, 32),      # R = 256, most experts
+    (5, 3, 64, 64, 19),
+]
+
+
+@pytest.mark.parametrize("case", SMALL_PATH_CASES, ids=lambda c: "E{}k{}H{}I{}T{}".format(*c))
+def test_small_path_matches_the_permutation_kernel(moe, oracle_lib, synth_lib, case):
+    E, k, H, I, T = case
+    L = synth_lib.make_layer(E=E, T=T, H=H, I=I, top_k=k, seed=1500 + T + E, router_w_std=0.05)
+    dev = to_device(L)
+    runs = []
+    for mode in (1, 0):
+        moe.moe_set_tuning("small_path", mode)
+        try:
+            runs.append(gpu_forward(moe, L, dev=dev))
+        finally:
+            moe.moe_set_tuning("small_path", 1)
+    (i1, w1, o1, ws1), (i0, w0, o0, ws0) = runs
+    assert moe.moe_get_device_status(ws1) == 0 and moe.moe_get_device_status(ws0) == 0
+    assert torch.equal(i1, i0) and torch.equal(w1, w0)
+    assert (o1 - o0).abs().max().item() <= 1e-5 * o0.abs().max().item()
+    _check(moe, oracle_lib, L, dev=dev)
