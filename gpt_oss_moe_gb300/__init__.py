@@ -286,14 +286,15 @@ def moe_stage_stats(workspace: torch.Tensor):
 
 def moe_trace_read():
     """Phase timestamps of the last call (trace build only): a dict of
-    int64 tensors router [512, 8], permute [512, 8], gemm [2, 512, 8]."""
-    cap = 4 * 512 * 8
+    int64 tensors router [512, 8], permute [512, 8], gemm [2, 512, 8],
+    attn [2, 512, 8]."""
+    cap = 6 * 512 * 8
     buf = (ctypes.c_uint64 * cap)()
     n = ctypes.c_size_t(0)
     _check(lib().moe_trace_read(buf, cap, ctypes.byref(n)), "moe_trace_read")
     t = torch.tensor(list(buf[:n.value]), dtype=torch.int64)
     return {"router": t[:4096].view(512, 8), "permute": t[4096:8192].view(512, 8),
-            "gemm": t[8192:].view(2, 512, 8)}
+            "gemm": t[8192:16384].view(2, 512, 8), "attn": t[16384:].view(2, 512, 8)}
 
 
 def moe_clear_device_status(workspace: torch.Tensor, stream=None):

@@ -17,6 +17,8 @@
 // masked (its tile max is -inf: all keys in the future or slid out of the
 // window) leaves the row's state untouched -- the guard whose absence, with
 // a running max of -inf, turns exp(-inf - -inf) into NaN.
+#include <atomic>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "../../include/moe.h"
@@ -378,13 +380,49 @@ size_t attn_ws_bytes(const moe_attn_shape& s, int nsplit) {
     return rows * kD * sizeof(float) + 256 + rows * sizeof(float2);
 }
 
+// Prefill-sized calls run on the tcgen05 kernel (attention_tc.cu): at least
+// kTcMinTq queries (one 128-row block per query head keeps few SMs busy
+// below that, where the 64-row kernel with key splits does better).
+// "attn_tc" tuning: 0 = automatic, 1 = never, 2 = always.
+constexpr int kTcMinTq = 512;
+std::atomic<int> g_attn_tc{0};
+// hand-off waits of the tcgen05 kernel: 1 polling (mbarrier.test_wait),
+// 0 suspending (mbarrier.try_wait)
+std::atomic<int> g_attn_poll{1};
+
+bool attn_use_tc(const moe_attn_shape& s) {
+    const int mode = g_attn_tc.load();
+    return mode == 2 || (mode == 0 && s.Tq >= kTcMinTq);
+}
+
 }  // namespace
+
+size_t attention_tc_smem_bytes();
+cudaError_t launch_attention_tc(const moe_attn_shape& s, const void* q, const void* k,
+                                const void* v, const float* sinks, float* out, int32_t* status,
+                                PFN_cuTensorMapEncodeTiled_v12000 enc, int poll,
+                                cudaStream_t stream);
+
+int set_attn_tc_mode(int mode) {
+    if (mode < 0 || mode > 2) return MOE_ERR_ARG;
+    g_attn_tc.store(mode);
+    return MOE_OK;
+}
+
+int set_attn_poll(int mode) {
+    if (mode != 0 && mode != 1) return MOE_ERR_ARG;
+    g_attn_poll.store(mode);
+    return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
 
 extern "C" size_t moe_attention_workspace_bytes(const moe_attn_shape* shape) {
     if (!shape || !attn_shape_ok(*shape)) return 0;
+    // the tcgen05 kernel: a status word
+    if (attn_use_tc(*shape)) return 256;
     return attn_ws_bytes(*shape, attn_splits(*shape, sm_count()));
 }
 
@@ -400,6 +438,18 @@ extern "C" moe_status moe_attention_sinks(const moe_attn_shape* shape, const voi
     for (const void* ptr : {q, k, v, static_cast<const void*>(out)})
         if (reinterpret_cast<uintptr_t>(ptr) & 15) return MOE_ERR_ALIGN;
     if (reinterpret_cast<uintptr_t>(sinks) & 3) return MOE_ERR_ALIGN;
+    if (attn_use_tc(s)) {
+        // status word at the workspace's start, cleared for this call
+        if (!workspace || workspace_bytes < 256) return MOE_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 15) return MOE_ERR_ALIGN;
+        PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+        if (!enc) return MOE_ERR_CUDA;
+        int32_t* status = static_cast<int32_t*>(workspace);
+        if (cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
+        return launch_attention_tc(s, q, k, v, sinks, out, status, enc, g_attn_poll.load(),
+                                   stream) == cudaSuccess
+                   ? MOE_OK : MOE_ERR_CUDA;
+    }
     const int nsplit = attn_splits(s, sm_count());
     const size_t need = attn_ws_bytes(s, nsplit);
     if (need > 0 && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;

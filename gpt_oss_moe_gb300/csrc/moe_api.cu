@@ -69,6 +69,15 @@ moe_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     return MOE_OK;
 }
 
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    return encode_fn(&fn) == MOE_OK ? fn : nullptr;
+}
+
+namespace {
+
 // Every map uses the 128-byte swizzle: box inner extent 128 B (64 bf16
 // elements, or 128 MXFP4 code bytes = 4 k-blocks of one row).
 moe_status make_tmap_dt(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank,
@@ -143,6 +152,8 @@ std::atomic<int> g_inject{0};
 // 1: small bf16 batches skip the permutation kernel (the router permutes,
 // gate_up gathers token rows itself); 0: always the permutation kernel
 std::atomic<int> g_small_path{1};
+// 1: small-batch calls of at most 8 tokens route in one CTA (router_tiny)
+std::atomic<int> g_tiny_router{1};
 // 1: MXFP4 weights with bf16 activations run on f16 operands (hardware E2M1
 // conversion; exact for scale bytes in [104, 140] and activations within
 // +-65504, others reported as MOE_DEV_RANGE); 0: bf16 operands, exact for
@@ -383,7 +394,10 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     rp.sorted_assign = r.sorted_assign;
     rp.assign_row = reinterpret_cast<int32_t*>(ws + L.assign_row);
     rp.status = status;
-    {
+    if (small_perm && g_tiny_router.load() != 0 && router_tiny_fits(s.T, s.H, s.E)) {
+        NvtxRange nv("moe.router_tiny");
+        MOE_CUDA(launch_router_tiny(rp, hidden, router_w, stream, g_pdl.load() != 0));
+    } else {
         NvtxRange nv("moe.router_topk");
         MOE_CUDA(launch_router(rp, &tm_x, &tm_wr, router_smem_bytes(stages), stream,
                                g_pdl.load() != 0));
@@ -644,7 +658,7 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     // gathers its token rows from `hidden` (no permutation kernel, no x_perm
     // round trip; gate_up clears the output rows)
     const bool small = g_small_path.load() != 0 && !mxfp4 && !fp8 && !mx && !pair &&
-                       R <= kSmallPermRows && box <= 64 && stages > 4;
+                       R <= kSmallPermRows && s.T <= kSmallPathMaxT && box <= 64 && stages > 4;
     // deterministic combine: the ordered sum writes every output element,
     // so the output needs no clearing
     MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r,
@@ -867,7 +881,10 @@ moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count) {
     n += n2;
     const size_t n3 = trace_copy_gemm(o + n, cap - n);
     if (n3 == 0) return MOE_ERR_UNSUPPORTED;
-    *count = n + n3;
+    n += n3;
+    const size_t n4 = trace_copy_attn(o + n, cap - n);
+    if (n4 == 0) return MOE_ERR_UNSUPPORTED;
+    *count = n + n4;
     return MOE_OK;
 }
 
@@ -898,6 +915,13 @@ moe_status moe_set_tuning(const char* key, int value) {
     if (std::strcmp(key, "mxfp4_f16") == 0) {
         if (value != 0 && value != 1) return MOE_ERR_ARG;
         g_mxfp4_f16.store(value);
+        return MOE_OK;
+    }
+    if (std::strcmp(key, "attn_tc") == 0) return static_cast<moe_status>(set_attn_tc_mode(value));
+    if (std::strcmp(key, "attn_poll") == 0) return static_cast<moe_status>(set_attn_poll(value));
+    if (std::strcmp(key, "tiny_router") == 0) {
+        if (value != 0 && value != 1) return MOE_ERR_ARG;
+        g_tiny_router.store(value);
         return MOE_OK;
     }
     if (std::strcmp(key, "small_path") == 0) {

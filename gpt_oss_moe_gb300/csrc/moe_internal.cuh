@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -234,8 +235,12 @@ struct RouterParams {
     int32_t* assign_row;         // [T*k] (small_perm)
     int32_t* status;             // status region (status word, tile count, counter)
 };
-// Largest T * top_k whose permutation the router's last CTA makes itself.
+// Largest T * top_k whose permutation the router's last CTA makes itself,
+// and the largest T of that path (measured on gpt-oss-20b: 5-10 us faster
+// at T = 16 and 32, 4 us slower at T = 64, where gate_up cannot load
+// weights before the router, its immediate predecessor, has finished).
 constexpr int kSmallPermRows = 256;
+constexpr int kSmallPathMaxT = 32;
 
 // ------------------------------------------------------------ permutation (K2)
 
@@ -376,12 +381,23 @@ int router_max_stages();
 int router_stage_multiple();
 cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tmap_x,
                           const CUtensorMap* tmap_wr, size_t smem, cudaStream_t s, bool pdl);
+// Tiny batches (T <= 8, the small-batch path): one CTA routes everything.
+bool router_tiny_fits(int T, int H, int E);
+cudaError_t launch_router_tiny(const RouterParams& p, const void* x, const void* wr,
+                               cudaStream_t s, bool pdl);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s, bool pdl);
 // cg = 2 (bf16 only): CTA pairs (clusters of 2) on 256-row weight blocks,
 // each CTA holding token_box / 2 rows of every token tile; `grid` counts CTAs.
 cudaError_t launch_gemm(int epi, int wf, int cg, const GemmParams& p, const CUtensorMap* tmap_w,
                         const CUtensorMap* tmap_x, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
+// "attn_tc" tuning switch of the attention step (0 automatic, 1 never, 2
+// always the tcgen05 kernel); returns a moe_status value.
+int set_attn_tc_mode(int mode);
+int set_attn_poll(int mode);
+// cuTensorMapEncodeTiled from the driver (looked up once); null if absent.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 // Stage check: counts the non-finite elements of buf (n elements of type
 // dtype: 0 = bf16, 1 = fp32, 2 = E4M3 codes, 3 = f16) and their largest finite
 // magnitude into the stage's status words.

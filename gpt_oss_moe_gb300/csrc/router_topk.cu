@@ -295,8 +295,10 @@ __device__ void topk_warp(const RouterParams& p, const float* logits, int ls, co
 // scan took 14 us at T = 4096 and 37 us at E = 128, T = 8192.
 // ids_s: the routed ids of all tokens (small_perm; this block's already
 // there, the others' loaded here).
+template <int kNT = kThreads>
 __device__ void finish_routing(const RouterParams& p, int* total_s, int* offs_s, int* tcnt_s,
                                int* toff_s, int* ids_s) {
+    constexpr int kThreads = kNT;              // the calling kernel's block size
     const int tid = threadIdx.x, warp = tid >> 5;
     const int E = p.E;
     if (p.nblocks > 1) {
@@ -681,6 +683,164 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 }  // namespace
+
+// ------------------------------------------------------------ tiny batches
+//
+// Batches of at most kTinyTokens tokens: one CTA of kTinyThreads threads
+// does the whole routing.  Warp w computes the logits of experts 2w, 2w + 1,
+// then 2w + 32, ...: each lane loads its share of both experts' router rows
+// (16-byte loads, six per row in flight) and of the token rows (L1 hits)
+// and accumulates, per token, sequential fp32 sums over its share, which a
+// warp reduction then adds (a fixed order: the same logits every run; the
+// tensor-core router's order differs, as any two sum orders may, in the
+// last bits).  The top k (a warp per token), the expert offsets, the GEMM
+// tiles and the stable permutation follow in the same CTA, with no ticket or
+// merge between CTAs.  Measured on GB300 at gpt-oss-20b, T = 1: the
+// multi-CTA router spent ~11 us from its dependency wait to the finished
+// tables, mostly in hand-offs between its phases.
+constexpr int kTinyThreads = 512;
+constexpr int kTinyTokens = 8;
+
+__global__ void __launch_bounds__(kTinyThreads, 1)
+    router_tiny_kernel(const RouterParams p, const __nv_bfloat16* __restrict__ x,
+                       const __nv_bfloat16* __restrict__ wr) {
+    extern __shared__ uint8_t smem_raw[];
+    const int T = p.T, H = p.H, E = p.E;
+    float* logits = reinterpret_cast<float*>(smem_raw);                     // [T][E]
+    int* hist = reinterpret_cast<int*>(logits + kTinyTokens * kMaxExperts);  // [256]
+    int* scan_a = hist + kMaxExperts;                                        // [257]
+    int* scan_b = scan_a + kMaxExperts + 1;                                  // [256]
+    int* scan_c = scan_b + kMaxExperts;                                      // [257]
+    int* ids_s = scan_c + kMaxExperts + 1;                                   // [256]
+    float* bias_s = reinterpret_cast<float*>(ids_s + kMaxExperts);           // [256]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 0);
+    // inputs, workspace and counters may be written by the kernel before
+    pdl_wait();
+    pdl_launch_dependents();
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 1);
+
+    const int hv = H / 8;                                   // 16-byte vectors per row
+    const uint4* xg = reinterpret_cast<const uint4*>(x);    // (read through L1: every
+                                                            // warp reads all of it)
+    for (int e = tid; e < kMaxExperts; e += kTinyThreads) {
+        hist[e] = 0;
+        bias_s[e] = e < E ? __bfloat162float(p.br[e]) : 0.f;
+    }
+    __syncthreads();
+
+    // logits: warp w takes experts 2w, 2w + 1, then 2w + 2 * warps, ...
+    // (two rows' loads in flight per lane)
+    constexpr int kWarps = kTinyThreads / 32;
+    constexpr int kBatch = 6;                               // loads per row per lane
+    for (int e0 = 2 * warp; e0 < E; e0 += 2 * kWarps) {
+        float acc[2][kTinyTokens];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int t = 0; t < kTinyTokens; ++t) acc[r][t] = 0.f;
+        for (int v0 = 0; v0 < hv; v0 += 32 * kBatch) {
+            uint4 w[2][kBatch];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint4* wrow =
+                    reinterpret_cast<const uint4*>(wr) + static_cast<size_t>(e0 + r) * hv;
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int v = v0 + u * 32 + lane;
+                    w[r][u] = (v < hv && e0 + r < E) ? __ldg(wrow + v) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v >= hv) break;
+#pragma unroll
+                for (int t = 0; t < kTinyTokens; ++t) {
+                    if (t >= T) break;
+                    const uint4 xv = __ldg(xg + t * hv + v);
+                    const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const uint32_t ww[4] = {w[r][u].x, w[r][u].y, w[r][u].z, w[r][u].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            acc[r][t] = fmaf(__uint_as_float(ww[j] << 16),
+                                             __uint_as_float(xx[j] << 16), acc[r][t]);
+                            acc[r][t] = fmaf(__uint_as_float(ww[j] & 0xFFFF0000u),
+                                             __uint_as_float(xx[j] & 0xFFFF0000u), acc[r][t]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int t = 0; t < kTinyTokens; ++t) {
+                if (t >= T) break;
+                float v = acc[r][t];
+#pragma unroll
+                for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+                if (lane == 0 && e0 + r < E) logits[t * E + e0 + r] = v;
+            }
+    }
+    __syncthreads();
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 3);
+
+    switch (p.top_k) {
+        case 1: topk_warp<1>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+        case 2: topk_warp<2>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+        case 3: topk_warp<3>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+        case 4: topk_warp<4>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+        case 5: topk_warp<5>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+        case 6: topk_warp<6>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+        case 7: topk_warp<7>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+        default: topk_warp<8>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+    }
+    __syncthreads();
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 4);
+    finish_routing<kTinyThreads>(p, hist, scan_a, scan_b, scan_c, ids_s);
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 5);
+}
+
+size_t router_tiny_smem_bytes(int T, int H) {
+    (void)T;
+    (void)H;
+    return kTinyTokens * kMaxExperts * 4 + (6 * kMaxExperts + 2) * 4;
+}
+
+// (one SM reads the whole router matrix: with 128 experts, 737 KB at
+// H = 2880, the multi-block router measured faster at T = 8)
+bool router_tiny_fits(int T, int H, int E) {
+    return T >= 1 && T <= kTinyTokens && E <= 64 && H % 8 == 0 &&
+           router_tiny_smem_bytes(T, H) <= 96 * 1024;
+}
+
+cudaError_t launch_router_tiny(const RouterParams& p, const void* x, const void* wr,
+                               cudaStream_t s, bool pdl) {
+    if (!router_tiny_fits(p.T, p.H, p.E) || !p.small_perm || p.nblocks != 1)
+        return cudaErrorInvalidValue;
+    const size_t smem = router_tiny_smem_bytes(p.T, p.H);
+    cudaError_t err = cudaFuncSetAttribute(router_tiny_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kTinyThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, router_tiny_kernel, p,
+                              static_cast<const __nv_bfloat16*>(x),
+                              static_cast<const __nv_bfloat16*>(wr));
+}
 
 size_t router_stage_bytes() { return kStageBytes; }
 

@@ -47,5 +47,6 @@ constexpr int kTracePoints = 8;   // every kernel: 8 slots per CTA
 size_t trace_copy_router(unsigned long long* dst, size_t cap);
 size_t trace_copy_permute(unsigned long long* dst, size_t cap);
 size_t trace_copy_gemm(unsigned long long* dst, size_t cap);
+size_t trace_copy_attn(unsigned long long* dst, size_t cap);
 
 }  // namespace moe

@@ -254,13 +254,17 @@ moe_status moe_stage_stats(const void* workspace, int32_t nonfinite[3], float ma
  * them; other builds return MOE_ERR_UNSUPPORTED.  Each kernel records the
  * GPU's global timer (ns) at fixed points of each of its first 512 CTAs
  * (CTA i: the linear block index).  *count receives the number of uint64
- * values written to out (cap at least 16384): the router's [512][8] (entry,
+ * values written to out (cap at least 24576): the router's [512][8] (entry,
  * past the dependency wait, loads done, logits ready, routing tables
  * started, done), the permutation's [512][8] (entry, past the wait, ranks
  * done, exit), then the two GEMMs' [2][512][8] (gate_up, down: entry,
  * set-up done, weight loads issued before the wait, producer past the wait,
- * first MMA slot ready, last MMA commit, epilogue done, exit); unrecorded
- * points hold earlier values.  Synchronises with the device. */
+ * first MMA slot ready, last MMA commit, epilogue done, exit), then the
+ * tensor-core attention kernel's [2][512][8] (per CTA: entry, set-up done, Q
+ * landed, last scores issued, softmax done, exit; per key tile of the first
+ * CTA: scores issued, previous P.V issued, softmax has the scores, row
+ * maxima done, previous P.V accumulated, P written); unrecorded points hold
+ * earlier values.  Synchronises with the device. */
 moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
 
 /* Process-wide tuning switches for tests and benchmarks:
@@ -290,10 +294,21 @@ moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
  *                 value outside is clamped and MOE_DEV_RANGE reported
  *                 (default); 0 = bf16 operands, exact for every scale;
  *   "small_path": 1 = batches of bf16 weights with T * top_k <= 256 (and
- *                 T <= 64) skip the permutation kernel: the router's last
+ *                 T <= 32) skip the permutation kernel: the router's last
  *                 block computes the permutation and the gate_up GEMM copies
  *                 its token rows from `hidden` itself (default); 0 = always
  *                 the permutation kernel and the gathered activation rows;
+ *   "attn_tc":    moe_attention_sinks: 0 = calls of at least 512 queries
+ *                 run on the tensor-core (tcgen05) kernel, smaller ones on
+ *                 the 64-row kernel with key splits (default); 1 = never the
+ *                 tcgen05 kernel; 2 = always (query the workspace size
+ *                 after setting this switch);
+ *   "attn_poll":  hand-off waits of the tcgen05 attention kernel: 1 = poll
+ *                 (mbarrier.test_wait; default), 0 = suspending try_wait;
+ *   "tiny_router": 1 = small-batch calls of at most 8 tokens and at most
+ *                 64 experts compute the
+ *                 router, top-k and permutation in one thread block
+ *                 (default); 0 = the multi-block router;
  *   "inject":     test faults that the device status word must report, as
  *                 a bit mask (0 = none, default): 1 = token 0's first
  *                 routed id is written as E (after it was counted), so the
@@ -354,8 +369,10 @@ typedef struct {
 
 /* Bytes of scratch moe_attention_sinks needs for this shape on the current
  * device (0: none; small grids -- decode -- split the keys over several
- * CTAs and merge their partial results through it; 0 also for an invalid
- * shape). */
+ * CTAs and merge their partial results through it; calls served by the
+ * tensor-core kernel need 256 bytes, whose first word receives that call's
+ * device status bits, readable with moe_get_device_status; 0 also for an
+ * invalid shape). */
 size_t moe_attention_workspace_bytes(const moe_attn_shape* shape);
 
 /* workspace: device scratch of at least moe_attention_workspace_bytes

@@ -33,11 +33,19 @@ CASES = [
     (200, 3000, 8, 2, 0, "none"),        # split keys, no sink, four query blocks
     (100, 100, 12, 4, 0, "n"),           # 3 heads per KV head: one head per CTA
     (1, 500, 12, 4, 128, "n"),           # ... decode
+    (1024, 1024, 64, 8, 0, "n"),         # prefill-sized: several 128-query blocks
+    (1024, 1024, 64, 8, 128, "n"),       # ... sliding: tiles before the window skipped
+    (600, 4096, 8, 1, 0, "none"),        # queries at the end of a longer cache
 ]
 
+# "attn_tc": 1 = the 64-row mma.sync kernel (with key splits), 2 = the
+# tcgen05 kernel (128-query blocks; TMEM scores, P back through TMEM)
+MODES = [1, 2]
 
+
+@pytest.mark.parametrize("mode", MODES, ids=["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "Tq{}Tkv{}Hq{}Hkv{}W{}{}".format(*c))
-def test_attention_sinks_matches_oracle(moe, oracle_lib, synth_lib, case):
+def test_attention_sinks_matches_oracle(moe, oracle_lib, synth_lib, case, mode):
     Tq, Tkv, Hq, Hkv, W, sk = case
     a = synth_lib.make_attention(Tkv, Tkv, Hq=Hq, Hkv=Hkv, D=64, seed=Tq + Tkv + W)
     q = a["q"][Tkv - Tq:]
@@ -47,8 +55,18 @@ def test_attention_sinks_matches_oracle(moe, oracle_lib, synth_lib, case):
     elif sk == "big":
         sinks = torch.full_like(sinks, 20.0)
     ref = oracle_lib.attention_sinks(q, a["k"], a["v"], sinks, window=W)
-    out = moe.attention_sinks(q.cuda(), a["k"].cuda(), a["v"].cuda(), sinks.cuda(), window=W)
-    torch.cuda.synchronize()
+    moe.moe_set_tuning("attn_tc", mode)
+    try:
+        ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+        if mode == 2:
+            ws = torch.full((256,), 0x55, dtype=torch.uint8, device="cuda")   # cleared by the call
+        out = moe.attention_sinks(q.cuda(), a["k"].cuda(), a["v"].cuda(), sinks.cuda(), window=W,
+                                  workspace=ws if mode == 2 else None)
+        torch.cuda.synchronize()
+        if mode == 2:
+            assert moe.moe_get_device_status(ws) == 0
+    finally:
+        moe.moe_set_tuning("attn_tc", 0)
     got = out.cpu()
     assert torch.isfinite(got).all()
     err = (got - ref).abs().max().item()

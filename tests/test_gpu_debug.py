@@ -190,13 +190,22 @@ _, _, out2, ws2 = gpu_forward(moe, L2)
 _, _, o2 = oracle.forward(L2)
 res["status2"] = moe.moe_get_device_status(ws2)
 res["err2"] = (out2.cpu() - o2).abs().max().item() / o2.abs().max().item()
-# a NaN in one activation: the first stage's check must see it
+# a NaN in one activation: the first stage's check must see it (in the
+# gathered rows of the permutation path: the token's four copies; in the
+# layer input for the small-batch path, which stores no copies: once)
 if os.environ.get("MOE_CHECK_STAGES") == "1":
     L.x = L.x.clone(); L.x[5, 7] = float("nan")
     dev["x"] = L.x.cuda()
-    _, _, out3, ws3 = gpu_forward(moe, L, dev=dev)
-    res["nan_status"] = moe.moe_get_device_status(ws3)
-    res["nan_stats"] = moe.moe_stage_stats(ws3)
+    for small in (0, 1):
+        moe.moe_set_tuning("small_path", small)
+        L8 = synth.make_layer(E=8, T=24, H=320, I=192, top_k=4, seed=1400, router_w_std=0.05)
+        LL = L if small == 0 else L8
+        if small:
+            LL.x = LL.x.clone(); LL.x[5, 7] = float("nan")
+        _, _, out3, ws3 = gpu_forward(moe, LL)
+        res[f"nan_status{{small}}"] = moe.moe_get_device_status(ws3)
+        res[f"nan_stats{{small}}"] = moe.moe_stage_stats(ws3)
+    moe.moe_set_tuning("small_path", 1)
 print("RESULT " + json.dumps(res))
 '''
 
@@ -219,12 +228,10 @@ def test_stage_checks_count_nonfinite_values_per_stage(moe):
     (nf0, m0), (nf1, m1), (nf2, m2) = res["stats"]
     assert nf0 == nf1 == nf2 == 0
     assert 0 < m0 < 10 and 0 < m1 < 56 and abs(m2 - res["max_out"]) <= 1e-6 * res["max_out"]
-    # the planted NaN shows from the first stage on, and sets its status bit;
-    # this batch (37 tokens, top-4, bf16) takes the small-batch path, whose
-    # first stage is the layer input itself (the gathered copies are not
-    # stored), so the NaN counts once
-    assert res["nan_status"] & 0x8
-    assert res["nan_stats"][0][0] == 1
+    # the planted NaN shows from the first stage on, and sets its status bit
+    assert res["nan_status0"] & 0x8 and res["nan_status1"] & 0x8
+    assert res["nan_stats0"][0][0] == 4      # the token's row, gathered for 4 experts
+    assert res["nan_stats1"][0][0] == 1      # the layer input (small batches)
 
 
 def test_nvtx_ranges_switch(moe):
