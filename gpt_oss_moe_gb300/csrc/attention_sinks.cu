@@ -386,9 +386,10 @@ size_t attn_ws_bytes(const moe_attn_shape& s, int nsplit) {
 // "attn_tc" tuning: 0 = automatic, 1 = never, 2 = always.
 constexpr int kTcMinTq = 512;
 std::atomic<int> g_attn_tc{0};
-// hand-off waits of the tcgen05 kernel: 1 polling (mbarrier.test_wait),
-// 0 suspending (mbarrier.try_wait)
-std::atomic<int> g_attn_poll{1};
+// softmax hand-off waits of the tcgen05 kernel: 1 polling
+// (mbarrier.test_wait), 0 suspending (mbarrier.try_wait; measured faster:
+// a polling warp takes issue slots from the other softmax group)
+std::atomic<int> g_attn_poll{0};
 
 bool attn_use_tc(const moe_attn_shape& s) {
     const int mode = g_attn_tc.load();

@@ -176,8 +176,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     (void)tcta;
     (void)ttile;
     if (threadIdx.x == 0) MOE_TRACE_POINT(g_trace_attn, 0, tcta, 0);
-    // query blocks with the most keys (the last, under causality) first
-    const int qb = static_cast<int>(gridDim.x - 1 - blockIdx.x), h = blockIdx.y;
+    // blocks start in linear order (x fastest): all heads of the query block
+    // with the most keys (the last, under causality) first, then the next
+    const int qb = static_cast<int>(gridDim.y - 1 - blockIdx.y), h = blockIdx.x;
     const int kvh = h / (p.Hq / p.Hkv);
     const int q0 = qb * kTcBq;                                   // first query row
     const int pos0 = p.q_start + q0;                             // its position
@@ -274,8 +275,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t idesc_s = idesc_bf16_f32(kTcBq, kTcBk);
         const uint32_t idesc_o = idesc_bf16_f32(kTcBq, kTcD) | (1u << 16);   // B MN-major
         const uint64_t qd = smem_desc_sw128(smem_u32(q_s));
+        // (the issuer's waits always suspend: a polling warp takes issue
+        // slots from the softmax warps that share its scheduler)
         const auto wwait = [&](uint64_t* bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, await(bar, parity));
+            return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, flags));
         };
         bool ok = wwait(q_full, 0);
         if (lane == 0) MOE_TRACE_POINT(g_trace_attn, 0, tcta, 2);
@@ -388,9 +391,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // the window, before Tkv)
                 const int hi = min(pos + 1, p.Tkv) - key0;
                 const int lo = p.window > 0 ? pos - p.window + 1 - key0 : 0;
+                if (p.window == 0) {           // (one compare per key)
 #pragma unroll
-                for (int i = 0; i < kTcBk; ++i)
-                    if (i < lo || i >= hi) sr[i >> 4][i & 15] = __float_as_uint(-INFINITY);
+                    for (int i = 0; i < kTcBk; ++i)
+                        if (i >= hi) sr[i >> 4][i & 15] = __float_as_uint(-INFINITY);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kTcBk; ++i)
+                        if (i < lo || i >= hi) sr[i >> 4][i & 15] = __float_as_uint(-INFINITY);
+                }
             }
 #pragma unroll
             for (int i = 0; i < kTcBk; i += 2)
@@ -577,7 +586,9 @@ cudaError_t launch_attention_tc(const moe_attn_shape& s, const void* q, const vo
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    const dim3 grid((s.Tq + kTcBq - 1) / kTcBq, s.Hq);
+    const int n_qb = (s.Tq + kTcBq - 1) / kTcBq;
+    if (n_qb > 65535) return cudaErrorInvalidConfiguration;   // grid y limit
+    const dim3 grid(s.Hq, n_qb);
     attention_tc_kernel<<<grid, kTcThreads, smem, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }

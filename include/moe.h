@@ -303,8 +303,9 @@ moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
  *                 the 64-row kernel with key splits (default); 1 = never the
  *                 tcgen05 kernel; 2 = always (query the workspace size
  *                 after setting this switch);
- *   "attn_poll":  hand-off waits of the tcgen05 attention kernel: 1 = poll
- *                 (mbarrier.test_wait; default), 0 = suspending try_wait;
+ *   "attn_poll":  softmax hand-off waits of the tcgen05 attention kernel:
+ *                 0 = suspending try_wait (default), 1 = poll
+ *                 (mbarrier.test_wait);
  *   "tiny_router": 1 = small-batch calls of at most 8 tokens and at most
  *                 64 experts compute the
  *                 router, top-k and permutation in one thread block

@@ -39,11 +39,13 @@ CASES = [
 ]
 
 # "attn_tc": 1 = the 64-row mma.sync kernel (with key splits), 2 = the
-# tcgen05 kernel (128-query blocks; TMEM scores, P back through TMEM)
-MODES = [1, 2]
+# tcgen05 kernel (128-query blocks; TMEM scores, P back through TMEM) with
+# suspending hand-off waits (the default), 3 = the tcgen05 kernel with
+# polling waits ("attn_poll" 1)
+MODES = [1, 2, 3]
 
 
-@pytest.mark.parametrize("mode", MODES, ids=["mma_sync", "tcgen05"])
+@pytest.mark.parametrize("mode", MODES, ids=["mma_sync", "tcgen05", "tcgen05_poll"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "Tq{}Tkv{}Hq{}Hkv{}W{}{}".format(*c))
 def test_attention_sinks_matches_oracle(moe, oracle_lib, synth_lib, case, mode):
     Tq, Tkv, Hq, Hkv, W, sk = case
@@ -55,18 +57,21 @@ def test_attention_sinks_matches_oracle(moe, oracle_lib, synth_lib, case, mode):
     elif sk == "big":
         sinks = torch.full_like(sinks, 20.0)
     ref = oracle_lib.attention_sinks(q, a["k"], a["v"], sinks, window=W)
-    moe.moe_set_tuning("attn_tc", mode)
+    tc = mode >= 2
+    moe.moe_set_tuning("attn_tc", 2 if tc else 1)
+    moe.moe_set_tuning("attn_poll", 1 if mode == 3 else 0)
     try:
         ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
-        if mode == 2:
+        if tc:
             ws = torch.full((256,), 0x55, dtype=torch.uint8, device="cuda")   # cleared by the call
         out = moe.attention_sinks(q.cuda(), a["k"].cuda(), a["v"].cuda(), sinks.cuda(), window=W,
-                                  workspace=ws if mode == 2 else None)
+                                  workspace=ws if tc else None)
         torch.cuda.synchronize()
-        if mode == 2:
+        if tc:
             assert moe.moe_get_device_status(ws) == 0
     finally:
         moe.moe_set_tuning("attn_tc", 0)
+        moe.moe_set_tuning("attn_poll", 0)
     got = out.cpu()
     assert torch.isfinite(got).all()
     err = (got - ref).abs().max().item()
