@@ -396,6 +396,50 @@ def measure(moe, layer, args, dist, workload):
     return m, dev, step, out, ids
 
 
+def measure_attention(moe, T=4096, reps=30):
+    """The adjacent step of a gpt-oss block, attention with sinks at prefill
+    (64 query / 8 KV heads, D = 64, bf16 in, fp32 out), full and 128-key
+    sliding-window layers: each launch timed alone with CUDA events on the
+    launching stream, an L2 flush (a 256 MB write) between launches."""
+    import synth
+    _, tf_burst, _, pkind = peaks()
+    a = synth.make_attention(T, T, Hq=64, Hkv=8, D=64, seed=1)
+    q, k, v, s = (a[n].cuda() for n in ("q", "k", "v", "sinks"))
+    out = torch.empty((T, 64, 64), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    res = {"workload": f"gpt-oss attention with sinks, prefill T={T}, 64 query / 8 KV heads, "
+                       "D=64, bf16 q/k/v, fp32 out, seed 1",
+           "timing": f"CUDA events per launch, mean of {reps} after 3 warm-up launches, "
+                     "L2 flushed (256 MB write) before each",
+           "peak": tf_burst, "unit": "TFLOP/s",
+           "peak_source": f"MEASURED_PEAKS.json ({pkind}, burst bf16 GEMM rate)"}
+    for name, W in (("full", 0), ("window128", 128)):
+        keys = sum(min(i + 1, W) if W else i + 1 for i in range(T))
+        flops = 4 * 64 * 64 * keys
+        for _ in range(3):
+            moe.attention_sinks(q, k, v, s, out=out, window=W, workspace=ws)
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(reps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            moe.attention_sinks(q, k, v, s, out=out, window=W, workspace=ws)
+            e1.record()
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+        ms = tot / reps
+        if moe.moe_get_device_status(ws) != 0:
+            raise RuntimeError("attention device status non-zero")
+        tf = flops / (ms * 1e-3) / 1e12
+        res[name] = {"ms": ms, "algorithmic_flops": flops, "achieved": tf,
+                     "frac": tf / tf_burst}
+    del flush
+    return res
+
+
 def oracle_parity(layer, out, ids, n_tokens, threads=0):
     """The oracle on the first n tokens (timed) and its agreement with the
     GPU's last step on those tokens; near ties counted over all tokens."""
@@ -448,6 +492,8 @@ def main():
     ap.add_argument("--prefill-T", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-attention", action="store_true",
+                    help="skip the attention-with-sinks figures")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args()
@@ -519,6 +565,11 @@ def main():
         rec["gpu_launches"] += pm["gpu_launches"]
         prefill_out, prefill_ids = pout.cpu(), pids.cpu()
         del pdev
+
+    # The attention half of a gpt-oss block at prefill (outside the layer's
+    # timed region and its launch count).
+    if not args.no_attention:
+        rec["attention"] = measure_attention(moe)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, dt, cores = cpu_oracle_rate(layer, args.cpu_budget)
