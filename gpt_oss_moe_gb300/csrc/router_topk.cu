@@ -698,15 +698,47 @@ __global__ void __launch_bounds__(kThreads)
 // merge between CTAs.  Measured on GB300 at gpt-oss-20b, T = 1: the
 // multi-CTA router spent ~11 us from its dependency wait to the finished
 // tables, mostly in hand-offs between its phases.
+//
+// The token rows are copied to shared memory first, by every thread at once
+// (read in the dot-product loop, each load waited for in turn, they cost
+// ~5 us of dependent L2 round trips at T = 1).  When the router matrix also
+// fits (gpt-oss-20b: 32 x 2880 bf16, 184 KB) it is copied there by bulk
+// copies issued before the dependency wait, so its load overlaps the kernel
+// before this one (the weights are not written by it).
 constexpr int kTinyThreads = 512;
 constexpr int kTinyTokens = 8;
+constexpr size_t kTinySmemMax = 220 * 1024;
+
+// Rows in shared memory are H * 2 + 16 bytes apart, so that the eight rows
+// an ldmatrix reads at one column fall in different banks.
+size_t router_tiny_row_bytes(int H) { return static_cast<size_t>(H) * 2 + 16; }
+size_t router_tiny_base_bytes() {
+    return kTinyTokens * kMaxExperts * 4 + (6 * kMaxExperts + 2) * 4;
+}
+// the token rows and one zero row
+size_t router_tiny_x_bytes(int T, int H) { return static_cast<size_t>(T + 1) * router_tiny_row_bytes(H); }
+// the warps' partial logits [16 warps][64 experts][8 tokens] fp32 (they
+// alias the staged matrix once it has been read, when it is large enough)
+constexpr size_t kTinyRedBytes = 16 * 64 * kTinyTokens * 4;
+// bytes of the staged router matrix (0: read from global memory)
+size_t router_tiny_stage_bytes(int T, int H, int E) {
+    const size_t b = static_cast<size_t>(E) * router_tiny_row_bytes(H);
+    const size_t red = b >= kTinyRedBytes ? 0 : kTinyRedBytes;
+    return (H % 16 == 0 &&
+            b + red + router_tiny_x_bytes(T, H) + router_tiny_base_bytes() <= kTinySmemMax)
+               ? b + red : 0;
+}
 
 __global__ void __launch_bounds__(kTinyThreads, 1)
     router_tiny_kernel(const RouterParams p, const __nv_bfloat16* __restrict__ x,
-                       const __nv_bfloat16* __restrict__ wr) {
-    extern __shared__ uint8_t smem_raw[];
+                       const __nv_bfloat16* __restrict__ wr, uint32_t wstage) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t wbar;
     const int T = p.T, H = p.H, E = p.E;
-    float* logits = reinterpret_cast<float*>(smem_raw);                     // [T][E]
+    const uint32_t rs = static_cast<uint32_t>(H) * 2u + 16u;               // padded row bytes
+    uint8_t* w_s = smem_raw;                                                // [E][rs], staged
+    uint8_t* x_s = smem_raw + wstage;                                       // [T + 1][rs]
+    float* logits = reinterpret_cast<float*>(x_s + static_cast<size_t>(T + 1) * rs);
     int* hist = reinterpret_cast<int*>(logits + kTinyTokens * kMaxExperts);  // [256]
     int* scan_a = hist + kMaxExperts;                                        // [257]
     int* scan_b = scan_a + kMaxExperts + 1;                                  // [256]
@@ -716,65 +748,148 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 0);
-    // inputs, workspace and counters may be written by the kernel before
+    if (wstage && tid == 0) {
+        // the router matrix, one bulk copy per expert row (16-byte multiples)
+        mbar_init(smem_u32(&wbar), 1);
+        mbar_fence_init();
+        const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
+        mbar_arrive_expect_tx(smem_u32(&wbar), row_bytes * static_cast<uint32_t>(E));
+        for (int e = 0; e < E; ++e)
+            bulk_load(smem_u32(w_s) + static_cast<uint32_t>(e) * rs,
+                      wr + static_cast<size_t>(e) * H, row_bytes, smem_u32(&wbar));
+    }
+    // token rows, workspace and counters may be written by the kernel before
     pdl_wait();
     pdl_launch_dependents();
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 1);
 
     const int hv = H / 8;                                   // 16-byte vectors per row
-    const uint4* xg = reinterpret_cast<const uint4*>(x);    // (read through L1: every
-                                                            // warp reads all of it)
+    const uint4* xg = reinterpret_cast<const uint4*>(x);
     for (int e = tid; e < kMaxExperts; e += kTinyThreads) {
         hist[e] = 0;
         bias_s[e] = e < E ? __bfloat162float(p.br[e]) : 0.f;
     }
+    // token rows t < T, then a zero row (the operand rows past T or E)
+    for (int i = tid; i < (T + 1) * hv; i += kTinyThreads) {
+        const int t = i / hv, v = i - t * hv;
+        *reinterpret_cast<uint4*>(x_s + t * rs + v * 16) =
+            t < T ? __ldg(xg + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
     __syncthreads();
-
-    // logits: warp w takes experts 2w, 2w + 1, then 2w + 2 * warps, ...
-    // (two rows' loads in flight per lane)
+    // the staged matrix has landed (a bounded wait; if it gives up, the
+    // logits are computed from global memory instead and the status word
+    // reports the timeout)
+    bool staged = wstage != 0;
+    if (staged) {
+        staged = __syncthreads_and(mbar_wait(smem_u32(&wbar), 0, nullptr) ? 1 : 0) != 0;
+        if (!staged && tid == 0) atomicOr(p.status, MOE_DEV_WAIT_TIMEOUT);
+    }
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 2);
     constexpr int kWarps = kTinyThreads / 32;
-    constexpr int kBatch = 6;                               // loads per row per lane
+    if (staged) {
+        // logits on the tensor cores: D[expert][token] += W[expert][k] x[token][k]
+        // (mma.sync m16n8k16, bf16 in, fp32 accumulation).  Warp w takes
+        // the 16-wide K steps w, w + 16, ... for every 16-expert tile; the
+        // warps' partial tiles are then added in warp order.
+        const int nmt = (E + 15) / 16;                      // <= 4
+        const int nks = H / 16;
+        const uint8_t* zrow = x_s + static_cast<size_t>(T) * rs;
+        float d[4][4];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[mt][i] = 0.f;
+        // this lane's ldmatrix rows: B (token lane % 8, k half (lane / 8) % 2),
+        // A (expert 16 mt + lane % 16, k half lane / 16)
+        const int bn = lane & 7, bk = (lane >> 3) & 1;
+        const uint32_t b_row = smem_u32(bn < T ? x_s + static_cast<size_t>(bn) * rs : zrow) + 16u * bk;
+        uint32_t a_row[4];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            const int e = 16 * mt + (lane & 15);
+            a_row[mt] = smem_u32(e < E ? w_s + static_cast<size_t>(e) * rs : zrow) + 16u * (lane >> 4);
+        }
+        for (int ks = warp; ks < nks; ks += kWarps) {
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(b_row + 32u * ks, b0, b1, b2, b3);   // (b2, b3: lanes 16-31's rows, unused)
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                if (mt >= nmt) break;
+                uint32_t a[4];
+                ldmatrix_x4(a_row[mt] + 32u * ks, a[0], a[1], a[2], a[3]);
+                mma_bf16_16816(d[mt], a, b0, b1);
+            }
+        }
+        __syncthreads();                                    // every warp is done with w_s
+        // partials [warp][expert 0..63][token 0..7]
+        float* red = reinterpret_cast<float*>(w_s);
+        const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            if (mt >= nmt) break;
+            float* rw = red + (warp * 64 + 16 * mt) * kTinyTokens;
+            rw[g * kTinyTokens + 2 * q] = d[mt][0];
+            rw[g * kTinyTokens + 2 * q + 1] = d[mt][1];
+            rw[(g + 8) * kTinyTokens + 2 * q] = d[mt][2];
+            rw[(g + 8) * kTinyTokens + 2 * q + 1] = d[mt][3];
+        }
+        __syncthreads();
+        for (int i = tid; i < E * T; i += kTinyThreads) {
+            const int t = i / E, e = i - t * E;
+            float v = 0.f;
+#pragma unroll 4
+            for (int w = 0; w < kWarps; ++w) v += red[(w * 64 + e) * kTinyTokens + t];
+            logits[t * E + e] = v;
+        }
+    } else {
+    const uint4* wbase = reinterpret_cast<const uint4*>(wr);
+
+    // logits from global memory: warp w takes experts 2w, 2w + 1, then
+    // 2w + 2 * warps, ...  Lane l sums vectors l, l + 32, ... of both rows:
+    // every load of a row pass is issued before the first multiply
+    // (predicated, no early exit).
+    constexpr int kBatch = 6;                               // loads per row per lane and pass
+    const auto row_pass = [&](const uint4* w0row, const uint4* w1row, int v0, float (&acc)[2][kTinyTokens]) {
+        uint4 w[2][kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = v0 + u * 32 + lane;
+            const bool in = v < hv;
+            w[0][u] = in ? w0row[v] : make_uint4(0u, 0u, 0u, 0u);
+            w[1][u] = in && w1row ? w1row[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int t = 0; t < kTinyTokens; ++t) {
+            if (t >= T) break;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int v = v0 + u * 32 + lane;
+                const uint4 xv = v < hv ? *reinterpret_cast<const uint4*>(x_s + t * rs + v * 16)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t ww[4] = {w[r][u].x, w[r][u].y, w[r][u].z, w[r][u].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[r][t] = fmaf(__uint_as_float(ww[q] << 16),
+                                         __uint_as_float(xx[q] << 16), acc[r][t]);
+                        acc[r][t] = fmaf(__uint_as_float(ww[q] & 0xFFFF0000u),
+                                         __uint_as_float(xx[q] & 0xFFFF0000u), acc[r][t]);
+                    }
+                }
+            }
+        }
+    };
     for (int e0 = 2 * warp; e0 < E; e0 += 2 * kWarps) {
         float acc[2][kTinyTokens];
 #pragma unroll
         for (int r = 0; r < 2; ++r)
 #pragma unroll
             for (int t = 0; t < kTinyTokens; ++t) acc[r][t] = 0.f;
-        for (int v0 = 0; v0 < hv; v0 += 32 * kBatch) {
-            uint4 w[2][kBatch];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const uint4* wrow =
-                    reinterpret_cast<const uint4*>(wr) + static_cast<size_t>(e0 + r) * hv;
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int v = v0 + u * 32 + lane;
-                    w[r][u] = (v < hv && e0 + r < E) ? __ldg(wrow + v) : make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int v = v0 + u * 32 + lane;
-                if (v >= hv) break;
-#pragma unroll
-                for (int t = 0; t < kTinyTokens; ++t) {
-                    if (t >= T) break;
-                    const uint4 xv = __ldg(xg + t * hv + v);
-                    const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const uint32_t ww[4] = {w[r][u].x, w[r][u].y, w[r][u].z, w[r][u].w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            acc[r][t] = fmaf(__uint_as_float(ww[j] << 16),
-                                             __uint_as_float(xx[j] << 16), acc[r][t]);
-                            acc[r][t] = fmaf(__uint_as_float(ww[j] & 0xFFFF0000u),
-                                             __uint_as_float(xx[j] & 0xFFFF0000u), acc[r][t]);
-                        }
-                    }
-                }
-            }
-        }
+        const uint4* w0row = wbase + static_cast<size_t>(e0) * hv;
+        const uint4* w1row = e0 + 1 < E ? w0row + hv : nullptr;
+        for (int v0 = 0; v0 < hv; v0 += 32 * kBatch) row_pass(w0row, w1row, v0, acc);
 #pragma unroll
         for (int r = 0; r < 2; ++r)
 #pragma unroll
@@ -786,6 +901,8 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
                 if (lane == 0 && e0 + r < E) logits[t * E + e0 + r] = v;
             }
     }
+    }
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 6);
     __syncthreads();
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 3);
 
@@ -805,24 +922,23 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 5);
 }
 
-size_t router_tiny_smem_bytes(int T, int H) {
-    (void)T;
-    (void)H;
-    return kTinyTokens * kMaxExperts * 4 + (6 * kMaxExperts + 2) * 4;
+size_t router_tiny_smem_bytes(int T, int H, int E) {
+    return router_tiny_stage_bytes(T, H, E) + router_tiny_x_bytes(T, H) + router_tiny_base_bytes();
 }
 
 // (one SM reads the whole router matrix: with 128 experts, 737 KB at
 // H = 2880, the multi-block router measured faster at T = 8)
 bool router_tiny_fits(int T, int H, int E) {
     return T >= 1 && T <= kTinyTokens && E <= 64 && H % 8 == 0 &&
-           router_tiny_smem_bytes(T, H) <= 96 * 1024;
+           router_tiny_x_bytes(T, H) + router_tiny_base_bytes() <= kTinySmemMax;
 }
 
 cudaError_t launch_router_tiny(const RouterParams& p, const void* x, const void* wr,
                                cudaStream_t s, bool pdl) {
     if (!router_tiny_fits(p.T, p.H, p.E) || !p.small_perm || p.nblocks != 1)
         return cudaErrorInvalidValue;
-    const size_t smem = router_tiny_smem_bytes(p.T, p.H);
+    const uint32_t wstage = static_cast<uint32_t>(router_tiny_stage_bytes(p.T, p.H, p.E));
+    const size_t smem = router_tiny_smem_bytes(p.T, p.H, p.E);
     cudaError_t err = cudaFuncSetAttribute(router_tiny_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
@@ -839,7 +955,7 @@ cudaError_t launch_router_tiny(const RouterParams& p, const void* x, const void*
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, router_tiny_kernel, p,
                               static_cast<const __nv_bfloat16*>(x),
-                              static_cast<const __nv_bfloat16*>(wr));
+                              static_cast<const __nv_bfloat16*>(wr), wstage);
 }
 
 size_t router_stage_bytes() { return kStageBytes; }

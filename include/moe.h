@@ -272,7 +272,12 @@ moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
  *                 multiple of 16 in [16, 256] (MXFP4 and MXFP4 x MXFP8
  *                 layers use at most 128);
  *   "pdl":        1 = launch dependent kernels with programmatic dependent
- *                 launch (default), 0 = plain stream order;
+ *                 launch (default), 0 = plain stream order.  With 1 the
+ *                 layer's kernels start reading weights (the router matrix,
+ *                 expert weights and their scales) before the work that
+ *                 precedes the call on the stream has finished: weights
+ *                 written by that work need 0 here or a synchronisation
+ *                 (an event the stream waits on) in between;
  *   "ksplit":     0 = split the GEMMs' K range when a small batch leaves
  *                 SMs idle (default), 1 = never split (every output then
  *                 sums its K range in one fixed order), 2..8 = split every

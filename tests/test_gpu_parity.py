@@ -720,6 +720,8 @@ SMALL_PATH_CASES = [
     (8, 1, 128, 128, 64),        # top-1, 64-row tiles (rows 32..63 of a tile)
     (256, 8, 128, 128, 32),      # R = 256, most experts
     (5, 3, 64, 64, 19),
+    (20, 4, 64, 64, 5),          # single-block router, matrix staged: a partial 16-expert tile
+    (64, 4, 128, 128, 8),        # ... four 16-expert tiles, eight tokens
 ]
 
 
