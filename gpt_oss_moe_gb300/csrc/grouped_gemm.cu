@@ -823,8 +823,10 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int half = (warp - 2) >> 2;         // this warp's share of the columns
         const int row_in_tile = quad * 32 + lane;
-        if (p.zero_out != nullptr) {
-            // the output rows the down projection will accumulate into
+        // the output rows the down projection will accumulate into (with
+        // bf16 weights and no gathering to do, the gather warp clears them
+        // in the background instead)
+        if (p.zero_out != nullptr && !(kGatherWarpOf<WF> >= 0 && p.gather_x == nullptr)) {
             float4* z = reinterpret_cast<float4*>(p.zero_out);
             for (size_t i = static_cast<size_t>(blockIdx.x) * kEpiThreads + ep; i < p.n_zero / 4;
                  i += static_cast<size_t>(gridDim.x) * kEpiThreads)
@@ -1078,6 +1080,14 @@ __global__ void __launch_bounds__(kThreadsOf<WF>, 1)
         // (The slot's own "gfull" barrier, not "full", takes the arrival, so
         // that "full" still tracks the TMA bytes alone for the producer's
         // bounded drain after an abort.)
+        if (p.gather_x == nullptr && p.zero_out != nullptr) {
+            // nothing to gather: this warp clears the output rows the down
+            // projection will accumulate into, alongside the pipeline
+            float4* z = reinterpret_cast<float4*>(p.zero_out);
+            for (size_t i = static_cast<size_t>(blockIdx.x) * 32 + lane; i < p.n_zero / 4;
+                 i += static_cast<size_t>(gridDim.x) * 32)
+                z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         if (p.gather_x != nullptr) {
             int stage = 0;
             uint32_t phase = 0;

@@ -659,11 +659,14 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     // round trip; gate_up clears the output rows)
     const bool small = g_small_path.load() != 0 && !mxfp4 && !fp8 && !mx && !pair &&
                        R <= kSmallPermRows && s.T <= kSmallPathMaxT && box <= 64 && stages > 4;
-    // deterministic combine: the ordered sum writes every output element,
-    // so the output needs no clearing
-    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r,
-                           det || small ? nullptr : out32, small ? nullptr : x_perm, box, dev,
-                           stream, ex_lo, ex_n, small));
+    // The output rows the down projection accumulates into are cleared by
+    // gate_up's epilogue warps, not by the permutation: at prefill the
+    // permutation is bound by its writes (the gathered rows), while gate_up
+    // is bound by the tensor cores (20b T=4096: 47 MB of zeros off the
+    // permutation's path).  The deterministic combine writes every output
+    // element, so its output needs no clearing.
+    MOE_TRY(launch_routing(s, L, ws, hidden, router_w, router_b, r, nullptr,
+                           small ? nullptr : x_perm, box, dev, stream, ex_lo, ex_n, small));
     // element type of the GEMM token operands: E4M3 codes (FP8, MXFP8) or bf16
     const int tok_dtype = (fp8 || mx) ? 2 : (mxfp4 && g_mxfp4_f16.load() != 0) ? 3 : 0;
     if (checks)
@@ -748,14 +751,14 @@ moe_status forward_impl(const moe_shape* shape, int ex_lo, int ex_n, const void*
     g.inject_stall = (g_inject.load() & 4) && !mxfp4 ? 1 : 0;
     // small batches: token rows gathered from the input; the tile list comes
     // from the router, the kernel just before, so nothing starts before the
-    // dependency wait; the output rows are cleared here
+    // dependency wait.  Every batch: the output rows are cleared here
     g.gather_x = small ? static_cast<const __nv_bfloat16*>(hidden) : nullptr;
     g.gather_K = s.H;
     // (the gather reads the permutation: row r of a tile is assignment
     // sorted_assign[r] of token sorted_assign[r] / top_k)
     g.sorted_assign = r.sorted_assign;
     g.top_k = s.top_k;
-    g.zero_out = small && !det ? out32 : nullptr;
+    g.zero_out = det ? nullptr : out32;
     g.n_zero = static_cast<size_t>(s.T) * s.H;
     g.prewait = small ? 0 : 1;
     {
