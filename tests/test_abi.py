@@ -204,6 +204,56 @@ def test_tuning_switches(moe):
             moe.moe_set_tuning("pair", v)
 
 
+# every switch with its accepted values (the default last) and values the
+# library must refuse without changing anything
+SWITCHES = {
+    "mxfp4_f16": ((0, 1), (-1, 2)),
+    "attn_tc": ((1, 2, 0), (-1, 3)),
+    "attn_poll": ((1, 0), (-1, 2)),
+    "tiny_router": ((0, 1), (-1, 2)),
+    "small_path": ((0, 1), (-1, 2)),
+    "inject": ((7, 1, 0), (-1, 8)),
+    "deterministic": ((1, 0), (-1, 2)),
+    "noalloc_poison": ((1, 0), (-1, 2)),
+}
+
+
+@pytest.mark.parametrize("key", sorted(SWITCHES))
+def test_switch_values(moe, key):
+    good, bad = SWITCHES[key]
+    for v in bad:
+        with pytest.raises(moe.MoEError):
+            moe.moe_set_tuning(key, v)
+    for v in good:
+        moe.moe_set_tuning(key, v)
+
+
+def test_attention_workspace_follows_the_kernel_choice(moe):
+    """The tcgen05 kernel (calls of 512 queries or more, or attn_tc 2) needs
+    only the 256-byte status word; the key-split kernel's workspace holds
+    its partial rows."""
+    L = moe.lib()
+
+    def ws(**kw):
+        d = dict(Tq=4, Tkv=4, Hq=8, Hkv=1, D=64, window=0, q_start=0)
+        d.update(kw)
+        sh = moe.moe_attn_shape(*[d[n] for n, _ in moe.moe_attn_shape._fields_])
+        return L.moe_attention_workspace_bytes(ctypes.byref(sh))
+    decode = dict(Tq=1, Tkv=4096, Hq=64, Hkv=8, q_start=4095)
+    prefill = dict(Tq=4096, Tkv=4096, Hq=64, Hkv=8)
+    try:
+        moe.moe_set_tuning("attn_tc", 0)
+        assert ws(**prefill) == 256
+        assert ws(**decode) > 256
+        moe.moe_set_tuning("attn_tc", 2)
+        assert ws(**decode) == 256
+        assert ws(Tq=0, Tkv=4, q_start=4) == 256
+        moe.moe_set_tuning("attn_tc", 1)
+        assert ws(**prefill) == 0          # the key-split kernel: no split at this size
+    finally:
+        moe.moe_set_tuning("attn_tc", 0)
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import gpt_oss_moe_gb300 as m
     monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
