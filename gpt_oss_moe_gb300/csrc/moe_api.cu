@@ -394,8 +394,12 @@ moe_status launch_routing(const moe_shape& s, const WsLayout& L, uint8_t* ws, co
     rp.sorted_assign = r.sorted_assign;
     rp.assign_row = reinterpret_cast<int32_t*>(ws + L.assign_row);
     rp.status = status;
-    if (small_perm && g_tiny_router.load() != 0 && router_tiny_fits(s.T, s.H, s.E)) {
+    // few tokens: the single-block router (a grid of 4-token blocks up to 64
+    // tokens when the router matrix can be staged in shared memory)
+    const int tiny_tb = g_tiny_router.load() != 0 ? router_tiny_tokens_per_cta(s.T, s.H, s.E) : 0;
+    if (tiny_tb > 0) {
         NvtxRange nv("moe.router_tiny");
+        rp.nblocks = (s.T + tiny_tb - 1) / tiny_tb;
         MOE_CUDA(launch_router_tiny(rp, hidden, router_w, stream, g_pdl.load() != 0));
     } else {
         NvtxRange nv("moe.router_topk");

@@ -383,6 +383,7 @@ cudaError_t launch_router(const RouterParams& p, const CUtensorMap* tmap_x,
                           const CUtensorMap* tmap_wr, size_t smem, cudaStream_t s, bool pdl);
 // Tiny batches (T <= 8, the small-batch path): one CTA routes everything.
 bool router_tiny_fits(int T, int H, int E);
+int router_tiny_tokens_per_cta(int T, int H, int E);
 cudaError_t launch_router_tiny(const RouterParams& p, const void* x, const void* wr,
                                cudaStream_t s, bool pdl);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s, bool pdl);

@@ -707,7 +707,16 @@ __global__ void __launch_bounds__(kThreads)
 // before this one (the weights are not written by it).
 constexpr int kTinyThreads = 512;
 constexpr int kTinyTokens = 8;
-constexpr size_t kTinySmemMax = 220 * 1024;
+constexpr size_t kTinySmemMax = 224 * 1024;
+// Batches of up to kTinyGridMaxT tokens whose router matrix can be staged
+// next to four token rows: a grid of CTAs of kTinyGridTokens tokens each,
+// every CTA staging the whole matrix before the wait; their counts are
+// added by the last CTA to finish (an atomic ticket), which then finishes
+// the tables as the single CTA does.
+constexpr int kTinyGridTokens = 4;
+constexpr int kTinyGridMaxT = 64;
+static_assert(64 * (kTinyGridMaxT / kTinyGridTokens) <= kMaxTokenBlocks,
+              "the grid's per-CTA counts must fit the token-block ticket area");
 
 // Rows in shared memory are H * 2 + 16 bytes apart, so that the eight rows
 // an ldmatrix reads at one column fall in different banks.
@@ -731,10 +740,13 @@ size_t router_tiny_stage_bytes(int T, int H, int E) {
 
 __global__ void __launch_bounds__(kTinyThreads, 1)
     router_tiny_kernel(const RouterParams p, const __nv_bfloat16* __restrict__ x,
-                       const __nv_bfloat16* __restrict__ wr, uint32_t wstage) {
+                       const __nv_bfloat16* __restrict__ wr, uint32_t wstage, int tb) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t wbar;
-    const int T = p.T, H = p.H, E = p.E;
+    __shared__ int last_cta;
+    // this CTA's tokens: [t0, t0 + T) of the batch (tb per CTA)
+    const int t0 = static_cast<int>(blockIdx.x) * tb;
+    const int T = min(tb, p.T - t0), H = p.H, E = p.E;
     const uint32_t rs = static_cast<uint32_t>(H) * 2u + 16u;               // padded row bytes
     uint8_t* w_s = smem_raw;                                                // [E][rs], staged
     uint8_t* x_s = smem_raw + wstage;                                       // [T + 1][rs]
@@ -747,7 +759,7 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     float* bias_s = reinterpret_cast<float*>(ids_s + kMaxExperts);           // [256]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 0);
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, blockIdx.x, 0);
     if (wstage && tid == 0) {
         // the router matrix, one bulk copy per expert row (16-byte multiples)
         mbar_init(smem_u32(&wbar), 1);
@@ -761,10 +773,10 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     // token rows, workspace and counters may be written by the kernel before
     pdl_wait();
     pdl_launch_dependents();
-    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 1);
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, blockIdx.x, 1);
 
     const int hv = H / 8;                                   // 16-byte vectors per row
-    const uint4* xg = reinterpret_cast<const uint4*>(x);
+    const uint4* xg = reinterpret_cast<const uint4*>(x) + static_cast<size_t>(t0) * hv;
     for (int e = tid; e < kMaxExperts; e += kTinyThreads) {
         hist[e] = 0;
         bias_s[e] = e < E ? __bfloat162float(p.br[e]) : 0.f;
@@ -784,7 +796,7 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
         staged = __syncthreads_and(mbar_wait(smem_u32(&wbar), 0, nullptr) ? 1 : 0) != 0;
         if (!staged && tid == 0) atomicOr(p.status, MOE_DEV_WAIT_TIMEOUT);
     }
-    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 2);
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, blockIdx.x, 2);
     constexpr int kWarps = kTinyThreads / 32;
     if (staged) {
         // logits on the tensor cores: D[expert][token] += W[expert][k] x[token][k]
@@ -902,24 +914,64 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
             }
     }
     }
-    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 6);
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, blockIdx.x, 6);
     __syncthreads();
-    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 3);
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, blockIdx.x, 3);
 
     switch (p.top_k) {
-        case 1: topk_warp<1>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
-        case 2: topk_warp<2>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
-        case 3: topk_warp<3>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
-        case 4: topk_warp<4>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
-        case 5: topk_warp<5>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
-        case 6: topk_warp<6>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
-        case 7: topk_warp<7>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
-        default: topk_warp<8>(p, logits, E, bias_s, 0, T, hist, ids_s); break;
+        case 1: topk_warp<1>(p, logits, E, bias_s, t0, T, hist, ids_s); break;
+        case 2: topk_warp<2>(p, logits, E, bias_s, t0, T, hist, ids_s); break;
+        case 3: topk_warp<3>(p, logits, E, bias_s, t0, T, hist, ids_s); break;
+        case 4: topk_warp<4>(p, logits, E, bias_s, t0, T, hist, ids_s); break;
+        case 5: topk_warp<5>(p, logits, E, bias_s, t0, T, hist, ids_s); break;
+        case 6: topk_warp<6>(p, logits, E, bias_s, t0, T, hist, ids_s); break;
+        case 7: topk_warp<7>(p, logits, E, bias_s, t0, T, hist, ids_s); break;
+        default: topk_warp<8>(p, logits, E, bias_s, t0, T, hist, ids_s); break;
     }
     __syncthreads();
-    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 4);
+    if (gridDim.x > 1) {
+        // This CTA's counts per expert and the totals; the last CTA to take a
+        // ticket adds the counts per 32-token block for the permutation
+        // kernel and finishes the tables.  The counts go to [E][CTAs] ints of
+        // the completion-counter block that the multi-block router keeps its
+        // per-token-block tickets in (unused by this router, zero between
+        // calls: the last CTA clears what it read).
+        const int nb = static_cast<int>(gridDim.x);
+        int32_t* cnt = p.counters + kPairSlots;
+        for (int e = tid; e < E; e += kTinyThreads) {
+            cnt[e * nb + blockIdx.x] = hist[e];
+            if (hist[e] != 0) atomicAdd(p.counters + kExpertTotalsOffset + e, hist[e]);
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) last_cta = atomicAdd(p.status + kGridCounterWord, 1) == nb - 1;
+        __syncthreads();
+        if (!last_cta) return;   // block-uniform
+        __threadfence();
+        const int R = p.T * p.top_k;
+        if (p.small_perm) {
+            // every token's ids (this CTA's own among them) from global memory
+            for (int a = tid; a < R; a += kTinyThreads) ids_s[a] = __ldcg(p.topk_ids + a);
+        } else {
+            const int nb32 = (p.T + kRouterTokens - 1) / kRouterTokens;
+            const int per32 = kRouterTokens / tb;      // router CTAs per 32-token block
+            for (int i = tid; i < E * nb32; i += kTinyThreads) {
+                const int e = i / nb32, b = i - e * nb32;
+                int c_sum = 0;
+                for (int c = b * per32; c < min(nb, (b + 1) * per32); ++c)
+                    c_sum += __ldcg(cnt + e * nb + c);
+                p.blk_cnt[e * nb32 + b] = c_sum;
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < E * nb; i += kTinyThreads) cnt[i] = 0;
+    } else if (!p.small_perm) {
+        // one CTA, one 32-token block: its counts for the permutation kernel
+        for (int e = tid; e < E; e += kTinyThreads) p.blk_cnt[e] = hist[e];
+    }
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, blockIdx.x, 4);
     finish_routing<kTinyThreads>(p, hist, scan_a, scan_b, scan_c, ids_s);
-    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, 0, 5);
+    if (tid == 0) MOE_TRACE_POINT(g_trace_router, 0, blockIdx.x, 5);
 }
 
 size_t router_tiny_smem_bytes(int T, int H, int E) {
@@ -928,23 +980,32 @@ size_t router_tiny_smem_bytes(int T, int H, int E) {
 
 // (one SM reads the whole router matrix: with 128 experts, 737 KB at
 // H = 2880, the multi-block router measured faster at T = 8)
-bool router_tiny_fits(int T, int H, int E) {
-    return T >= 1 && T <= kTinyTokens && E <= 64 && H % 8 == 0 &&
-           router_tiny_x_bytes(T, H) + router_tiny_base_bytes() <= kTinySmemMax;
+// tokens per CTA of the single-block router for a batch of T (0: not used)
+int router_tiny_tokens_per_cta(int T, int H, int E) {
+    if (T < 1 || E > 64 || H % 8 != 0) return 0;
+    if (T <= kTinyTokens)
+        return router_tiny_x_bytes(T, H) + router_tiny_base_bytes() <= kTinySmemMax ? T : 0;
+    // larger batches only with the router matrix staged
+    if (T <= kTinyGridMaxT && router_tiny_stage_bytes(kTinyGridTokens, H, E) > 0)
+        return kTinyGridTokens;
+    return 0;
 }
+
+bool router_tiny_fits(int T, int H, int E) { return router_tiny_tokens_per_cta(T, H, E) > 0; }
 
 cudaError_t launch_router_tiny(const RouterParams& p, const void* x, const void* wr,
                                cudaStream_t s, bool pdl) {
-    if (!router_tiny_fits(p.T, p.H, p.E) || !p.small_perm || p.nblocks != 1)
-        return cudaErrorInvalidValue;
-    const uint32_t wstage = static_cast<uint32_t>(router_tiny_stage_bytes(p.T, p.H, p.E));
-    const size_t smem = router_tiny_smem_bytes(p.T, p.H, p.E);
+    const int tb = router_tiny_tokens_per_cta(p.T, p.H, p.E);
+    const int nb = tb > 0 ? (p.T + tb - 1) / tb : 0;
+    if (tb == 0 || p.nblocks != nb) return cudaErrorInvalidValue;
+    const uint32_t wstage = static_cast<uint32_t>(router_tiny_stage_bytes(tb, p.H, p.E));
+    const size_t smem = router_tiny_smem_bytes(tb, p.H, p.E);
     cudaError_t err = cudaFuncSetAttribute(router_tiny_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1);
+    cfg.gridDim = dim3(nb);
     cfg.blockDim = dim3(kTinyThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -955,7 +1016,7 @@ cudaError_t launch_router_tiny(const RouterParams& p, const void* x, const void*
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, router_tiny_kernel, p,
                               static_cast<const __nv_bfloat16*>(x),
-                              static_cast<const __nv_bfloat16*>(wr), wstage);
+                              static_cast<const __nv_bfloat16*>(wr), wstage, tb);
 }
 
 size_t router_stage_bytes() { return kStageBytes; }

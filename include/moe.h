@@ -311,10 +311,12 @@ moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
  *   "attn_poll":  softmax hand-off waits of the tcgen05 attention kernel:
  *                 0 = suspending try_wait (default), 1 = poll
  *                 (mbarrier.test_wait);
- *   "tiny_router": 1 = small-batch calls of at most 8 tokens and at most
- *                 64 experts compute the
- *                 router, top-k and permutation in one thread block
- *                 (default); 0 = the multi-block router;
+ *   "tiny_router": 1 = calls of at most 8 tokens and at most 64 experts
+ *                 route in one thread block (with the permutation on the
+ *                 small-batch path), and calls of 9 to 64 tokens whose
+ *                 router matrix fits in shared memory beside four token
+ *                 rows in a grid of 4-token blocks (default); 0 = the
+ *                 multi-block router;
  *   "inject":     test faults that the device status word must report, as
  *                 a bit mask (0 = none, default): 1 = token 0's first
  *                 routed id is written as E (after it was counted), so the
