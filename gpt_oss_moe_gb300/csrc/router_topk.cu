@@ -982,7 +982,10 @@ size_t router_tiny_smem_bytes(int T, int H, int E) {
 // H = 2880, the multi-block router measured faster at T = 8)
 // tokens per CTA of the single-block router for a batch of T (0: not used)
 int router_tiny_tokens_per_cta(int T, int H, int E) {
-    if (T < 1 || E > 64 || H % 8 != 0) return 0;
+    // (one SM reads the whole matrix: with 128 experts, 737 KB at H = 2880,
+    // it wins at T <= 2 -- 120b shape, T = 1: 59.3 -> 57.9 us per layer --
+    // and the multi-block router at T = 8)
+    if (T < 1 || E > (T <= 2 ? 128 : 64) || H % 8 != 0) return 0;
     if (T <= kTinyTokens)
         return router_tiny_x_bytes(T, H) + router_tiny_base_bytes() <= kTinySmemMax ? T : 0;
     // larger batches only with the router matrix staged

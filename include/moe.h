@@ -312,7 +312,7 @@ moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
  *                 0 = suspending try_wait (default), 1 = poll
  *                 (mbarrier.test_wait);
  *   "tiny_router": 1 = calls of at most 8 tokens and at most 64 experts
- *                 route in one thread block (with the permutation on the
+ *                 (at most 2 tokens: 128 experts) route in one thread block (with the permutation on the
  *                 small-batch path), and calls of 9 to 64 tokens whose
  *                 router matrix fits in shared memory beside four token
  *                 rows in a grid of 4-token blocks (default); 0 = the

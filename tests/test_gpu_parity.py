@@ -720,7 +720,9 @@ SMALL_PATH_CASES = [
     (8, 1, 128, 128, 64),        # top-1, 64-row tiles (rows 32..63 of a tile)
     (256, 8, 128, 128, 32),      # R = 256, most experts
     (5, 3, 64, 64, 19),
+    (128, 4, 2880, 2880, 2),     # single-block router with 128 experts (matrix read from global)
     (20, 4, 64, 64, 5),          # single-block router, matrix staged: a partial 16-expert tile
+    (32, 4, 2880, 2880, 48),     # grid of 4-token router blocks beside the permutation kernel
     (64, 4, 128, 128, 8),        # ... four 16-expert tiles, eight tokens
 ]
 
