@@ -237,10 +237,11 @@ struct RouterParams {
 };
 // Largest T * top_k whose permutation the router's last CTA makes itself,
 // and the largest T of that path (measured on gpt-oss-20b: 5-10 us faster
-// at T = 16 and 32, 4 us slower at T = 64, where gate_up cannot load
-// weights before the router, its immediate predecessor, has finished).
+// at T = 16 and 32, 6.4 us faster at T = 48, 4 us slower at T = 64, where
+// gate_up cannot load weights before the router, its immediate
+// predecessor, has finished).
 constexpr int kSmallPermRows = 256;
-constexpr int kSmallPathMaxT = 32;
+constexpr int kSmallPathMaxT = 48;
 
 // ------------------------------------------------------------ permutation (K2)
 

@@ -299,7 +299,7 @@ moe_status moe_trace_read(uint64_t* out, size_t cap, size_t* count);
  *                 value outside is clamped and MOE_DEV_RANGE reported
  *                 (default); 0 = bf16 operands, exact for every scale;
  *   "small_path": 1 = batches of bf16 weights with T * top_k <= 256 (and
- *                 T <= 32) skip the permutation kernel: the router's last
+ *                 T <= 48) skip the permutation kernel: the router's last
  *                 block computes the permutation and the gate_up GEMM copies
  *                 its token rows from `hidden` itself (default); 0 = always
  *                 the permutation kernel and the gathered activation rows;
