@@ -4,7 +4,10 @@
 // one sink logit per head, GQA 64 / 8 heads of dim 64; §3 on the fully
 // masked tile of a sliding window).
 //
-// One CTA per (128 query rows, query head).  The key tiles of 128 keys are
+// One CTA per (128 query rows, query head); the blocks start with every head
+// of the query block that sees the most keys (the last, under causality),
+// then the next, so that the longest blocks do not end the launch.  The
+// key tiles of 128 keys are
 // dealt alternately to two softmax groups, each with its own running max,
 // sum and output accumulator, merged once at the end (the same online-
 // softmax merge as a split over keys): while one group works on its scores
@@ -23,11 +26,12 @@
 //   warps 2..5  softmax group 0 (tiles 0, 2, 4, ...), warps 6..9 group 1
 //               (tiles 1, 3, 5, ...): one query row per thread (its TMEM
 //               lane), all 128 scores of a tile: the row maximum, P =
-//               exp2(scaled, masked score - m) as bf16 pairs into TMEM.  The
-//               reference max m is raised (and O_g, held in TMEM, rescaled
-//               by the thread that owns the row) only when a tile's maximum
-//               exceeds it by more than 2^8, so P stays below 256 and the
-//               rescale is rare once the row's maximum has settled.
+//               exp2(scaled, masked score - m) as bf16 pairs into TMEM.
+//               When a tile raises the row's running max m, the thread that
+//               owns the row rescales its row of O_g (held in TMEM) before
+//               the next product adds to it (kRescaleLog2 = 0: m stays the
+//               exact running max, so the row's largest weight is exactly 1
+//               in bf16).
 // The sink is the starting reference max with one unit in group 0's sum, so
 // it weighs in the softmax and carries no value.  A row with no visible key
 // yet keeps a reference of -inf and weights of zero: the guard whose absence
