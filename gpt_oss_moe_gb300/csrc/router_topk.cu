@@ -687,24 +687,25 @@ __global__ void __launch_bounds__(kThreads)
 // ------------------------------------------------------------ tiny batches
 //
 // Batches of at most kTinyTokens tokens: one CTA of kTinyThreads threads
-// does the whole routing.  Warp w computes the logits of experts 2w, 2w + 1,
-// then 2w + 32, ...: each lane loads its share of both experts' router rows
-// (16-byte loads, six per row in flight) and of the token rows (L1 hits)
-// and accumulates, per token, sequential fp32 sums over its share, which a
-// warp reduction then adds (a fixed order: the same logits every run; the
-// tensor-core router's order differs, as any two sum orders may, in the
-// last bits).  The top k (a warp per token), the expert offsets, the GEMM
-// tiles and the stable permutation follow in the same CTA, with no ticket or
-// merge between CTAs.  Measured on GB300 at gpt-oss-20b, T = 1: the
-// multi-CTA router spent ~11 us from its dependency wait to the finished
-// tables, mostly in hand-offs between its phases.
+// does the whole routing -- the logits, the top k (a warp per token), the
+// expert offsets, the GEMM tiles and, on the small-batch path, the stable
+// permutation -- with no ticket or merge between CTAs.  Measured on GB300 at
+// gpt-oss-20b, T = 1: the multi-CTA router spent ~11 us from its dependency
+// wait to the finished tables, mostly in hand-offs between its phases.
 //
 // The token rows are copied to shared memory first, by every thread at once
 // (read in the dot-product loop, each load waited for in turn, they cost
 // ~5 us of dependent L2 round trips at T = 1).  When the router matrix also
 // fits (gpt-oss-20b: 32 x 2880 bf16, 184 KB) it is copied there by bulk
 // copies issued before the dependency wait, so its load overlaps the kernel
-// before this one (the weights are not written by it).
+// before this one (the weights are not written by it), and the logits are
+// an mma.sync contraction: warp w takes the 16-wide K steps w, w + 16, ...
+// of every 16-expert tile, and the warps' partial tiles are added in warp
+// order.  Otherwise warp w computes the logits of experts 2w, 2w + 1, then
+// 2w + 32, ... with fp32 FMAs over its lanes' shares of both rows (every
+// load of a pass issued before the first multiply) and a warp reduction.
+// Either way the order is fixed (the same logits every run); the other
+// routers' orders differ, as any two sum orders may, in the last bits.
 constexpr int kTinyThreads = 512;
 constexpr int kTinyTokens = 8;
 constexpr size_t kTinySmemMax = 224 * 1024;
