@@ -97,8 +97,10 @@ constexpr int kMxScaleWarps = 4;        // MXFP4 x MXFP8: warps 6..9 write the s
 // (their other warps convert or write scales).
 template <int WF>
 constexpr int kEpiWarps = (WF == 0 || WF == 2) ? 8 : 4;
-// bf16 kernels: one more warp gathers token rows from the layer input for
-// small batches (GemmParams::gather_x), the last warp of the CTA.
+// bf16 kernels: one more warp, the last of the CTA, gathers token rows from
+// the layer input for small batches (GemmParams::gather_x); in gate_up
+// without gathering it clears the output rows the down projection
+// accumulates into (GemmParams::zero_out), alongside the pipeline.
 template <int WF>
 constexpr int kGatherWarpOf = WF == 0 ? 2 + kEpiWarps<WF> : -1;
 template <int WF>
